@@ -1,0 +1,213 @@
+/*
+ * kivi.h - C ABI of a KIVI-style low-bit KV cache with single-query decode
+ * attention, for NVIDIA GB300 (sm_103a).
+ *
+ * The method (three web pages describe it):
+ *   [explainer]  KIVI explainer, discosf.com/news/3594501, sections 2.1-3.2, 5.2
+ *   [axis-guide] "KV cache quantization axis selection guide", unite.ai
+ *   [survey]     "3.2.3 KV Cache Quantization", blog.csdn.net
+ *
+ *   - Keys are quantized per channel over groups of G consecutive tokens;
+ *     values per token over groups of G consecutive channels ([axis-guide]
+ *     "keys: outliers sit in fixed channels" and "values: where intuition
+ *     breaks"; [explainer] 3.1 pseudo-code; [survey]).
+ *   - Each group is quantized uniformly and asymmetrically to B bits: the
+ *     zero point is the group minimum, the step is (max - min) / (2^B - 1),
+ *     every element goes to the nearest step ([axis-guide] "what
+ *     quantization error is made of").  The exact arithmetic is:
+ *         mn, mx   = group min / max (fp16 values, taken exactly; -0 -> +0)
+ *         z        = (fp16) mn
+ *         s        = (fp16) ((fp32)(mx - mn) / (2^B - 1))        IEEE fp32, RN
+ *         code(x)  = s == 0 ? 0 : clamp(rint(((fp32)x - z) / s), 0, 2^B - 1)
+ *         x_hat    = code * s + z
+ *     each fp32 operation rounded to nearest-even separately (no FMA); the
+ *     rint tie rule is ties-to-even.
+ *   - The newest tokens (at most R) stay in an fp16 residual window; when the
+ *     window is full it is quantized as one batch and emptied ([explainer]
+ *     3.1, [axis-guide] "the system tax").  A prompt of L tokens keeps
+ *     Lq = G * ceil(max(L - R, 0) / G) tokens quantized and r = L - Lq in the
+ *     residual; an append that finds r == R first flushes all R residual
+ *     tokens (keys and values together), then stores the new token.
+ *   - Decode attention reads every cached token for each new query
+ *     ([axis-guide] "why the KV cache is the problem"):
+ *         o = sum_t softmax_t(scale * q . k_hat_t) * v_hat_t,
+ *     scale = 1/sqrt(D) by default, no mask, query head h reads kv head
+ *     h / (Hq / Hkv).  Accumulation is fp32; the output is fp16.
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device addresses on the current device.  The
+ *     caller allocates and owns ALL device memory: the cache buffer, inputs,
+ *     outputs and workspace.  The library owns only the small host handle.
+ *   - Calls that take a stream enqueue kernels on it and return without
+ *     synchronizing.  Token counts live on the host handle, so no call reads
+ *     device memory back.  Buffers passed in must stay valid until the
+ *     enqueued work finishes.
+ *   - All tensors are fp16, dense, row-major, 16-byte aligned.
+ *   - Errors are return codes; nothing is launched when a call fails its
+ *     checks, and the handle's state is then unchanged.  A failed launch
+ *     returns KIVI_ERR_CUDA.  kivi_last_error_string() describes the last
+ *     failure on the calling thread.
+ *   - One handle must not be used from two threads at once.  One handle is
+ *     one layer's cache; a model with several layers uses several handles.
+ *   - There is no CPU fallback: every computation runs in the library's
+ *     sm_103a kernels.
+ */
+#ifndef KIVI_H
+#define KIVI_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t); NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* kivi_stream_t;
+
+typedef enum {
+    KIVI_OK = 0,
+    KIVI_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, bad size or config */
+    KIVI_ERR_UNSUPPORTED = 2,   /* valid in principle, not built (e.g. head_dim 96) */
+    KIVI_ERR_CAPACITY = 3,      /* the cache or workspace is too small */
+    KIVI_ERR_STATE = 4,         /* call out of order (prefill twice, decode on empty) */
+    KIVI_ERR_CUDA = 5           /* a CUDA call failed; see kivi_last_error_string() */
+} kivi_status;
+
+/*
+ * Cache shape.  Supported: bits in {2, 4}; head_dim in {64, 128};
+ * group in {32, 64, 128} with head_dim % group == 0 (value groups) and
+ * residual % group == 0, residual >= group; n_q_heads / n_kv_heads in
+ * {1, 2, 4}; max_tokens >= 1 is the most tokens (quantized + residual) one
+ * sequence may hold.  All sequences of the batch have the same length.
+ * Typical group sizes 32-128 and residual lengths 64-128 follow
+ * [explainer] 5.2.
+ */
+typedef struct {
+    int batch;
+    int n_q_heads;
+    int n_kv_heads;
+    int head_dim;
+    int bits;
+    int group;
+    int residual;
+    long long max_tokens;
+} kivi_config;
+
+/*
+ * Byte layout of the cache buffer (all offsets from the buffer start).
+ *
+ *   NB   = floor(max_tokens / G)      quantized blocks per (batch, kv-head) slot
+ *   TILE = 2 * D * bits               bytes of one 16-token code tile
+ *   PART = (G / 16) * TILE + 4 * D    bytes of one block's key part or value part
+ *
+ *   blocks  : [B][Hkv][2][NB][PART] at offset 0; index 2: 0 = keys, 1 = values
+ *   k_resid : [B][Hkv][R][D] fp16 at k_resid_offset
+ *   v_resid : [B][Hkv][R][D] fp16 at v_resid_offset
+ *
+ * Block n of a slot holds that slot's tokens [n*G, (n+1)*G).  Residual row j
+ * holds token Lq + j.
+ *   key part  : G/16 code tiles (tokens in order), then D entries (s, z);
+ *               entry c is the step and zero of channel c over the block.
+ *   value part: G/16 code tiles, then G*(D/G) entries (s, z); entry
+ *               t*(D/G) + j is the step and zero of the block's token t over
+ *               channels [j*G, (j+1)*G).
+ *   An entry (s, z) is two fp16: s at bytes 0-1, z at bytes 2-3.
+ *
+ * Code tile: 16 tokens x D channels of b-bit codes in D*b/2 little-endian
+ * 32-bit words.  Lane l (0..31) owns words [l*W, (l+1)*W), W = D*b/64.
+ * Write l = 4*g + i.  The lane's D/4 code pairs are numbered p = 0..D/4-1;
+ * pair p is in the lane's word p / (16/b), slot u = p % (16/b): its first
+ * code at bits [b*u, b*u + b), its second at bits [16 + b*u, 16 + b*u + b).
+ * With k = p / 4 and r = p % 4:
+ *   key tile  : both codes are token g + 8*(r%2); the first is channel
+ *               16k + 2i + 8*(r/2), the second the next channel.
+ *   value tile: both codes are channel 16k + g + 8*(r%2); the first is token
+ *               2i + 8*(r/2), the second the next token.
+ * (Each lane's words are thereby the fragments of a 16x16 fp16 A operand of
+ * an m16n8k16 MMA: keys as [token][channel], values as [channel][token].)
+ */
+typedef struct {
+    size_t total_bytes;       /* == kivi_cache_bytes() */
+    long long blocks_per_slot;/* NB */
+    size_t tile_bytes;        /* TILE */
+    size_t part_bytes;        /* PART */
+    size_t slot_bytes;        /* 2 * NB * PART: one (batch, kv-head) slot */
+    size_t k_resid_offset;    /* 256-byte aligned */
+    size_t v_resid_offset;    /* 256-byte aligned */
+    size_t resid_slot_bytes;  /* R * D * 2: one slot's residual rows */
+} kivi_layout;
+
+typedef struct kivi_cache* kivi_cache_t;
+
+/* Bytes of device memory a cache of this shape needs; 0 if cfg is invalid.
+ * Host-only. */
+size_t kivi_cache_bytes(const kivi_config* cfg);
+
+/* Fill *out with the buffer layout described above.  Host-only.
+ * KIVI_ERR_INVALID_ARG / KIVI_ERR_UNSUPPORTED for a bad config. */
+kivi_status kivi_cache_layout(const kivi_config* cfg, kivi_layout* out);
+
+/* Create a handle over the caller's device buffer dev_buf (256-byte aligned,
+ * at least kivi_cache_bytes(cfg) bytes; the contents need no initialization).
+ * The cache starts empty.  Host-only: no CUDA call is made.  The buffer stays
+ * owned by the caller and must outlive the handle. */
+kivi_status kivi_cache_create(const kivi_config* cfg, void* dev_buf, size_t bytes,
+                              kivi_cache_t* out);
+
+/* Free the host handle (not the buffer).  Work already enqueued is unaffected. */
+kivi_status kivi_cache_destroy(kivi_cache_t cache);
+
+/* Forget all cached tokens (host counters only; no device work). */
+kivi_status kivi_cache_reset(kivi_cache_t cache);
+
+/* Token counts: *n_quant = Lq (quantized), *n_resid = r (fp16 residual). */
+kivi_status kivi_cache_counts(kivi_cache_t cache, long long* n_quant, long long* n_resid);
+
+/*
+ * Prefill ([explainer] 3.1): K, V are fp16 [B][Hkv][L][D] device tensors.
+ * Quantizes tokens [0, Lq) into blocks and copies tokens [Lq, L) bit for bit
+ * into the residual, Lq = G * ceil(max(L - R, 0) / G).  Only on an empty
+ * cache (KIVI_ERR_STATE otherwise); L may be 0.  KIVI_ERR_CAPACITY if
+ * L > max_tokens.
+ */
+kivi_status kivi_prefill(kivi_cache_t cache, const void* K, const void* V, long long L,
+                         kivi_stream_t stream);
+
+/*
+ * Append one token ([explainer] 3.1, [axis-guide] "the system tax"): k, v are
+ * fp16 [B][Hkv][D] device tensors.  If the residual holds R tokens they are
+ * first quantized into blocks (R/G key groups, R value tokens) and the
+ * residual is emptied; then k, v become the newest residual row.
+ * KIVI_ERR_CAPACITY if the cache already holds max_tokens tokens.
+ */
+kivi_status kivi_append(kivi_cache_t cache, const void* k, const void* v,
+                        kivi_stream_t stream);
+
+/* Bytes of decode workspace needed for any context of this shape on any
+ * device; 0 if cfg is invalid.  Host-only. */
+size_t kivi_decode_workspace_bytes(const kivi_config* cfg);
+
+/*
+ * Decode attention ([axis-guide] "why the KV cache is the problem", "values:
+ * where intuition breaks"): q fp16 [B][Hq][D] device tensor; out fp16
+ * [B][Hq][D] device tensor.  softmax_scale <= 0 selects 1/sqrt(D).
+ * workspace: device scratch of ws_bytes >= kivi_decode_workspace_bytes(cfg)
+ * bytes, 256-byte aligned; its contents need no initialization and are
+ * garbage afterwards.  Reads all Lq + r cached tokens.  KIVI_ERR_STATE on an
+ * empty cache; KIVI_ERR_CAPACITY if ws_bytes is too small.
+ */
+kivi_status kivi_decode_attn(kivi_cache_t cache, const void* q, void* out, float softmax_scale,
+                             void* workspace, size_t ws_bytes, kivi_stream_t stream);
+
+/* Description of the last failure on the calling thread ("" if none). */
+const char* kivi_last_error_string(void);
+
+/* Number of kernel launches this library has issued in this process. */
+unsigned long long kivi_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KIVI_H */
