@@ -1,0 +1,451 @@
+"""Benchmark of the KIVI KV-cache decode path on GB300.
+
+One step = one pass of the whole path over a batch of synthetic input: for
+each rotated layer cache, prefill the prompt (quantize + residual), then for
+every decode step and layer append one token (flushing the residual when
+full) and run decode attention.  The step is replayed as a CUDA graph; the
+value is decode-attention KV tokens per second (batch rows x attended tokens,
+summed over layers and decode calls) over the whole step time.
+
+Also measured in the same run:
+  roofline     decode calls replayed back to back (graph), average duration per
+               call, algorithmic bytes per call (codes, steps/zeros, fp16
+               residual, q, out) / duration, against the measured HBM copy
+               bandwidth;
+  e2e          the same step through the Python API with inputs copied from
+               pinned host memory each step and outputs copied back;
+  cpu_baseline the CPU oracle on a bounded sample of the same workload;
+  clocks       nvidia-smi samples taken during the timed region.
+
+--impl reference times the CPU oracle alone (the reference implementation
+of the method), on this arm's workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV tokens/s and HBM GB/s vs ~8 TB/s peak (2-bit, Llama-2-7B shape)"
+UNIT = "KV tokens/s"
+
+# name -> shape and call sequence (layers = distinct caches rotated in a step)
+WORKLOADS = {
+    "tiny-b1h1d64": dict(B=1, Hq=1, Hkv=1, D=64, bits=2, G=32, R=32, prompt=256, decode=1, layers=1,
+                         outliers="fixed4x20", sink=False, seed=1000),
+    "llama2-7b-layer": dict(B=8, Hq=32, Hkv=32, D=128, bits=2, G=32, R=128, prompt=4096, decode=64,
+                            layers=4, outliers="range", sink=True, seed=1001),
+    "llama2-13b-40layer": dict(B=32, Hq=40, Hkv=40, D=128, bits=2, G=32, R=128, prompt=4096, decode=1,
+                               layers=40, outliers="range", sink=True, seed=1002),
+    "llama3-8b-gqa": dict(B=64, Hq=32, Hkv=8, D=128, bits=4, G=128, R=128, prompt=8192, decode=20,
+                          layers=2, outliers="range", sink=True, seed=1003),
+    "long-context": dict(B=2, Hq=32, Hkv=32, D=128, bits=2, G=32, R=128, prompt=131072, decode=512,
+                         layers=1, outliers="range", sink=True, seed=1004),
+}
+DEFAULT = "llama2-7b-layer"
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _prefill_split(L, G, R):
+    over = max(L - R, 0)
+    Lq = G * ((over + G - 1) // G)
+    return Lq, L - Lq
+
+
+def _call_counts(w):
+    """Per decode call: (n_quant, n_resid) after its append, for one layer."""
+    Lq, r = _prefill_split(w["prompt"], w["G"], w["R"])
+    out = []
+    for _ in range(w["decode"]):
+        if r == w["R"]:
+            Lq, r = Lq + w["R"], 0
+        r += 1
+        out.append((Lq, r))
+    return out
+
+
+def _bytes_per_call(w, Lq, r):
+    per_tok = 2 * (w["D"] * w["bits"] // 8) + 2 * (4 * w["D"] // w["G"])
+    return w["B"] * w["Hkv"] * (Lq * per_tok + r * 4 * w["D"]) + 2 * w["B"] * w["Hq"] * w["D"] * 2
+
+
+def _kv_tokens_per_step(w):
+    return w["layers"] * w["B"] * sum(Lq + r for Lq, r in _call_counts(w))
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks ----
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import torch
+        uid = str(getattr(torch.cuda.get_device_properties(device), "uuid", ""))
+        self.dev = uid if uid.startswith("GPU-") else (f"GPU-{uid}" if uid else str(device.index or 0))
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [ln.strip().split(", ") for ln in f if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ oracle (CPU) ----
+def oracle_sample(w, n_slots=None, budget_s=15.0, step_seed=0):
+    """Run the CPU oracle on whole (batch, kv-head) slots of the workload.
+
+    Each slot: prefill the prompt, then every decode step append + attention
+    for the slot's query heads.  Stops after budget_s seconds (at least one
+    slot).  Returns (kv_tokens_equivalent, seconds, slots_done).
+    One KV token of the metric covers all Hkv heads of a batch row, so a
+    single slot contributes its attended tokens / Hkv.
+    """
+    import numpy as np
+    import torch
+    from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV
+    from oracle.attention import decode_attention
+    from oracle.cache import OracleCache
+
+    outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
+    syn = SynthKV(1, w["Hq"] // w["Hkv"], 1, w["D"], seed=w["seed"] + step_seed, outliers=outl,
+                  sink=w["sink"], device="cpu")
+    K, V = syn.prompt(w["prompt"])
+    Kn, Vn = K.numpy(), V.numpy()
+    steps = [tuple(t.numpy() for t in syn.step(s)) for s in range(w["decode"])]
+    t0 = time.perf_counter()
+    done, tokens = 0, 0
+    while True:
+        oc = OracleCache(1, 1, w["D"], w["bits"], w["G"], w["R"])
+        oc.prefill(Kn, Vn)
+        for (q, k, v) in steps:
+            oc.append(k, v)
+            decode_attention(q, oc.keys_hat(), oc.values_hat())
+            tokens += oc.n_quant + oc.n_resid
+        done += 1
+        el = time.perf_counter() - t0
+        if (n_slots is not None and done >= n_slots) or (n_slots is None and el >= budget_s):
+            break
+    return tokens / w["Hkv"], time.perf_counter() - t0, done
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(w, n_slots=1)
+    tok, secs = 0.0, 0.0
+    for s in range(args.steps):
+        t, sec, _ = oracle_sample(w, n_slots=1, step_seed=s)
+        tok += t
+        secs += sec
+    value = tok / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w, args.workload),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"per step one (batch, kv-head) slot of {args.workload}: prefill "
+                                   f"{w['prompt']} + {w['decode']} x (append + attention); "
+                                   f"KV tokens counted per slot / {w['Hkv']} heads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, name):
+    return {"workload": name, "batch": w["B"], "q_heads": w["Hq"], "kv_heads": w["Hkv"],
+            "head_dim": w["D"], "bits": w["bits"], "group": w["G"], "residual": w["R"],
+            "prompt": w["prompt"], "decode_steps": w["decode"], "layers_rotated": w["layers"]}
+
+
+# --------------------------------------------------------------- GPU arm ----
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    from bit_kivi_kv_gb300 import build as _b
+    _b.build()
+    from bit_kivi_kv_gb300 import kivi as K
+    from bit_kivi_kv_gb300.kivi import KiviCache
+    from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV
+
+    outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
+    NL, S = w["layers"], w["decode"]
+    max_tokens = w["prompt"] + S
+    caches, prompts, steps = [], [], []
+    for li in range(NL):
+        syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=w["seed"] + 7919 * li + 104729 * rank,
+                      outliers=outl, sink=w["sink"], device=dev)
+        prompts.append(syn.prompt(w["prompt"]))
+        steps.append([syn.step(s) for s in range(S)])
+        caches.append(KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], max_tokens,
+                                device=dev))
+    outs = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
+
+    def step():
+        for li in range(NL):
+            caches[li].reset()
+            caches[li].prefill(*prompts[li])
+        for s in range(S):
+            for li in range(NL):
+                q, k, v = steps[li][s]
+                caches[li].append(k, v)
+                caches[li].decode_attn(q, out=outs[li])
+
+    def decode_only():
+        for li in range(NL):
+            caches[li].decode_attn(steps[li][S - 1][0], out=outs[li])
+
+    # eager warm-up (also the first device query), then capture
+    step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g_step, stream=stream):
+            step()
+        decode_only()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g_dec, stream=stream):
+            for _ in range(8):
+                decode_only()
+    launches_per_step = None
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        g_step.replay()
+    barrier()
+    n0 = K.kivi_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                g_step.replay()
+        ev1.record(stream)
+        barrier()
+    ms = ev0.elapsed_time(ev1)
+    # kernels launched per step = the launches the captured step issued
+    launches_per_step = _launches_in(step, K, stream, torch)
+    gpu_launches = launches_per_step * args.steps
+    clocks = clk.summary()
+    t_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    tokens_step = _kv_tokens_per_step(w)
+    value = world * tokens_step * args.steps / (t_max / 1e3)
+
+    # ---- roofline: decode calls back to back (graph), rotated across layers ----
+    reps = max(4, int(200 / max(NL * 8, 1)))
+    for _ in range(3):
+        g_dec.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g_dec.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    calls = reps * 8 * NL
+    dec_ms = e0.elapsed_time(e1) / calls
+    Lq_last, r_last = _call_counts(w)[-1]
+    bytes_call = _bytes_per_call(w, Lq_last, r_last)
+    achieved = bytes_call / (dec_ms / 1e3) / 1e9
+    peak, peak_kind = _peaks()
+    traffic = _profile_traffic(args.workload)
+
+    # ---- e2e through the Python API from pinned host memory ----
+    e2e = _e2e(args, w, caches, prompts, steps, torch, dev)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; key outlier channels, attention sink)",
+        "config": dict(_config(w, args.workload), parallelism=f"replicas x{world}",
+                       l2="inputs larger than L2: each step rotates layer caches "
+                          f"({NL} x ~{bytes_call / 1e6:.0f} MB read per decode round)"),
+        "decode_call": {"us": dec_ms * 1e3, "bytes": bytes_call, "gbs": achieved,
+                        "kv_tokens_per_s": w["B"] * (Lq_last + r_last) / (dec_ms / 1e3),
+                        "steps_per_s": 1e3 / dec_ms},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "decode attention call "
+                     "(split-KV kernel + log-sum-exp combine)"},
+        "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, secs, done = oracle_sample(w, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {
+            "value": tok / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} (batch, kv-head) slot(s) of {args.workload}: prefill {w['prompt']} + "
+                      f"{w['decode']} x (append + fp64 attention), {secs:.1f} s; KV tokens per slot "
+                      f"counted / {w['Hkv']} heads"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _launches_in(step, K, stream, torch):
+    """Kernel launches one eager step issues (the captured graph holds the same kernels)."""
+    n0 = K.kivi_launch_count()
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    return K.kivi_launch_count() - n0
+
+
+def _profile_traffic(name):
+    """DRAM bytes per decode call from the committed ncu summary, if one matches."""
+    p = os.path.join(ROOT, "profiles", f"decode_{name}.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("traffic_bytes_per_call")
+    return None
+
+
+def _e2e(args, w, caches, prompts, steps, torch, dev):
+    NL, S = w["layers"], w["decode"]
+    pin = lambda t: t.cpu().pin_memory()
+    h_prompts = [(pin(K_), pin(V_)) for K_, V_ in prompts]
+    h_steps = [[tuple(pin(t) for t in st) for st in layer] for layer in steps]
+    d_prompts = [(torch.empty_like(K_), torch.empty_like(V_)) for K_, V_ in prompts]
+    d_qkv = [tuple(torch.empty_like(t) for t in steps[0][0]) for _ in range(NL)]
+    h_out = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16).pin_memory() for _ in range(NL)]
+    d_out = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
+    h2d = sum(K_.numel() * 2 + V_.numel() * 2 for K_, V_ in h_prompts)
+    h2d += sum(t.numel() * 2 for layer in h_steps for st in layer for t in st)
+    d2h = NL * S * h_out[0].numel() * 2
+
+    def step():
+        for li in range(NL):
+            d_prompts[li][0].copy_(h_prompts[li][0], non_blocking=True)
+            d_prompts[li][1].copy_(h_prompts[li][1], non_blocking=True)
+            caches[li].reset()
+            caches[li].prefill(*d_prompts[li])
+        for s in range(S):
+            for li in range(NL):
+                q, k, v = d_qkv[li]
+                hq, hk, hv = h_steps[li][s]
+                q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
+                caches[li].append(k, v)
+                caches[li].decode_attn(q, out=d_out[li])
+                h_out[li].copy_(d_out[li], non_blocking=True)
+
+    n = max(3, min(args.steps, 10))
+    step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    secs = (time.perf_counter() - t0) / n
+    return {"value": _kv_tokens_per_step(w) / secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3, "steps": n,
+            "how": "eager calls through bit_kivi_kv_gb300.kivi, host-timed, pinned host buffers"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+// Host side of the C ABI declared in include/kivi.h: argument checks, the
+// streaming state (quantized / residual token counts), and kernel launches.
+//
+// Streaming rule (KIVI explainer, discosf.com, 3.1; "KV cache quantization
+// axis selection guide", unite.ai, "the system tax"): a prompt keeps its
+// G-aligned prefix quantized and at most R tokens in fp16; an append that
+// finds R residual tokens quantizes them as one batch first.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <new>
+
+#include "kivi_common.cuh"
+
+struct kivi_cache {
+    kivi::Geometry geo;
+    uint8_t* buf;
+    long long n_quant;
+    long long n_resid;
+    int device;      // -1 until the first decode queries it
+    int num_sms;
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+std::atomic<unsigned long long> g_launches{0};
+
+kivi_status fail(kivi_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kivi_status ok() {
+    g_err[0] = '\0';
+    return KIVI_OK;
+}
+
+kivi_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(KIVI_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+namespace kivi {
+
+kivi_status derive_geometry(const kivi_config* c, Geometry* g, const char** why) {
+    if (!c) { *why = "null config"; return KIVI_ERR_INVALID_ARG; }
+    if (c->batch < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 1 ||
+        c->group < 1 || c->residual < 1 || c->max_tokens < 1) {
+        *why = "batch, heads, head_dim, group, residual and max_tokens must be positive";
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (c->bits != 2 && c->bits != 4) { *why = "bits must be 2 or 4"; return KIVI_ERR_UNSUPPORTED; }
+    if (c->head_dim != 64 && c->head_dim != 128) { *why = "head_dim must be 64 or 128"; return KIVI_ERR_UNSUPPORTED; }
+    if (c->group != 32 && c->group != 64 && c->group != 128) { *why = "group must be 32, 64 or 128"; return KIVI_ERR_UNSUPPORTED; }
+    if (c->head_dim % c->group) { *why = "head_dim must be a multiple of group (value groups)"; return KIVI_ERR_INVALID_ARG; }
+    if (c->residual % c->group || c->residual < c->group) { *why = "residual must be a positive multiple of group"; return KIVI_ERR_INVALID_ARG; }
+    if (c->n_q_heads % c->n_kv_heads) { *why = "n_q_heads must be a multiple of n_kv_heads"; return KIVI_ERR_INVALID_ARG; }
+    const int nq = c->n_q_heads / c->n_kv_heads;
+    if (nq != 1 && nq != 2 && nq != 4) { *why = "n_q_heads / n_kv_heads must be 1, 2 or 4"; return KIVI_ERR_UNSUPPORTED; }
+    if ((long long)c->batch * c->n_kv_heads > 65535) { *why = "batch * n_kv_heads must be <= 65535"; return KIVI_ERR_UNSUPPORTED; }
+    if ((long long)c->batch * c->n_q_heads > 0x7fffffffLL) { *why = "batch * n_q_heads too large"; return KIVI_ERR_UNSUPPORTED; }
+    if (c->max_tokens > (1LL << 30)) { *why = "max_tokens must be <= 2^30"; return KIVI_ERR_UNSUPPORTED; }
+    g->B = c->batch; g->Hq = c->n_q_heads; g->Hkv = c->n_kv_heads; g->D = c->head_dim;
+    g->bits = c->bits; g->G = c->group; g->R = c->residual; g->max_tokens = c->max_tokens;
+    g->NB = c->max_tokens / c->group;
+    g->tile_bytes = 2LL * g->D * g->bits;
+    g->part_bytes = (g->G / 16) * g->tile_bytes + 4LL * g->D;
+    g->slot_bytes = 2 * g->NB * g->part_bytes;
+    const long long slots = (long long)g->B * g->Hkv;
+    g->resid_slot_bytes = (long long)g->R * g->D * 2;
+    g->k_resid_off = round_up(slots * g->slot_bytes, 256);
+    g->v_resid_off = round_up(g->k_resid_off + slots * g->resid_slot_bytes, 256);
+    g->total_bytes = round_up(g->v_resid_off + slots * g->resid_slot_bytes, 256);
+    *why = "";
+    return KIVI_OK;
+}
+
+}  // namespace kivi
+
+extern "C" {
+
+size_t kivi_cache_bytes(const kivi_config* cfg) {
+    kivi::Geometry g;
+    const char* why;
+    if (kivi::derive_geometry(cfg, &g, &why) != KIVI_OK) { fail(KIVI_ERR_INVALID_ARG, "%s", why); return 0; }
+    return (size_t)g.total_bytes;
+}
+
+kivi_status kivi_cache_layout(const kivi_config* cfg, kivi_layout* out) {
+    if (!out) return fail(KIVI_ERR_INVALID_ARG, "null layout pointer");
+    kivi::Geometry g;
+    const char* why;
+    const kivi_status st = kivi::derive_geometry(cfg, &g, &why);
+    if (st != KIVI_OK) return fail(st, "%s", why);
+    out->total_bytes = (size_t)g.total_bytes;
+    out->blocks_per_slot = g.NB;
+    out->tile_bytes = (size_t)g.tile_bytes;
+    out->part_bytes = (size_t)g.part_bytes;
+    out->slot_bytes = (size_t)g.slot_bytes;
+    out->k_resid_offset = (size_t)g.k_resid_off;
+    out->v_resid_offset = (size_t)g.v_resid_off;
+    out->resid_slot_bytes = (size_t)g.resid_slot_bytes;
+    return ok();
+}
+
+kivi_status kivi_cache_create(const kivi_config* cfg, void* dev_buf, size_t bytes, kivi_cache_t* out) {
+    if (!out) return fail(KIVI_ERR_INVALID_ARG, "null output handle pointer");
+    *out = nullptr;
+    kivi::Geometry g;
+    const char* why;
+    const kivi_status st = kivi::derive_geometry(cfg, &g, &why);
+    if (st != KIVI_OK) return fail(st, "%s", why);
+    if (!dev_buf) return fail(KIVI_ERR_INVALID_ARG, "null cache buffer");
+    if (!aligned(dev_buf, 256)) return fail(KIVI_ERR_INVALID_ARG, "cache buffer must be 256-byte aligned");
+    if (bytes < (size_t)g.total_bytes)
+        return fail(KIVI_ERR_CAPACITY, "cache buffer has %zu bytes, needs %lld", bytes, g.total_bytes);
+    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0};
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "out of host memory");
+    *out = c;
+    return ok();
+}
+
+kivi_status kivi_cache_destroy(kivi_cache_t c) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    delete c;
+    return ok();
+}
+
+kivi_status kivi_cache_reset(kivi_cache_t c) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    c->n_quant = 0;
+    c->n_resid = 0;
+    return ok();
+}
+
+kivi_status kivi_cache_counts(kivi_cache_t c, long long* n_quant, long long* n_resid) {
+    if (!c || !n_quant || !n_resid) return fail(KIVI_ERR_INVALID_ARG, "null argument");
+    *n_quant = c->n_quant;
+    *n_resid = c->n_resid;
+    return ok();
+}
+
+kivi_status kivi_prefill(kivi_cache_t c, const void* K, const void* V, long long L, kivi_stream_t stream) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    if (c->n_quant || c->n_resid) return fail(KIVI_ERR_STATE, "prefill needs an empty cache");
+    if (L < 0) return fail(KIVI_ERR_INVALID_ARG, "negative length");
+    if (L > c->geo.max_tokens) return fail(KIVI_ERR_CAPACITY, "prompt of %lld tokens exceeds max_tokens %lld", L, c->geo.max_tokens);
+    if (L == 0) return ok();
+    if (!K || !V) return fail(KIVI_ERR_INVALID_ARG, "null K or V");
+    if (!aligned(K, 16) || !aligned(V, 16)) return fail(KIVI_ERR_INVALID_ARG, "K and V must be 16-byte aligned");
+    const kivi::Geometry& g = c->geo;
+    const long long over = L > g.R ? L - g.R : 0;
+    const long long Lq = (over + g.G - 1) / g.G * g.G;
+    const long long r = L - Lq;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const __half* k = static_cast<const __half*>(K);
+    const __half* v = static_cast<const __half*>(V);
+    if (Lq) {
+        const cudaError_t e = kivi::launch_quantize_blocks(g, c->buf, k, v, L * g.D, 0, Lq / g.G, st);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill quantize launch");
+        g_launches++;
+    }
+    if (r) {
+        const cudaError_t e = kivi::launch_copy_rows(g, c->buf, k + Lq * g.D, v + Lq * g.D, L * g.D, 0, (int)r, st);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill residual copy launch");
+        g_launches++;
+    }
+    c->n_quant = Lq;
+    c->n_resid = r;
+    return ok();
+}
+
+kivi_status kivi_append(kivi_cache_t c, const void* k, const void* v, kivi_stream_t stream) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    if (!k || !v) return fail(KIVI_ERR_INVALID_ARG, "null k or v");
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(KIVI_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    const kivi::Geometry& g = c->geo;
+    if (c->n_quant + c->n_resid + 1 > g.max_tokens)
+        return fail(KIVI_ERR_CAPACITY, "cache already holds max_tokens (%lld) tokens", g.max_tokens);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (c->n_resid == g.R) {
+        const __half* rk = reinterpret_cast<const __half*>(c->buf + g.k_resid_off);
+        const __half* rv = reinterpret_cast<const __half*>(c->buf + g.v_resid_off);
+        const cudaError_t e = kivi::launch_quantize_blocks(g, c->buf, rk, rv, (long long)g.R * g.D,
+                                                           c->n_quant / g.G, g.R / g.G, st);
+        if (e != cudaSuccess) return cuda_fail(e, "residual flush launch");
+        g_launches++;
+        c->n_quant += g.R;
+        c->n_resid = 0;
+    }
+    const cudaError_t e = kivi::launch_copy_rows(g, c->buf, static_cast<const __half*>(k),
+                                                 static_cast<const __half*>(v), g.D, (int)c->n_resid, 1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "append copy launch");
+    g_launches++;
+    c->n_resid += 1;
+    return ok();
+}
+
+size_t kivi_decode_workspace_bytes(const kivi_config* cfg) {
+    kivi::Geometry g;
+    const char* why;
+    if (kivi::derive_geometry(cfg, &g, &why) != KIVI_OK) { fail(KIVI_ERR_INVALID_ARG, "%s", why); return 0; }
+    return (size_t)g.B * g.Hq * kivi::kPartialSlots * kivi::partial_stride(g.D) * sizeof(float);
+}
+
+kivi_status kivi_decode_attn(kivi_cache_t c, const void* q, void* out, float softmax_scale,
+                             void* workspace, size_t ws_bytes, kivi_stream_t stream) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    if (!q || !out || !workspace) return fail(KIVI_ERR_INVALID_ARG, "null q, out or workspace");
+    if (!aligned(q, 16) || !aligned(out, 16)) return fail(KIVI_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    if (!aligned(workspace, 256)) return fail(KIVI_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (!(softmax_scale == softmax_scale) || isinf(softmax_scale)) return fail(KIVI_ERR_INVALID_ARG, "softmax_scale must be finite");
+    const kivi::Geometry& g = c->geo;
+    if (c->n_quant + c->n_resid == 0) return fail(KIVI_ERR_STATE, "decode on an empty cache");
+    const size_t need = (size_t)g.B * g.Hq * kivi::kPartialSlots * kivi::partial_stride(g.D) * sizeof(float);
+    if (ws_bytes < need) return fail(KIVI_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+    if (c->device < 0) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "device query");
+        c->device = dev;
+        c->num_sms = sms;
+    }
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)g.D);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    const kivi::DecodePlan plan = kivi::plan_decode(g, c->n_quant, c->n_resid, c->num_sms);
+    int launches = 0;
+    const cudaError_t e = kivi::launch_decode(g, c->buf, c->n_quant, c->n_resid, static_cast<const __half*>(q),
+                                              static_cast<__half*>(out), scale_log2, static_cast<float*>(workspace),
+                                              plan, reinterpret_cast<cudaStream_t>(stream), &launches);
+    g_launches += (unsigned long long)launches;
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ok();
+}
+
+const char* kivi_last_error_string(void) { return g_err; }
+
+unsigned long long kivi_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal declarations shared by the host API and the kernels of the KIVI
+// KV-cache library.  The public contract (argument meaning, buffer layout,
+// errors) is in include/kivi.h.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kivi.h"
+
+namespace kivi {
+
+// Everything derived from a kivi_config that kernels need to address the cache.
+struct Geometry {
+    int B, Hq, Hkv, D, bits, G, R;
+    long long max_tokens;
+    long long NB;              // quantized blocks per (batch, kv-head) slot
+    long long tile_bytes;      // one 16-token code tile: 2*D*bits
+    long long part_bytes;      // one block's key or value part: (G/16)*tile + 4*D
+    long long slot_bytes;      // 2 * NB * part
+    long long k_resid_off;     // byte offset of the key residual region
+    long long v_resid_off;     // byte offset of the value residual region
+    long long resid_slot_bytes;// R * D * 2
+    long long total_bytes;
+};
+
+// Validates cfg; on failure returns the status and writes a reason.
+kivi_status derive_geometry(const kivi_config* cfg, Geometry* g, const char** why);
+
+// Upper bound on decode partial results per (batch, query head).
+constexpr int kMaxSplits = 64;          // quantized-token splits
+constexpr int kPartialSlots = kMaxSplits + 1;  // + one split for the fp16 residual
+
+// Floats per partial result (m, l, two pad, o[D]); D + 4 keeps o 16-byte aligned.
+__host__ __device__ constexpr int partial_stride(int D) { return D + 4; }
+
+// ---- launchers (defined in the .cu files; return the launch status) -------
+
+// Quantize nblk whole blocks per slot.  Block j of slot s is read from
+// src_k/src_v + s*src_slot_elems + j*G*D (rows of D fp16, consecutive tokens)
+// and written to block first_block + j of that slot.
+cudaError_t launch_quantize_blocks(const Geometry& g, uint8_t* cache, const __half* src_k,
+                                   const __half* src_v, long long src_slot_elems,
+                                   long long first_block, long long nblk, cudaStream_t st);
+
+// Copy nrows token rows per slot (K and V) into residual rows [row0, row0+nrows).
+cudaError_t launch_copy_rows(const Geometry& g, uint8_t* cache, const __half* src_k,
+                             const __half* src_v, long long src_slot_elems, int row0, int nrows,
+                             cudaStream_t st);
+
+struct DecodePlan {
+    int tiles_per_split;   // 16-token tiles of quantized cache per split
+    int n_qsplits;         // splits over the quantized tokens
+    int n_splits;          // n_qsplits + (residual split ? 1 : 0)
+};
+
+DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, int num_sms);
+
+cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_quant,
+                          long long n_resid, const __half* q, __half* out, float scale_log2,
+                          float* workspace, const DecodePlan& plan, cudaStream_t st,
+                          int* launches);
+
+}  // namespace kivi

@@ -1,0 +1,184 @@
+"""Python binding of the C ABI in include/kivi.h (ctypes; marshalling only).
+
+The module-level functions carry the C names and take plain integers for
+pointers and streams.  ``KiviCache`` wraps one handle with torch tensors for
+device memory and the current torch stream.  Every computation runs in the
+library's CUDA kernels; importing this module fails loudly when libkivi.so is
+missing (build it with ``python -m bit_kivi_kv_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkivi.so")
+
+KIVI_OK, KIVI_ERR_INVALID_ARG, KIVI_ERR_UNSUPPORTED, KIVI_ERR_CAPACITY, KIVI_ERR_STATE, KIVI_ERR_CUDA = range(6)
+STATUS_NAMES = ["KIVI_OK", "KIVI_ERR_INVALID_ARG", "KIVI_ERR_UNSUPPORTED", "KIVI_ERR_CAPACITY",
+                "KIVI_ERR_STATE", "KIVI_ERR_CUDA"]
+
+
+class kivi_config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("bits", ctypes.c_int), ("group", ctypes.c_int),
+                ("residual", ctypes.c_int), ("max_tokens", ctypes.c_longlong)]
+
+
+class kivi_layout(ctypes.Structure):
+    _fields_ = [("total_bytes", ctypes.c_size_t), ("blocks_per_slot", ctypes.c_longlong),
+                ("tile_bytes", ctypes.c_size_t), ("part_bytes", ctypes.c_size_t),
+                ("slot_bytes", ctypes.c_size_t), ("k_resid_offset", ctypes.c_size_t),
+                ("v_resid_offset", ctypes.c_size_t), ("resid_slot_bytes", ctypes.c_size_t)]
+
+
+class KiviError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES[status] if 0 <= status < 6 else status}: {message}")
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m bit_kivi_kv_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, SZ, LL, I, F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_longlong, ctypes.c_int, ctypes.c_float
+    cfgp = ctypes.POINTER(kivi_config)
+    sigs = {
+        "kivi_cache_bytes": (SZ, [cfgp]),
+        "kivi_cache_layout": (I, [cfgp, ctypes.POINTER(kivi_layout)]),
+        "kivi_cache_create": (I, [cfgp, P, SZ, ctypes.POINTER(P)]),
+        "kivi_cache_destroy": (I, [P]),
+        "kivi_cache_reset": (I, [P]),
+        "kivi_cache_counts": (I, [P, ctypes.POINTER(LL), ctypes.POINTER(LL)]),
+        "kivi_prefill": (I, [P, P, P, LL, P]),
+        "kivi_append": (I, [P, P, P, P]),
+        "kivi_decode_workspace_bytes": (SZ, [cfgp]),
+        "kivi_decode_attn": (I, [P, P, P, F, P, SZ, P]),
+        "kivi_last_error_string": (ctypes.c_char_p, []),
+        "kivi_launch_count": (ctypes.c_ulonglong, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int):
+    if status != KIVI_OK:
+        raise KiviError(status, lib.kivi_last_error_string().decode())
+
+
+def make_config(batch, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_tokens) -> kivi_config:
+    return kivi_config(batch, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_tokens)
+
+
+# ---- the C calls, same names --------------------------------------------------
+def kivi_cache_bytes(cfg: kivi_config) -> int:
+    return lib.kivi_cache_bytes(ctypes.byref(cfg))
+
+
+def kivi_cache_layout(cfg: kivi_config) -> kivi_layout:
+    out = kivi_layout()
+    _check(lib.kivi_cache_layout(ctypes.byref(cfg), ctypes.byref(out)))
+    return out
+
+
+def kivi_cache_create(cfg: kivi_config, dev_buf: int, nbytes: int) -> int:
+    h = ctypes.c_void_p()
+    _check(lib.kivi_cache_create(ctypes.byref(cfg), dev_buf, nbytes, ctypes.byref(h)))
+    return h.value
+
+
+def kivi_cache_destroy(h: int):
+    _check(lib.kivi_cache_destroy(h))
+
+
+def kivi_cache_reset(h: int):
+    _check(lib.kivi_cache_reset(h))
+
+
+def kivi_cache_counts(h: int):
+    a, b = ctypes.c_longlong(), ctypes.c_longlong()
+    _check(lib.kivi_cache_counts(h, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def kivi_prefill(h: int, K: int, V: int, L: int, stream: int):
+    _check(lib.kivi_prefill(h, K, V, L, stream))
+
+
+def kivi_append(h: int, k: int, v: int, stream: int):
+    _check(lib.kivi_append(h, k, v, stream))
+
+
+def kivi_decode_workspace_bytes(cfg: kivi_config) -> int:
+    return lib.kivi_decode_workspace_bytes(ctypes.byref(cfg))
+
+
+def kivi_decode_attn(h: int, q: int, out: int, softmax_scale: float, workspace: int, ws_bytes: int, stream: int):
+    _check(lib.kivi_decode_attn(h, q, out, softmax_scale, workspace, ws_bytes, stream))
+
+
+def kivi_last_error_string() -> str:
+    return lib.kivi_last_error_string().decode()
+
+
+def kivi_launch_count() -> int:
+    return lib.kivi_launch_count()
+
+
+# ---- torch convenience wrapper -----------------------------------------------
+class KiviCache:
+    """One layer's cache: a torch-owned device buffer plus the library handle."""
+
+    def __init__(self, batch, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_tokens,
+                 device="cuda"):
+        import torch
+        self.cfg = make_config(batch, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_tokens)
+        nbytes = kivi_cache_bytes(self.cfg)
+        if nbytes == 0:
+            raise KiviError(KIVI_ERR_INVALID_ARG, kivi_last_error_string())
+        self.layout = kivi_cache_layout(self.cfg)
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.workspace = torch.empty(kivi_decode_workspace_bytes(self.cfg), dtype=torch.uint8, device=device)
+        self.handle = kivi_cache_create(self.cfg, self.buffer.data_ptr(), nbytes)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            lib.kivi_cache_destroy(h)
+            self.handle = None
+
+    @staticmethod
+    def _stream(stream):
+        import torch
+        return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+    @staticmethod
+    def _ptr(t):
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return t.data_ptr()
+
+    def counts(self):
+        return kivi_cache_counts(self.handle)
+
+    def reset(self):
+        kivi_cache_reset(self.handle)
+
+    def prefill(self, K, V, stream=None):
+        kivi_prefill(self.handle, self._ptr(K), self._ptr(V), K.shape[2], self._stream(stream))
+
+    def append(self, k, v, stream=None):
+        kivi_append(self.handle, self._ptr(k), self._ptr(v), self._stream(stream))
+
+    def decode_attn(self, q, out=None, softmax_scale=0.0, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        kivi_decode_attn(self.handle, self._ptr(q), self._ptr(out), softmax_scale,
+                         self.workspace.data_ptr(), self.workspace.numel(), self._stream(stream))
+        return out

@@ -1,0 +1,112 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Quantized blocks and residual rows are compared bit for bit; decode outputs
+(fp16) against the oracle's fp64 attention over the same dequantized cache,
+max |err| <= 4e-3 and relative L2 <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU hosts too
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+from bit_kivi_kv_gb300.kivi import KiviCache, KiviError, KIVI_ERR_CAPACITY  # noqa: E402
+from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50  # noqa: E402
+from kivi_harness import check_slots, run_gpu  # noqa: E402
+
+
+def test_tiny_single_step():
+    """B1 H1 D64, 2-bit, G32, R32: prefill 256 (224 quantized), append 1 (flush), decode."""
+    run = run_gpu(1, 1, 1, 64, 2, 32, 32, L=256, n_app=1, seed=1000, decode_at={0},
+                  outliers=FIXED_4_X20, sink=False)
+    assert run["cache"].counts() == (256, 1)
+    check_slots(run, [(0, 0)], {0})
+
+
+SMALL = [
+    # B, Hq, Hkv, D, bits, G, R, L, n_app
+    (2, 4, 4, 128, 2, 32, 128, 700, 12),      # ragged prompt, a flush after 4 appends
+    (2, 8, 2, 128, 4, 128, 128, 1000, 10),    # grouped queries, 4-bit, G = R = 128
+    (1, 4, 2, 64, 4, 64, 64, 300, 70),        # D64, 2 q heads per kv head, flushes
+    (3, 2, 2, 64, 2, 32, 64, 0, 100),         # empty prompt: residual only, then flushes
+    (2, 2, 2, 128, 2, 64, 128, 100, 5),       # prompt shorter than R: nothing quantized
+    (1, 4, 1, 128, 2, 32, 32, 515, 40),       # 4 q heads per kv head, R = G
+    (2, 2, 2, 128, 4, 32, 64, 161, 3),        # 4-bit with small groups
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}D{c[3]}b{c[4]}G{c[5]}R{c[6]}L{c[7]}n{c[8]}" for c in SMALL])
+def test_small_full_check(case):
+    B, Hq, Hkv, D, bits, G, R, L, n = case
+    steps = {0, n // 2, n - 1}
+    run = run_gpu(B, Hq, Hkv, D, bits, G, R, L, n, seed=17 + sum(case), decode_at=steps)
+    check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
+
+
+def test_degenerate_groups():
+    """Constant key channels / value groups (step 0) and signed zeros: codes 0, zero +0."""
+    B, H, D, G, R, L = 1, 2, 128, 32, 32, 160
+    gen = torch.Generator().manual_seed(5)
+    K = torch.randn(B, H, L, D, generator=gen)
+    V = torch.randn(B, H, L, D, generator=gen)
+    K[:, :, :, 5] = 1.5                       # a constant channel
+    K[:, 0, 32:64, 9] = 0.0
+    K[:, 0, 32:64:2, 9] = -0.0                # mixed signed zeros in one key group
+    V[:, 1, 40, 32:64] = -2.25                # one constant value group
+    V[:, 1, 41, :32] = -0.0
+    K, V = K.half().cuda(), V.half().cuda()
+    run = run_gpu(B, H, H, D, 2, G, R, L, 3, seed=3, decode_at={2}, prompt=(K, V))
+    check_slots(run, [(0, 0), (0, 1)], {2})
+
+
+def test_capacity_and_state_errors():
+    c = KiviCache(1, 1, 1, 64, 2, 32, 32, max_tokens=40)
+    K = torch.randn(1, 1, 41, 64, device="cuda").half()
+    with pytest.raises(KiviError) as e:
+        c.prefill(K, K)
+    assert e.value.status == KIVI_ERR_CAPACITY
+    c.prefill(K[:, :, :40].contiguous(), K[:, :, :40].contiguous())
+    k = torch.randn(1, 1, 64, device="cuda").half()
+    with pytest.raises(KiviError) as e:
+        c.append(k, k)
+    assert e.value.status == KIVI_ERR_CAPACITY
+    assert c.counts() == (32, 8)
+
+
+# ---- the full-size workloads, on sampled slots --------------------------------
+
+def _slots(B, Hkv):
+    return sorted({(0, 0), (B - 1, Hkv - 1), (B // 2, Hkv // 3)})
+
+
+def test_llama2_7b_layer_full_size():
+    """B8 H32 D128, 2-bit G32 R128, prompt 4096 (sink + outliers), 64 decode steps."""
+    steps = {0, 1, 31, 63}
+    run = run_gpu(8, 32, 32, 128, 2, 32, 128, 4096, 64, seed=1001, decode_at=steps)
+    assert run["cache"].counts() == (4096, 64)     # 3968 + one flush of 128; 64 appended
+    check_slots(run, _slots(8, 32), steps)
+
+
+def test_llama2_13b_layer_full_size():
+    """One layer of the 40-layer B32 H40 D128 2-bit step: prompt 4096, append (flush), decode."""
+    run = run_gpu(32, 40, 40, 128, 2, 32, 128, 4096, 1, seed=1002, decode_at={0})
+    assert run["cache"].counts() == (4096, 1)
+    check_slots(run, _slots(32, 40), {0})
+
+
+def test_gqa_llama3_8b_full_size():
+    """B64, 32 q heads on 8 kv heads, D128, 4-bit G128 R128, prompt 8192, append 1, decode."""
+    run = run_gpu(64, 32, 8, 128, 4, 128, 128, 8192, 1, seed=1003, decode_at={0})
+    assert run["cache"].counts() == (8192, 1)
+    check_slots(run, _slots(64, 8), {0})
+
+
+def test_long_context_streaming_full_size():
+    """B2 H32 D128 2-bit G32 R128: prompt 131072, 512 appends (flush every 128)."""
+    steps = {0, 1, 127, 128, 129, 255, 256, 383, 384, 385, 511}
+    run = run_gpu(2, 32, 32, 128, 2, 32, 128, 131072, 512, seed=1004, decode_at=steps)
+    assert run["cache"].counts() == (131072 + 384, 128)
+    check_slots(run, [(0, 0), (1, 31)], steps)
