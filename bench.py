@@ -377,14 +377,54 @@ def _launches_in(step, K, stream, torch):
     return K.kivi_launch_count() - n0
 
 
+def _decode_source_sha1():
+    import hashlib
+    h = hashlib.sha1()
+    for f in ("kivi_decode.cu", "kivi_common.cuh"):
+        with open(os.path.join(ROOT, "bit_kivi_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def _profile_traffic(name):
-    """DRAM bytes per decode call from the committed ncu summary, if one matches."""
+    """DRAM bytes per decode call from the committed ncu summary, if it was taken
+    on the decode kernel as it is now (same source hash); else None."""
     p = os.path.join(ROOT, "profiles", f"decode_{name}.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return d.get("traffic_bytes_per_call")
+        if d.get("decode_source_sha1") == _decode_source_sha1():
+            return d.get("traffic_bytes_per_call")
     return None
+
+
+def run_profile(args, w):
+    """Small eager run for ncu: build the workload's caches, run one full step,
+    then a few more decode calls (no graphs, no e2e, no oracle)."""
+    import torch
+    from bit_kivi_kv_gb300 import build as _b
+    _b.build()
+    from bit_kivi_kv_gb300.kivi import KiviCache
+    from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV
+    dev = torch.device("cuda", 0)
+    outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
+    NL, S = min(w["layers"], 2), w["decode"]
+    for li in range(NL):
+        syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=w["seed"] + 7919 * li, outliers=outl,
+                      sink=w["sink"], device=dev)
+        K_, V_ = syn.prompt(w["prompt"])
+        c = KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], w["prompt"] + S, device=dev)
+        c.prefill(K_, V_)
+        out = None
+        for s in range(S):
+            q, k, v = syn.step(s)
+            c.append(k, v)
+            out = c.decode_attn(q, out=out)
+        for _ in range(args.profile_calls):
+            c.decode_attn(q, out=out)
+        del K_, V_
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": args.workload, "decode_source_sha1": _decode_source_sha1()}))
 
 
 def _e2e(args, w, caches, prompts, steps, torch, dev):
@@ -437,11 +477,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="small eager run for ncu captures")
+    ap.add_argument("--profile-calls", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)
