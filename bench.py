@@ -52,6 +52,7 @@ WORKLOADS = {
                          layers=1, outliers="range", sink=True, seed=1004),
 }
 DEFAULT = "llama2-7b-layer"
+_KERNEL_IDS = {"auto": 0, "cuda-core": 1, "tensor-core": 2}
 
 
 def _dist_env():
@@ -251,6 +252,7 @@ def run_ours(args, w):
         steps.append([syn.step(s) for s in range(S)])
         caches.append(KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], max_tokens,
                                 device=dev))
+        caches[-1].set_decode_kernel(_KERNEL_IDS[args.decode_kernel])
     outs = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
 
     def step():
@@ -350,8 +352,8 @@ def run_ours(args, w):
                         "steps_per_s": 1e3 / dec_ms},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "decode attention call "
-                     "(split-KV kernel + log-sum-exp combine)"},
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": f"decode attention call ({args.decode_kernel}: "
+                     "split-KV kernel + log-sum-exp combine)"},
         "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -414,6 +416,7 @@ def run_profile(args, w):
                       sink=w["sink"], device=dev)
         K_, V_ = syn.prompt(w["prompt"])
         c = KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], w["prompt"] + S, device=dev)
+        c.set_decode_kernel(_KERNEL_IDS[args.decode_kernel])
         c.prefill(K_, V_)
         out = None
         for s in range(S):
@@ -478,6 +481,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true", help="small eager run for ncu captures")
+    ap.add_argument("--decode-kernel", choices=["auto", "cuda-core", "tensor-core"], default="auto")
     ap.add_argument("--profile-calls", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -21,6 +21,7 @@ struct kivi_cache {
     long long n_resid;
     int device;      // -1 until the first decode queries it
     int num_sms;
+    int decode_kernel;   // kivi_decode_kernel
 };
 
 namespace {
@@ -125,7 +126,7 @@ kivi_status kivi_cache_create(const kivi_config* cfg, void* dev_buf, size_t byte
     if (!aligned(dev_buf, 256)) return fail(KIVI_ERR_INVALID_ARG, "cache buffer must be 256-byte aligned");
     if (bytes < (size_t)g.total_bytes)
         return fail(KIVI_ERR_CAPACITY, "cache buffer has %zu bytes, needs %lld", bytes, g.total_bytes);
-    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0};
+    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0, KIVI_DECODE_AUTO};
     if (!c) return fail(KIVI_ERR_INVALID_ARG, "out of host memory");
     *out = c;
     return ok();
@@ -237,11 +238,20 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void* q, void* out, float sof
     const float scale_log2 = scale * 1.4426950408889634f;
     const kivi::DecodePlan plan = kivi::plan_decode(g, c->n_quant, c->n_resid, c->num_sms);
     int launches = 0;
+    const int variant = c->decode_kernel == KIVI_DECODE_AUTO ? KIVI_DECODE_TENSOR_CORE : c->decode_kernel;
     const cudaError_t e = kivi::launch_decode(g, c->buf, c->n_quant, c->n_resid, static_cast<const __half*>(q),
                                               static_cast<__half*>(out), scale_log2, static_cast<float*>(workspace),
-                                              plan, reinterpret_cast<cudaStream_t>(stream), &launches);
+                                              plan, variant, reinterpret_cast<cudaStream_t>(stream), &launches);
     g_launches += (unsigned long long)launches;
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ok();
+}
+
+kivi_status kivi_cache_set_decode_kernel(kivi_cache_t c, int kernel) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    if (kernel != KIVI_DECODE_AUTO && kernel != KIVI_DECODE_CUDA_CORE && kernel != KIVI_DECODE_TENSOR_CORE)
+        return fail(KIVI_ERR_INVALID_ARG, "unknown decode kernel %d", kernel);
+    c->decode_kernel = kernel;
     return ok();
 }
 

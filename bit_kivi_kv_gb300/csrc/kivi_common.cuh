@@ -57,9 +57,10 @@ struct DecodePlan {
 
 DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, int num_sms);
 
+// variant: KIVI_DECODE_CUDA_CORE or KIVI_DECODE_TENSOR_CORE (resolved, never AUTO).
 cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_quant,
                           long long n_resid, const __half* q, __half* out, float scale_log2,
-                          float* workspace, const DecodePlan& plan, cudaStream_t st,
+                          float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
                           int* launches);
 
 }  // namespace kivi

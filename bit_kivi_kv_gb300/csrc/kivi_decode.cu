@@ -13,6 +13,7 @@
 #include <math.h>
 
 #include "kivi_common.cuh"
+#include "kivi_decode_mma.cuh"
 
 namespace kivi {
 namespace {
@@ -326,10 +327,30 @@ DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, 
     return p;
 }
 
+cudaError_t launch_decode_mma_d128(const mma_detail::Args& a, int bits, int nq, int G, dim3 grid,
+                                   cudaStream_t st);
+cudaError_t launch_decode_mma_d64(const mma_detail::Args& a, int bits, int nq, int G, dim3 grid,
+                                  cudaStream_t st);
+
 cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_quant,
                           long long n_resid, const __half* q, __half* out, float scale_log2,
-                          float* workspace, const DecodePlan& plan, cudaStream_t st,
+                          float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
                           int* launches) {
+    if (variant == KIVI_DECODE_TENSOR_CORE) {
+        mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
+                           g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)(n_quant / 16),
+                           (int)n_resid, plan.tiles_per_split, plan.n_qsplits, scale_log2};
+        const dim3 grid(plan.n_splits, g.B * g.Hkv);
+        const int nq = g.Hq / g.Hkv;
+        cudaError_t e = g.D == 128 ? launch_decode_mma_d128(m, g.bits, nq, g.G, grid, st)
+                                   : launch_decode_mma_d64(m, g.bits, nq, g.G, grid, st);
+        *launches = 1;
+        if (e != cudaSuccess) return e;
+        if (g.D == 128) combine_kernel<128><<<g.B * g.Hq, 128, 0, st>>>(workspace, out, plan.n_splits);
+        else combine_kernel<64><<<g.B * g.Hq, 64, 0, st>>>(workspace, out, plan.n_splits);
+        *launches = 2;
+        return cudaGetLastError();
+    }
     DecodeArgs a{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                  g.k_resid_off, g.v_resid_off, g.R, g.G, g.Hq, g.Hkv,
                  (int)(n_quant / 16), (int)n_resid, plan.tiles_per_split, plan.n_qsplits, scale_log2};

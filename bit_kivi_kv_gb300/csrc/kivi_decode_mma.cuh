@@ -1,0 +1,445 @@
+// Tensor-core split-KV decode over the quantized cache and the fp16 residual.
+//
+// Same computation as the CUDA-core kernel (softmax-weighted sum of the
+// dequantized values over every cached token; "KV cache quantization axis
+// selection guide", unite.ai), arranged for mma.sync.m16n8k16 (fp16 x fp16 ->
+// fp32) with the cache as the M operand:
+//
+//   keys   : S[t][n]   = sum_c code[t][c] * Qt[c][n] + beta[n]
+//            Qt[c][2h] + Qt[c][2h+1] = q_h[c] * step_c (fp16 hi + lo parts,
+//            about 22 significant bits); beta = sum_c q_h[c] * zero_c enters
+//            as the accumulator's initial value.
+//   values : O^T[c][n] = sum_t code[c][t] * Pt[t][n]  (+ sum_t p_t zero_t per
+//            channel group, accumulated on the side in fp32)
+//            Pt[t][n] = p_h(t) * step(t, group) as fp16 hi + lo parts.  Column
+//            n = 2*(h*GB + j) + {hi, lo} carries group j of the GB groups one
+//            B fragment covers, so for one query head all channel groups share
+//            one fragment per 16-token tile; a lane keeps the accumulators of
+//            the column pair that matches its channels' group.
+//
+// Codes come out of the tile words exactly: a code field masked into an fp16
+// mantissa with exponent 2^10 gives 1024 + 4^u * code, and one f16x2 FMA with
+// (4^-u, -1024 * 4^-u) returns the code (all values exact in fp16).
+// Online softmax per warp in the log2 domain; each warp owns a contiguous run
+// of the split's 16-token tiles; warps and splits merge by log-sum-exp.
+#pragma once
+
+#include <math.h>
+
+#include "kivi_common.cuh"
+
+namespace kivi {
+namespace mma_detail {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct Args {
+    const uint8_t* cache;
+    const __half* q;
+    float* ws;
+    long long NB, part_bytes, slot_bytes, tile_bytes, k_resid_off, v_resid_off;
+    int R, Hq, Hkv;
+    int n_qtiles, n_resid;
+    int tiles_per_split, n_qsplits;
+    float scale_log2;
+};
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t d;   // low 16 bits <- lo
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+__device__ __forceinline__ uint32_t neg_f16x2(uint32_t v) { return v ^ 0x80008000u; }
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg_stream2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// Exact f16x2 pair of codes of slot u of a tile word (w8 = w >> 8).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int u) {
+    constexpr int PER = 16 / BITS;
+    constexpr int DIRECT = BITS == 2 ? 5 : 2;          // slots whose field sits in mantissa bits 0..9
+    const int pos = u < DIRECT ? u : u - PER / 2;       // position after the optional 8-bit shift
+    const uint32_t src = u < DIRECT ? w : w8;
+    const uint32_t field = (BITS == 2 ? 0x00030003u : 0x000F000Fu) << (BITS * pos);
+    const uint32_t x = (src & field) | 0x64006400u;     // 1024 + code * 2^(BITS*pos)
+    // scale 2^(-BITS*pos), bias -1024 * 2^(-BITS*pos); fp16 exponent field shifts by BITS*pos
+    const uint32_t e = (uint32_t)(BITS * pos);
+    const uint32_t sc = (uint32_t)(15 - e) << 10;               // 2^-e
+    const uint32_t bi = 0x8000u | ((uint32_t)(25 - e) << 10);   // -2^(10-e)
+    return hfma2(x, sc | (sc << 16), bi | (bi << 16));
+}
+
+// A fragment (4 registers) of k-step / m-tile kk from a lane's tile words.
+template <int BITS, int W>
+__device__ __forceinline__ void a_frag(const uint32_t (&w)[W], const uint32_t (&w8)[W], int kk, uint32_t (&a)[4]) {
+    constexpr int PER = 16 / BITS;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int p = 4 * kk + r;
+        a[r] = code_pair<BITS>(w[p / PER], w8[p / PER], p % PER);
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void load_tile_words(const uint8_t* p, uint32_t (&w)[W]) {
+    if constexpr (W % 4 == 0) {
+#pragma unroll
+        for (int v = 0; v < W / 4; ++v) {
+            const uint4 x = ldg_stream(p + 16 * v);
+            w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+    } else {
+        const uint2 x = ldg_stream2(p);
+        w[0] = x.x; w[1] = x.y;
+    }
+}
+
+template <int D, int BITS, int NQ, int G>
+struct Cfg {
+    static constexpr int KSTEPS = D / 16;             // k-steps (keys) = m-tiles (values)
+    static constexpr int W = D * BITS / 64;           // words per lane per tile
+    static constexpr int NGRP = D / G;                // value channel groups per token
+    static constexpr int GB = (NQ * NGRP <= 4) ? NGRP : 1;   // groups per B fragment
+    static constexpr int NBF = NGRP / GB;             // B fragments per tile (values)
+    static constexpr int QSTRIDE = 2 * KSTEPS + 4;    // u32 per lane row of the Qt fragment table
+    static constexpr int TPB = G / 16;                // tiles per block
+};
+
+// Build this warp's Qt B fragments (hi/lo of q_h * step) and its beta, from
+// the block's key (step, zero) entries; entries == nullptr means step 1,
+// zero 0 (the fp16 residual).
+template <class C, int D, int NQ>
+__device__ __forceinline__ void build_q_frags(const uint32_t* entries, const float (*qf)[D],
+                                              uint32_t* qfrag, int lane, uint32_t (&qb)[2 * C::KSTEPS],
+                                              float& beta) {
+    float bp[NQ];
+#pragma unroll
+    for (int h = 0; h < NQ; ++h) bp[h] = 0.f;
+    __syncwarp();
+#pragma unroll
+    for (int cp = lane; cp < D / 2; cp += 32) {
+        float s0 = 1.f, s1 = 1.f, z0 = 0.f, z1 = 0.f;
+        if (entries) {
+            const uint2 e = *reinterpret_cast<const uint2*>(entries + 2 * cp);
+            const float2 a = unpack_f16x2(e.x), b = unpack_f16x2(e.y);
+            s0 = a.x; z0 = a.y; s1 = b.x; z1 = b.y;
+        }
+        const int kk = cp >> 3, cc = (2 * cp) & 15, reg = cc >> 3, ii = (cc & 7) >> 1;
+#pragma unroll
+        for (int h = 0; h < NQ; ++h) {
+            const float x0 = qf[h][2 * cp] * s0, x1 = qf[h][2 * cp + 1] * s1;
+            bp[h] = fmaf(qf[h][2 * cp], z0, fmaf(qf[h][2 * cp + 1], z1, bp[h]));
+            const uint32_t hi = pack_f16x2(x0, x1);
+            const float2 hf = unpack_f16x2(hi);
+            const uint32_t lo = pack_f16x2(x0 - hf.x, x1 - hf.y);
+            qfrag[(4 * (2 * h) + ii) * C::QSTRIDE + 2 * kk + reg] = hi;
+            qfrag[(4 * (2 * h + 1) + ii) * C::QSTRIDE + 2 * kk + reg] = lo;
+        }
+    }
+    const int i = lane & 3;
+    beta = 0.f;
+#pragma unroll
+    for (int h = 0; h < NQ; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bp[h] += __shfl_xor_sync(kFull, bp[h], o);
+        if (i == h) beta = bp[h];
+    }
+    __syncwarp();
+    const uint4* row = reinterpret_cast<const uint4*>(qfrag + lane * C::QSTRIDE);
+#pragma unroll
+    for (int v = 0; v < C::KSTEPS / 2; ++v) {
+        const uint4 x = row[v];
+        qb[4 * v] = x.x; qb[4 * v + 1] = x.y; qb[4 * v + 2] = x.z; qb[4 * v + 3] = x.w;
+    }
+}
+
+template <int D, int BITS, int NQ, int G>
+__global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
+    using C = Cfg<D, BITS, NQ, G>;
+    constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
+    __shared__ float qf[NQ][D];
+    __shared__ __align__(16) uint32_t qfrag_all[kWarps][32 * C::QSTRIDE];
+    __shared__ float red_m[kWarps][NQ], red_l[kWarps][NQ];
+    __shared__ float red_o[kWarps][NQ][D];
+    __shared__ float red_z[kWarps][NQ][NGRP];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, i = lane & 3;
+    const int slot = blockIdx.y, split = blockIdx.x;
+    const int b = slot / a.Hkv, hk = slot % a.Hkv;
+    uint32_t* qfrag = qfrag_all[warp];
+
+    for (int idx = tid; idx < NQ * D; idx += kThreads) {
+        const int j = idx / D, c = idx % D;
+        qf[j][c] = __half2float(a.q[((long long)b * a.Hq + hk * NQ + j) * D + c]) * a.scale_log2;
+    }
+    for (int idx = lane; idx < 32 * C::QSTRIDE; idx += 32) qfrag[idx] = 0u;   // unused columns stay 0
+    __syncthreads();
+
+    // this lane's B column for the values: head hP, group slot jP, hi/lo
+    const int colP = g >> 1, hP = colP / GB, jP = colP % GB;
+    const bool lo_col = (g & 1) != 0;
+    const bool col_ok = hP < NQ;
+    // this lane's output columns (2i, 2i+1): head hO, group slot jO
+    const int hO = i / GB, jO = i % GB;
+
+    float m = -INFINITY, l = 0.f;
+    float o[KS][4];
+    float zeta[NBF];
+#pragma unroll
+    for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+#pragma unroll
+    for (int f = 0; f < NBF; ++f) zeta[f] = 0.f;
+
+    uint32_t qb[2 * KS];
+    float beta = 0.f;
+
+    // Online softmax step on the scores of tokens g and g+8 (head i); returns
+    // the probabilities of tokens 2i, 2i+1, 2i+8, 2i+9 of head hP.
+    auto softmax = [&](float s0, float s1, float (&pr)[4]) {
+        float mt = fmaxf(s0, s1);
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+        const float mn = fmaxf(m, mt);
+        if (__any_sync(kFull, mn > m)) {
+            const float alpha = exp2f(m - mn);
+            l *= alpha;
+            const float ao = __shfl_sync(kFull, alpha, (lane & ~3) | (hO < NQ ? hO : 0));
+#pragma unroll
+            for (int t = 0; t < KS; ++t) { o[t][0] *= ao; o[t][1] *= ao; o[t][2] *= ao; o[t][3] *= ao; }
+            const float az = __shfl_sync(kFull, alpha, col_ok ? hP : 0);
+#pragma unroll
+            for (int f = 0; f < NBF; ++f) zeta[f] *= az;
+            m = mn;
+        }
+        const float p0 = exp2f(s0 - m), p1 = exp2f(s1 - m);
+        l += p0 + p1;
+        const int src = 8 * i + (col_ok ? hP : 0);
+        pr[0] = __shfl_sync(kFull, p0, src);        // token 2i
+        pr[1] = __shfl_sync(kFull, p0, src + 4);    // token 2i+1
+        pr[2] = __shfl_sync(kFull, p1, src);        // token 2i+8
+        pr[3] = __shfl_sync(kFull, p1, src + 4);    // token 2i+9
+        if (!col_ok) pr[0] = pr[1] = pr[2] = pr[3] = 0.f;
+    };
+
+    // B fragment of P*step for one value fragment from the 4 tokens' (s, z) entries.
+    auto p_frag = [&](const float (&pr)[4], uint32_t ph01, uint32_t ph89, uint32_t pl01, uint32_t pl89,
+                      const uint32_t (&e)[4], uint32_t& b0, uint32_t& b1, float& z) {
+        const uint32_t s01 = __byte_perm(e[0], e[1], 0x5410), s89 = __byte_perm(e[2], e[3], 0x5410);
+        const uint32_t h01 = hmul2(ph01, s01), h89 = hmul2(ph89, s89);
+        const uint32_t l01 = hfma2(pl01, s01, hfma2(ph01, s01, neg_f16x2(h01)));
+        const uint32_t l89 = hfma2(pl89, s89, hfma2(ph89, s89, neg_f16x2(h89)));
+        b0 = lo_col ? l01 : h01;
+        b1 = lo_col ? l89 : h89;
+        const float2 z01 = unpack_f16x2(__byte_perm(e[0], e[1], 0x7632));
+        const float2 z89 = unpack_f16x2(__byte_perm(e[2], e[3], 0x7632));
+        z = fmaf(pr[0], z01.x, fmaf(pr[1], z01.y, fmaf(pr[2], z89.x, fmaf(pr[3], z89.y, z))));
+    };
+
+    auto split_p = [&](const float (&pr)[4], uint32_t& ph01, uint32_t& ph89, uint32_t& pl01, uint32_t& pl89) {
+        ph01 = pack_f16x2(pr[0], pr[1]);
+        ph89 = pack_f16x2(pr[2], pr[3]);
+        const float2 f01 = unpack_f16x2(ph01), f89 = unpack_f16x2(ph89);
+        pl01 = pack_f16x2(pr[0] - f01.x, pr[1] - f01.y);
+        pl89 = pack_f16x2(pr[2] - f89.x, pr[3] - f89.y);
+    };
+
+    const uint8_t* slot_base = a.cache + (long long)slot * a.slot_bytes;
+    if (split < a.n_qsplits) {
+        // ------------------------------ quantized tiles ------------------------------
+        const int t0 = split * a.tiles_per_split;
+        const int t1 = min(t0 + a.tiles_per_split, a.n_qtiles);
+        const int per_warp = (t1 - t0 + kWarps - 1) / kWarps;
+        const int tb = t0 + warp * per_warp, te = min(tb + per_warp, t1);
+        const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
+        const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
+
+        uint32_t kw[W], vw[W], ent[NBF][4];
+        auto fetch = [&](int T, uint32_t (&kwo)[W], uint32_t (&vwo)[W], uint32_t (&eo)[NBF][4]) {
+            const int blk = T / C::TPB, tin = T % C::TPB;
+            const uint8_t* kpart = slot_base + (long long)blk * a.part_bytes;
+            const uint8_t* vpart = kpart + a.NB * a.part_bytes;
+            load_tile_words<W>(kpart + tin * a.tile_bytes + lane * W * 4, kwo);
+            load_tile_words<W>(vpart + tin * a.tile_bytes + lane * W * 4, vwo);
+            const uint32_t* ve = reinterpret_cast<const uint32_t*>(vpart + tiles_bytes);
+            const int base = tin * 16;
+#pragma unroll
+            for (int f = 0; f < NBF; ++f) {
+                const int gr = f * GB + jP;
+                eo[f][0] = __ldg(ve + (base + tokA) * NGRP + gr);
+                eo[f][1] = __ldg(ve + (base + tokA + 1) * NGRP + gr);
+                eo[f][2] = __ldg(ve + (base + tokB) * NGRP + gr);
+                eo[f][3] = __ldg(ve + (base + tokB + 1) * NGRP + gr);
+            }
+        };
+        if (tb < te) fetch(tb, kw, vw, ent);
+        int cur_blk = -1;
+        for (int T = tb; T < te; ++T) {
+            uint32_t ckw[W], cvw[W], cent[NBF][4];
+#pragma unroll
+            for (int x = 0; x < W; ++x) { ckw[x] = kw[x]; cvw[x] = vw[x]; }
+#pragma unroll
+            for (int f = 0; f < NBF; ++f)
+#pragma unroll
+                for (int x = 0; x < 4; ++x) cent[f][x] = ent[f][x];
+            if (T + 1 < te) fetch(T + 1, kw, vw, ent);
+
+            const int blk = T / C::TPB;
+            if (blk != cur_blk) {
+                cur_blk = blk;
+                const uint32_t* ke = reinterpret_cast<const uint32_t*>(slot_base + (long long)blk * a.part_bytes + tiles_bytes);
+                build_q_frags<C, D, NQ>(ke, qf, qfrag, lane, qb, beta);
+            }
+            // keys: scores of tokens g, g+8 for head i
+            uint32_t w8[W];
+#pragma unroll
+            for (int x = 0; x < W; ++x) w8[x] = ckw[x] >> 8;
+            float c[4] = {beta, 0.f, beta, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t af[4];
+                a_frag<BITS, W>(ckw, w8, kk, af);
+                mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
+            }
+            float pr[4];
+            softmax(c[0] + c[1], c[2] + c[3], pr);
+            uint32_t ph01, ph89, pl01, pl89;
+            split_p(pr, ph01, ph89, pl01, pl89);
+            uint32_t pb[NBF][2];
+#pragma unroll
+            for (int f = 0; f < NBF; ++f) p_frag(pr, ph01, ph89, pl01, pl89, cent[f], pb[f][0], pb[f][1], zeta[f]);
+            // values
+#pragma unroll
+            for (int x = 0; x < W; ++x) w8[x] = cvw[x] >> 8;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t af[4];
+                a_frag<BITS, W>(cvw, w8, mt, af);
+                const int f = (16 * mt / G) / GB;
+                mma16816(o[mt], af, pb[f][0], pb[f][1]);
+            }
+        }
+    } else {
+        // ------------------------------ fp16 residual rows ------------------------------
+        const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + (long long)slot * a.R * D;
+        const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + (long long)slot * a.R * D;
+        const int n = a.n_resid, ntiles = (n + 15) / 16;
+        const int per_warp = (ntiles + kWarps - 1) / kWarps;
+        const int tb = warp * per_warp, te = min(tb + per_warp, ntiles);
+        if (tb < te) build_q_frags<C, D, NQ>(nullptr, qf, qfrag, lane, qb, beta);
+        for (int T = tb; T < te; ++T) {
+            const int r0 = T * 16;
+            const bool okg = r0 + g < n, okg8 = r0 + g + 8 < n;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const int ch = 16 * kk + 2 * i;
+                uint32_t af[4];
+                af[0] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g) * D + ch) : 0u;
+                af[1] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g + 8) * D + ch) : 0u;
+                af[2] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g) * D + ch + 8) : 0u;
+                af[3] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g + 8) * D + ch + 8) : 0u;
+                mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
+            }
+            float pr[4];
+            softmax(okg ? c[0] + c[1] : -INFINITY, okg8 ? c[2] + c[3] : -INFINITY, pr);
+            uint32_t ph01, ph89, pl01, pl89;
+            split_p(pr, ph01, ph89, pl01, pl89);
+            const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
+            const int tA = r0 + 2 * i, tB = r0 + 2 * i + 8;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int c0 = 16 * mt + g;
+                auto ld = [&](int t, int ch) -> uint32_t {
+                    return t < n ? (uint32_t)__half_as_ushort(vr[(long long)t * D + ch]) : 0u;
+                };
+                uint32_t af[4];
+                af[0] = ld(tA, c0) | (ld(tA + 1, c0) << 16);
+                af[1] = ld(tA, c0 + 8) | (ld(tA + 1, c0 + 8) << 16);
+                af[2] = ld(tB, c0) | (ld(tB + 1, c0) << 16);
+                af[3] = ld(tB, c0 + 8) | (ld(tB + 1, c0 + 8) << 16);
+                mma16816(o[mt], af, pb0, pb1);
+            }
+        }
+    }
+
+    // ------------------------------ merge the warps ------------------------------
+#pragma unroll
+    for (int f = 0; f < NBF; ++f) {
+        zeta[f] += __shfl_xor_sync(kFull, zeta[f], 1);
+        zeta[f] += __shfl_xor_sync(kFull, zeta[f], 2);
+    }
+    l += __shfl_xor_sync(kFull, l, 4);
+    l += __shfl_xor_sync(kFull, l, 8);
+    l += __shfl_xor_sync(kFull, l, 16);
+    if (g == 0 && i < NQ) { red_m[warp][i] = m; red_l[warp][i] = l; }
+    if (i == 0 && !lo_col && col_ok) {
+#pragma unroll
+        for (int f = 0; f < NBF; ++f) red_z[warp][hP][f * GB + jP] = zeta[f];
+    }
+    if (hO < NQ) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int gr = 16 * mt / G;
+            if (gr % GB == jO) {
+                red_o[warp][hO][16 * mt + g] = o[mt][0] + o[mt][1];
+                red_o[warp][hO][16 * mt + g + 8] = o[mt][2] + o[mt][3];
+            }
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < NQ * D; idx += kThreads) {
+        const int j = idx / D, c = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][j]);
+        float acc = 0.f, lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            if (red_m[w][j] == -INFINITY) continue;
+            const float e = exp2f(red_m[w][j] - M);
+            acc = fmaf(red_o[w][j][c] + red_z[w][j][c / G], e, acc);
+            lsum = fmaf(red_l[w][j], e, lsum);
+        }
+        float* pw = a.ws + ((long long)(b * a.Hq + hk * NQ + j) * kPartialSlots + split) * partial_stride(D);
+        if (c == 0) { pw[0] = M; pw[1] = lsum; }
+        pw[4 + c] = acc;
+    }
+}
+
+}  // namespace mma_detail
+}  // namespace kivi

@@ -56,6 +56,7 @@ def _load():
         "kivi_decode_attn": (I, [P, P, P, F, P, SZ, P]),
         "kivi_last_error_string": (ctypes.c_char_p, []),
         "kivi_launch_count": (ctypes.c_ulonglong, []),
+        "kivi_cache_set_decode_kernel": (I, [P, I]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -122,6 +123,13 @@ def kivi_decode_attn(h: int, q: int, out: int, softmax_scale: float, workspace: 
     _check(lib.kivi_decode_attn(h, q, out, softmax_scale, workspace, ws_bytes, stream))
 
 
+KIVI_DECODE_AUTO, KIVI_DECODE_CUDA_CORE, KIVI_DECODE_TENSOR_CORE = 0, 1, 2
+
+
+def kivi_cache_set_decode_kernel(h: int, kernel: int):
+    _check(lib.kivi_cache_set_decode_kernel(h, kernel))
+
+
 def kivi_last_error_string() -> str:
     return lib.kivi_last_error_string().decode()
 
@@ -165,6 +173,9 @@ class KiviCache:
 
     def counts(self):
         return kivi_cache_counts(self.handle)
+
+    def set_decode_kernel(self, kernel: int):
+        kivi_cache_set_decode_kernel(self.handle, kernel)
 
     def reset(self):
         kivi_cache_reset(self.handle)

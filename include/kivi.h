@@ -200,6 +200,22 @@ size_t kivi_decode_workspace_bytes(const kivi_config* cfg);
 kivi_status kivi_decode_attn(kivi_cache_t cache, const void* q, void* out, float softmax_scale,
                              void* workspace, size_t ws_bytes, kivi_stream_t stream);
 
+/*
+ * Which decode kernel kivi_decode_attn uses.  Both compute the same result
+ * within the same tolerance: the CUDA-core kernel accumulates fp32 products of
+ * the codes with q * step; the tensor-core kernel feeds exact fp16 codes and
+ * fp16 hi + lo splits of q * step (and of p * step) to mma.sync with fp32
+ * accumulation.  AUTO picks the faster one for the shape (the tensor-core
+ * kernel on sm_103a for every supported shape, from measurement).
+ */
+typedef enum {
+    KIVI_DECODE_AUTO = 0,
+    KIVI_DECODE_CUDA_CORE = 1,
+    KIVI_DECODE_TENSOR_CORE = 2
+} kivi_decode_kernel;
+
+kivi_status kivi_cache_set_decode_kernel(kivi_cache_t cache, int kernel);
+
 /* Description of the last failure on the calling thread ("" if none). */
 const char* kivi_last_error_string(void);
 

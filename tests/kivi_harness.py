@@ -16,7 +16,7 @@ RTOL_L2 = 1e-3   # ||out - oracle||_2 / ||oracle||_2
 
 
 def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RANGE_2_6_X10_50,
-            sink=True, max_tokens=None, prompt=None):
+            sink=True, max_tokens=None, prompt=None, decode_kernel=0):
     """Prefill L tokens, then n_app x append (decoding at the steps in decode_at).
 
     Returns dict(cache, K, V, steps=[(q,k,v)], outs={step: out fp16 cpu}).
@@ -24,6 +24,7 @@ def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RA
     syn = SynthKV(B, Hq, Hkv, D, seed, outliers=outliers, sink=sink, device="cuda")
     K, V = prompt if prompt is not None else syn.prompt(L)
     cache = KiviCache(B, Hq, Hkv, D, bits, G, R, max_tokens or max(L + n_app, 1))
+    cache.set_decode_kernel(decode_kernel)
     cache.prefill(K, V)
     steps, outs = [], {}
     for s in range(n_app):

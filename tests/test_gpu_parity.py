@@ -13,15 +13,19 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():  # pragma: no cover - collected on CPU hosts too
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from bit_kivi_kv_gb300.kivi import KiviCache, KiviError, KIVI_ERR_CAPACITY  # noqa: E402
+from bit_kivi_kv_gb300.kivi import (KIVI_DECODE_CUDA_CORE, KIVI_DECODE_TENSOR_CORE,  # noqa: E402
+                                    KIVI_ERR_CAPACITY, KiviCache, KiviError)
+
+KERNELS = {"cuda_core": KIVI_DECODE_CUDA_CORE, "tensor_core": KIVI_DECODE_TENSOR_CORE}
 from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50  # noqa: E402
 from kivi_harness import check_slots, run_gpu  # noqa: E402
 
 
-def test_tiny_single_step():
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_tiny_single_step(kernel):
     """B1 H1 D64, 2-bit, G32, R32: prefill 256 (224 quantized), append 1 (flush), decode."""
     run = run_gpu(1, 1, 1, 64, 2, 32, 32, L=256, n_app=1, seed=1000, decode_at={0},
-                  outliers=FIXED_4_X20, sink=False)
+                  outliers=FIXED_4_X20, sink=False, decode_kernel=KERNELS[kernel])
     assert run["cache"].counts() == (256, 1)
     check_slots(run, [(0, 0)], {0})
 
@@ -38,11 +42,13 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("case", SMALL, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}D{c[3]}b{c[4]}G{c[5]}R{c[6]}L{c[7]}n{c[8]}" for c in SMALL])
-def test_small_full_check(case):
+def test_small_full_check(case, kernel):
     B, Hq, Hkv, D, bits, G, R, L, n = case
     steps = {0, n // 2, n - 1}
-    run = run_gpu(B, Hq, Hkv, D, bits, G, R, L, n, seed=17 + sum(case), decode_at=steps)
+    run = run_gpu(B, Hq, Hkv, D, bits, G, R, L, n, seed=17 + sum(case), decode_at=steps,
+                  decode_kernel=KERNELS[kernel])
     check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
 
 
@@ -82,10 +88,12 @@ def _slots(B, Hkv):
     return sorted({(0, 0), (B - 1, Hkv - 1), (B // 2, Hkv // 3)})
 
 
-def test_llama2_7b_layer_full_size():
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_llama2_7b_layer_full_size(kernel):
     """B8 H32 D128, 2-bit G32 R128, prompt 4096 (sink + outliers), 64 decode steps."""
     steps = {0, 1, 31, 63}
-    run = run_gpu(8, 32, 32, 128, 2, 32, 128, 4096, 64, seed=1001, decode_at=steps)
+    run = run_gpu(8, 32, 32, 128, 2, 32, 128, 4096, 64, seed=1001, decode_at=steps,
+                  decode_kernel=KERNELS[kernel])
     assert run["cache"].counts() == (4096, 64)     # 3968 + one flush of 128; 64 appended
     check_slots(run, _slots(8, 32), steps)
 
@@ -110,3 +118,19 @@ def test_long_context_streaming_full_size():
     run = run_gpu(2, 32, 32, 128, 2, 32, 128, 131072, 512, seed=1004, decode_at=steps)
     assert run["cache"].counts() == (131072 + 384, 128)
     check_slots(run, [(0, 0), (1, 31)], steps)
+
+
+COMBOS = [(D, bits, nq, G) for D in (64, 128) for bits in (2, 4) for nq in (1, 2, 4)
+          for G in (32, 64, 128) if G <= D]
+
+
+@pytest.mark.parametrize("combo", COMBOS, ids=[f"D{c[0]}b{c[1]}nq{c[2]}G{c[3]}" for c in COMBOS])
+def test_every_tensor_core_instantiation(combo):
+    """Each (head_dim, bits, q-per-kv, G) kernel instance: ragged prompt, one
+    flush, decode over quantized + residual tokens."""
+    D, bits, nq, G = combo
+    R = max(G, 64)
+    L = 3 * G + R + 21
+    run = run_gpu(2, 2 * nq, 2, D, bits, G, R, L, R - 20, seed=sum(combo), decode_at={0, R - 21},
+                  decode_kernel=KIVI_DECODE_TENSOR_CORE)
+    check_slots(run, [(0, 0), (1, 1)], {0, R - 21})
