@@ -32,7 +32,8 @@ kivi_status derive_geometry(const kivi_config* cfg, Geometry* g, const char** wh
 constexpr int kMaxSplits = 64;          // quantized-token splits
 constexpr int kPartialSlots = kMaxSplits + 1;  // + one split for the fp16 residual
 
-// Floats per partial result (m, l, two pad, o[D]); D + 4 keeps o 16-byte aligned.
+// Floats per partial result (m, l, status, pad, o[D]); D + 4 keeps o 16-byte aligned.
+// status != 0 marks a split whose cache copy did not complete (its output is NaN).
 __host__ __device__ constexpr int partial_stride(int D) { return D + 4; }
 
 // ---- launchers (defined in the .cu files; return the launch status) -------

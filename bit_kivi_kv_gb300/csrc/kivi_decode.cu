@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
         }
         float* pw = a.ws + ((long long)(b * a.Hq + hk * NQ + j) * kPartialSlots + split) * partial_stride(D);
         if (c == 0) { pw[0] = M; pw[1] = lsum; }
+        if (c == 1) pw[2] = 0.f;
         pw[4 + c] = o;
     }
 }
@@ -289,14 +290,16 @@ __global__ void __launch_bounds__(D) combine_kernel(const float* ws, __half* out
     float M = -INFINITY;
     for (int s = 0; s < n_splits; ++s) M = fmaxf(M, base[s * partial_stride(D)]);
     float o = 0.f, lsum = 0.f;
+    bool failed = false;
     for (int s = 0; s < n_splits; ++s) {
         const float* ps = base + s * partial_stride(D);
+        failed |= ps[2] != 0.f;            // a split whose data copy timed out
         if (ps[0] == -INFINITY) continue;
         const float e = exp2f(ps[0] - M);
         lsum = fmaf(ps[1], e, lsum);
         o = fmaf(ps[4 + c], e, o);
     }
-    out[bh * D + c] = __float2half_rn(o / lsum);
+    out[bh * D + c] = failed ? __float2half_rn(NAN) : __float2half_rn(o / lsum);
 }
 
 template <int D, int BITS, int NQ>

@@ -86,6 +86,53 @@ __device__ __forceinline__ uint2 ldg_stream2(const void* p) {
     return v;
 }
 
+// ---- 1-D bulk copies (TMA) into shared memory, completed on an mbarrier ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for phase `parity` of an mbarrier, giving up after about 2 seconds
+// (or 2^26 polls); returns false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (global_ns() - t0 > 2000000000ull) return false;
+    }
+    return false;
+}
+
 // Exact f16x2 pair of codes of slot u of a tile word (w8 = w >> 8).
 template <int BITS>
 __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int u) {
@@ -136,6 +183,12 @@ struct Cfg {
     static constexpr int NBF = NGRP / GB;             // B fragments per tile (values)
     static constexpr int QSTRIDE = 2 * KSTEPS + 4;    // u32 per lane row of the Qt fragment table
     static constexpr int TPB = G / 16;                // tiles per block
+    static constexpr int TILE = 2 * D * BITS;         // bytes of one code tile
+    static constexpr int ENT = 16 * NGRP * 4;         // value (step, zero) entries of one tile
+    static constexpr int KSZ = 4 * D;                 // key (step, zero) entries of one block
+    static constexpr int STAGES = 4;                  // ring depth per warp
+    static constexpr int STAGE_BYTES = 2 * TILE + ENT + KSZ;
+    static constexpr int DYN_SMEM = kWarps * STAGES * STAGE_BYTES;
 };
 
 // Build this warp's Qt B fragments (hi/lo of q_h * step) and its beta, from
@@ -195,6 +248,10 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     __shared__ float red_m[kWarps][NQ], red_l[kWarps][NQ];
     __shared__ float red_o[kWarps][NQ][D];
     __shared__ float red_z[kWarps][NQ][NGRP];
+    __shared__ __align__(8) uint64_t full_bar[kWarps][C::STAGES];
+    __shared__ uint32_t red_status;
+    extern __shared__ __align__(128) uint8_t dyn_smem[];
+    uint32_t status = 0;   // 1: a bulk copy did not complete in time
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, i = lane & 3;
@@ -207,6 +264,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         qf[j][c] = __half2float(a.q[((long long)b * a.Hq + hk * NQ + j) * D + c]) * a.scale_log2;
     }
     for (int idx = lane; idx < 32 * C::QSTRIDE; idx += 32) qfrag[idx] = 0u;   // unused columns stay 0
+    if (tid == 0) red_status = 0u;
     __syncthreads();
 
     // this lane's B column for the values: head hP, group slot jP, hi/lo
@@ -281,49 +339,70 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     const uint8_t* slot_base = a.cache + (long long)slot * a.slot_bytes;
     if (split < a.n_qsplits) {
         // ------------------------------ quantized tiles ------------------------------
+        // Each warp streams its run of tiles through a STAGES-deep ring in shared
+        // memory; lane 0 issues the bulk copies, every lane waits on the stage's
+        // mbarrier, and a stage is refilled once the warp is done with it.
         const int t0 = split * a.tiles_per_split;
         const int t1 = min(t0 + a.tiles_per_split, a.n_qtiles);
         const int per_warp = (t1 - t0 + kWarps - 1) / kWarps;
         const int tb = t0 + warp * per_warp, te = min(tb + per_warp, t1);
         const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
         const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
-
-        uint32_t kw[W], vw[W], ent[NBF][4];
-        auto fetch = [&](int T, uint32_t (&kwo)[W], uint32_t (&vwo)[W], uint32_t (&eo)[NBF][4]) {
+        uint8_t* ring = dyn_smem + warp * C::STAGES * C::STAGE_BYTES;
+        uint64_t* bars = full_bar[warp];
+        if (lane == 0) {
+#pragma unroll
+            for (int st = 0; st < C::STAGES; ++st) mbar_init(&bars[st], 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        auto need_ksz = [&](int T) { return T == tb || (T % C::TPB) == 0; };
+        auto issue = [&](int T, int st) {            // lane 0
             const int blk = T / C::TPB, tin = T % C::TPB;
             const uint8_t* kpart = slot_base + (long long)blk * a.part_bytes;
             const uint8_t* vpart = kpart + a.NB * a.part_bytes;
-            load_tile_words<W>(kpart + tin * a.tile_bytes + lane * W * 4, kwo);
-            load_tile_words<W>(vpart + tin * a.tile_bytes + lane * W * 4, vwo);
-            const uint32_t* ve = reinterpret_cast<const uint32_t*>(vpart + tiles_bytes);
-            const int base = tin * 16;
+            uint8_t* dst = ring + st * C::STAGE_BYTES;
+            const bool kz = need_ksz(T);
+            mbar_expect_tx(&bars[st], 2 * C::TILE + C::ENT + (kz ? C::KSZ : 0));
+            tma_1d(dst, kpart + tin * C::TILE, C::TILE, &bars[st]);
+            tma_1d(dst + C::TILE, vpart + tin * C::TILE, C::TILE, &bars[st]);
+            tma_1d(dst + 2 * C::TILE, vpart + tiles_bytes + tin * C::ENT, C::ENT, &bars[st]);
+            if (kz) tma_1d(dst + 2 * C::TILE + C::ENT, kpart + tiles_bytes, C::KSZ, &bars[st]);
+        };
+        if (lane == 0) {
+            for (int k = 0; k < C::STAGES && tb + k < te; ++k) issue(tb + k, k);
+        }
+        int T = tb;
+        for (; T < te; ++T) {
+            const int k = T - tb, st = k % C::STAGES;
+            if (!__all_sync(kFull, mbar_wait(&bars[st], (uint32_t)(k / C::STAGES) & 1u))) break;
+            const uint8_t* stage = ring + st * C::STAGE_BYTES;
+            uint32_t ckw[W], cvw[W], cent[NBF][4];
+            if constexpr (W % 4 == 0) {
+#pragma unroll
+                for (int v = 0; v < W / 4; ++v) {
+                    const uint4 x = reinterpret_cast<const uint4*>(stage + lane * W * 4)[v];
+                    ckw[4 * v] = x.x; ckw[4 * v + 1] = x.y; ckw[4 * v + 2] = x.z; ckw[4 * v + 3] = x.w;
+                    const uint4 y = reinterpret_cast<const uint4*>(stage + C::TILE + lane * W * 4)[v];
+                    cvw[4 * v] = y.x; cvw[4 * v + 1] = y.y; cvw[4 * v + 2] = y.z; cvw[4 * v + 3] = y.w;
+                }
+            } else {
+                const uint2 x = *reinterpret_cast<const uint2*>(stage + lane * W * 4);
+                const uint2 y = *reinterpret_cast<const uint2*>(stage + C::TILE + lane * W * 4);
+                ckw[0] = x.x; ckw[1] = x.y; cvw[0] = y.x; cvw[1] = y.y;
+            }
+            const uint32_t* ve = reinterpret_cast<const uint32_t*>(stage + 2 * C::TILE);
 #pragma unroll
             for (int f = 0; f < NBF; ++f) {
                 const int gr = f * GB + jP;
-                eo[f][0] = __ldg(ve + (base + tokA) * NGRP + gr);
-                eo[f][1] = __ldg(ve + (base + tokA + 1) * NGRP + gr);
-                eo[f][2] = __ldg(ve + (base + tokB) * NGRP + gr);
-                eo[f][3] = __ldg(ve + (base + tokB + 1) * NGRP + gr);
+                cent[f][0] = ve[tokA * NGRP + gr];
+                cent[f][1] = ve[(tokA + 1) * NGRP + gr];
+                cent[f][2] = ve[tokB * NGRP + gr];
+                cent[f][3] = ve[(tokB + 1) * NGRP + gr];
             }
-        };
-        if (tb < te) fetch(tb, kw, vw, ent);
-        int cur_blk = -1;
-        for (int T = tb; T < te; ++T) {
-            uint32_t ckw[W], cvw[W], cent[NBF][4];
-#pragma unroll
-            for (int x = 0; x < W; ++x) { ckw[x] = kw[x]; cvw[x] = vw[x]; }
-#pragma unroll
-            for (int f = 0; f < NBF; ++f)
-#pragma unroll
-                for (int x = 0; x < 4; ++x) cent[f][x] = ent[f][x];
-            if (T + 1 < te) fetch(T + 1, kw, vw, ent);
-
-            const int blk = T / C::TPB;
-            if (blk != cur_blk) {
-                cur_blk = blk;
-                const uint32_t* ke = reinterpret_cast<const uint32_t*>(slot_base + (long long)blk * a.part_bytes + tiles_bytes);
-                build_q_frags<C, D, NQ>(ke, qf, qfrag, lane, qb, beta);
-            }
+            if (need_ksz(T))
+                build_q_frags<C, D, NQ>(reinterpret_cast<const uint32_t*>(stage + 2 * C::TILE + C::ENT), qf, qfrag,
+                                        lane, qb, beta);
             // keys: scores of tokens g, g+8 for head i
             uint32_t w8[W];
 #pragma unroll
@@ -351,6 +430,19 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                 a_frag<BITS, W>(cvw, w8, mt, af);
                 const int f = (16 * mt / G) / GB;
                 mma16816(o[mt], af, pb[f][0], pb[f][1]);
+            }
+            __syncwarp();                              // every lane is done with this stage
+            if (lane == 0 && T + C::STAGES < te) {
+                fence_proxy_async();
+                issue(T + C::STAGES, st);
+            }
+        }
+        if (T < te) {
+            // a copy timed out: flag it, then wait (bounded) for this warp's copies in flight
+            status = 1;
+            for (int U = T; U < te && U < T + C::STAGES; ++U) {
+                const int k = U - tb;
+                mbar_wait(&bars[k % C::STAGES], (uint32_t)(k / C::STAGES) & 1u);
             }
         }
     } else {
@@ -407,6 +499,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     l += __shfl_xor_sync(kFull, l, 8);
     l += __shfl_xor_sync(kFull, l, 16);
     if (g == 0 && i < NQ) { red_m[warp][i] = m; red_l[warp][i] = l; }
+    if (status && lane == 0) atomicOr(&red_status, status);
     if (i == 0 && !lo_col && col_ok) {
 #pragma unroll
         for (int f = 0; f < NBF; ++f) red_z[warp][hP][f * GB + jP] = zeta[f];
@@ -437,6 +530,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         }
         float* pw = a.ws + ((long long)(b * a.Hq + hk * NQ + j) * kPartialSlots + split) * partial_stride(D);
         if (c == 0) { pw[0] = M; pw[1] = lsum; }
+        if (c == 1) pw[2] = (float)red_status;
         pw[4 + c] = acc;
     }
 }
