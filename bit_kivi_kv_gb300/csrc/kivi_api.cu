@@ -260,3 +260,14 @@ const char* kivi_last_error_string(void) { return g_err; }
 unsigned long long kivi_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+namespace kivi {
+
+kivi_status report_error(kivi_status st, const char* msg) { return fail(st, "%s", msg); }
+
+size_t decode_workspace_need(const kivi_cache* c) {
+    const Geometry& g = c->geo;
+    return (size_t)g.B * g.Hq * kPartialSlots * partial_stride(g.D) * sizeof(float);
+}
+
+}  // namespace kivi

@@ -64,4 +64,9 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
                           float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
                           int* launches);
 
+// Host-side helpers of the C ABI (kivi_api.cu): set the calling thread's
+// error string and return st; the decode workspace bytes a handle needs.
+kivi_status report_error(kivi_status st, const char* msg);
+size_t decode_workspace_need(const struct ::kivi_cache* c);
+
 }  // namespace kivi

@@ -57,6 +57,7 @@ def _load():
         "kivi_last_error_string": (ctypes.c_char_p, []),
         "kivi_launch_count": (ctypes.c_ulonglong, []),
         "kivi_cache_set_decode_kernel": (I, [P, I]),
+        "kivi_decode_attn_static_ws": (I, [P, P, P, F, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -121,6 +122,11 @@ def kivi_decode_workspace_bytes(cfg: kivi_config) -> int:
 
 def kivi_decode_attn(h: int, q: int, out: int, softmax_scale: float, workspace: int, ws_bytes: int, stream: int):
     _check(lib.kivi_decode_attn(h, q, out, softmax_scale, workspace, ws_bytes, stream))
+
+
+def kivi_decode_attn_static_ws(h: int, q: int, out: int, softmax_scale: float, stream: int):
+    """Decode with the library's static workspace (for callers that cannot allocate)."""
+    _check(lib.kivi_decode_attn_static_ws(h, q, out, softmax_scale, stream))
 
 
 KIVI_DECODE_AUTO, KIVI_DECODE_CUDA_CORE, KIVI_DECODE_TENSOR_CORE = 0, 1, 2

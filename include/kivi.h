@@ -216,6 +216,28 @@ typedef enum {
 
 kivi_status kivi_cache_set_decode_kernel(kivi_cache_t cache, int kernel);
 
+/*
+ * Decode attention with a workspace owned by the library (the method's
+ * description has no counterpart; this is an integration aid).
+ *
+ * For callers that cannot allocate device memory: a plugin inside a host
+ * framework that owns all device memory through its own pool (a raw
+ * cudaMalloc is refused there, or would synchronize the device), or code that
+ * only receives device pointers.  Same arguments and result as
+ * kivi_decode_attn, minus the workspace: the library keeps one 16 MiB
+ * workspace per device in a static device array, which every device that
+ * loads the library holds until the process exits.  Shapes whose
+ * kivi_decode_workspace_bytes() exceeds 16 MiB (batch * n_q_heads above 488
+ * at head_dim 128, above 948 at head_dim 64) get KIVI_ERR_CAPACITY.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  No call
+ * allocates memory.  All calls on a device share the one workspace, so two
+ * calls whose kernels overlap on the GPU (different streams, no ordering
+ * between them) race and may return wrong results; serialize them.
+ */
+kivi_status kivi_decode_attn_static_ws(kivi_cache_t cache, const void* q, void* out,
+                                       float softmax_scale, kivi_stream_t stream);
+
 /* Description of the last failure on the calling thread ("" if none). */
 const char* kivi_last_error_string(void);
 
