@@ -324,6 +324,7 @@ DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, 
     if (tps < 8) tps = 8;
     const long long cap = (n_qtiles + kMaxSplits - 1) / kMaxSplits;
     if (tps < cap) tps = cap;
+    tps = (tps + 1) & ~1LL;   // whole tile pairs (the tensor-core kernel takes two tiles per stage)
     p.tiles_per_split = (int)tps;
     p.n_qsplits = n_qtiles ? (int)((n_qtiles + tps - 1) / tps) : 0;
     p.n_splits = p.n_qsplits + (n_resid > 0 ? 1 : 0);

@@ -17,11 +17,16 @@
 //            one fragment per 16-token tile; a lane keeps the accumulators of
 //            the column pair that matches its channels' group.
 //
-// Codes come out of the tile words exactly: a code field masked into an fp16
-// mantissa with exponent 2^10 gives 1024 + 4^u * code, and one f16x2 FMA with
-// (4^-u, -1024 * 4^-u) returns the code (all values exact in fp16).
+// Codes enter the MMA without arithmetic: each tile word is shifted so a code
+// field sits at bit 6 or 8 of an fp16 mantissa whose exponent is 2^10, which
+// reads as 1024 + 2^pos * code (exact).  The 1024 offset is removed exactly by
+// MMAs with a constant -1024 A operand (keys: once per block, as the
+// accumulator's start; values: a side accumulator), and the 2^-pos factor is
+// applied to the results.  Offset and value stay within a factor ~10 of each
+// other, so fp32 accumulation keeps ~20 bits of the result.
 // Online softmax per warp in the log2 domain; each warp owns a contiguous run
-// of the split's 16-token tiles; warps and splits merge by log-sum-exp.
+// of the split's tiles, taken two tiles (32 tokens) per ring stage; warps and
+// splits merge by log-sum-exp.
 #pragma once
 
 #include <math.h>
@@ -115,22 +120,31 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for phase `parity` of an mbarrier, giving up after about 2 seconds
 // (or 2^26 polls); returns false on time-out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     const uint32_t addr = smem_u32(bar);
+    if (mbar_try(addr, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 0; it < (1u << 26); ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(ok)
-            : "r"(addr), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (global_ns() - t0 > 2000000000ull) return false;
+        if (mbar_try(addr, parity)) return true;
+        if ((it & 63u) == 63u && global_ns() - t0 > 2000000000ull) return false;
     }
     return false;
+}
+__device__ __forceinline__ float fast_exp2(float x) {   // hardware 2^x (ex2.approx, rel. err ~2^-22)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Exact f16x2 pair of codes of slot u of a tile word (w8 = w >> 8).
@@ -147,6 +161,32 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int u) {
     const uint32_t sc = (uint32_t)(15 - e) << 10;               // 2^-e
     const uint32_t bi = 0x8000u | ((uint32_t)(25 - e) << 10);   // -2^(10-e)
     return hfma2(x, sc | (sc << 16), bi | (bi << 16));
+}
+
+// f16x2 pair of codes of slot u, left as 1024 + 2^pos * code: the word is
+// shifted so the field lands at mantissa bits [pos, pos + BITS).  For 2-bit
+// codes even slots land at pos 8 and odd slots at pos 6; 4-bit codes at pos 6.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair_raw(uint32_t w, int u) {
+    if constexpr (BITS == 2) {
+        const int sh = u == 0 ? 8 : u <= 2 ? 4 : u <= 4 ? 0 : u <= 6 ? -4 : -8;
+        const uint32_t src = sh > 0 ? (w << sh) : sh < 0 ? (w >> (-sh)) : w;
+        return (src & ((u & 1) ? 0x00C000C0u : 0x03000300u)) | 0x64006400u;
+    } else {
+        const int sh = 6 - 4 * u;
+        const uint32_t src = sh > 0 ? (w << sh) : (w >> (-sh));
+        return (src & 0x03C003C0u) | 0x64006400u;
+    }
+}
+
+template <int BITS, int W>
+__device__ __forceinline__ void a_frag_raw(const uint32_t (&w)[W], int kk, uint32_t (&a)[4]) {
+    constexpr int PER = 16 / BITS;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int p = 4 * kk + r;
+        a[r] = code_pair_raw<BITS>(w[p / PER], p % PER);
+    }
 }
 
 // A fragment (4 registers) of k-step / m-tile kk from a lane's tile words.
@@ -186,9 +226,14 @@ struct Cfg {
     static constexpr int TILE = 2 * D * BITS;         // bytes of one code tile
     static constexpr int ENT = 16 * NGRP * 4;         // value (step, zero) entries of one tile
     static constexpr int KSZ = 4 * D;                 // key (step, zero) entries of one block
-    static constexpr int STAGES = 4;                  // ring depth per warp
-    static constexpr int STAGE_BYTES = 2 * TILE + ENT + KSZ;
+    static constexpr int STAGES = BITS == 2 ? 3 : 2;   // ring depth per warp (stages of 2 tiles)
+    // a stage: key words of 2 tiles, value words of 2 tiles, their value
+    // entries, and the block's key entries
+    static constexpr int STAGE_BYTES = 4 * TILE + 2 * ENT + KSZ;
     static constexpr int DYN_SMEM = kWarps * STAGES * STAGE_BYTES;
+    // mantissa position of the codes of A rows g (even slots) and g+8 (odd slots)
+    static constexpr int POS_EVEN = BITS == 2 ? 8 : 6;
+    static constexpr int POS_ODD = 6;
 };
 
 // Build this warp's Qt B fragments (hi/lo of q_h * step) and its beta, from
@@ -276,36 +321,45 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 
     float m = -INFINITY, l = 0.f;
     float o[KS][4];
+    float voff[NBF][4];   // -1024 * sum_t Pt[t][n]: removes the code offset of the value MMAs
     float zeta[NBF];
 #pragma unroll
     for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
 #pragma unroll
-    for (int f = 0; f < NBF; ++f) zeta[f] = 0.f;
+    for (int f = 0; f < NBF; ++f) zeta[f] = voff[f][0] = voff[f][1] = voff[f][2] = voff[f][3] = 0.f;
+    const uint32_t kNeg1024[4] = {0xE400E400u, 0xE400E400u, 0xE400E400u, 0xE400E400u};
 
     uint32_t qb[2 * KS];
     float beta = 0.f;
 
-    // Online softmax step on the scores of tokens g and g+8 (head i); returns
-    // the probabilities of tokens 2i, 2i+1, 2i+8, 2i+9 of head hP.
-    auto softmax = [&](float s0, float s1, float (&pr)[4]) {
-        float mt = fmaxf(s0, s1);
+    // Online softmax step over two tiles: sc = logits of tokens g, g+8 of tile
+    // A and of tile B (head i); p receives their probabilities.
+    auto softmax = [&](const float (&sc)[4], float (&p)[4]) {
+        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
         const float mn = fmaxf(m, mt);
         if (__any_sync(kFull, mn > m)) {
-            const float alpha = exp2f(m - mn);
+            const float alpha = fast_exp2(m - mn);
             l *= alpha;
             const float ao = __shfl_sync(kFull, alpha, (lane & ~3) | (hO < NQ ? hO : 0));
 #pragma unroll
             for (int t = 0; t < KS; ++t) { o[t][0] *= ao; o[t][1] *= ao; o[t][2] *= ao; o[t][3] *= ao; }
+#pragma unroll
+            for (int f = 0; f < NBF; ++f) { voff[f][0] *= ao; voff[f][1] *= ao; voff[f][2] *= ao; voff[f][3] *= ao; }
             const float az = __shfl_sync(kFull, alpha, col_ok ? hP : 0);
 #pragma unroll
             for (int f = 0; f < NBF; ++f) zeta[f] *= az;
             m = mn;
         }
-        const float p0 = exp2f(s0 - m), p1 = exp2f(s1 - m);
-        l += p0 + p1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[j] = fast_exp2(sc[j] - m);
+        l += (p[0] + p[1]) + (p[2] + p[3]);
+    };
+    // probabilities of tokens 2i, 2i+1, 2i+8, 2i+9 of head hP from (p0, p1) =
+    // the probabilities of tokens g, g+8 held by every lane
+    auto gather = [&](float p0, float p1, float (&pr)[4]) {
         const int src = 8 * i + (col_ok ? hP : 0);
         pr[0] = __shfl_sync(kFull, p0, src);        // token 2i
         pr[1] = __shfl_sync(kFull, p0, src + 4);    // token 2i+1
@@ -339,13 +393,14 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     const uint8_t* slot_base = a.cache + (long long)slot * a.slot_bytes;
     if (split < a.n_qsplits) {
         // ------------------------------ quantized tiles ------------------------------
-        // Each warp streams its run of tiles through a STAGES-deep ring in shared
-        // memory; lane 0 issues the bulk copies, every lane waits on the stage's
-        // mbarrier, and a stage is refilled once the warp is done with it.
-        const int t0 = split * a.tiles_per_split;
-        const int t1 = min(t0 + a.tiles_per_split, a.n_qtiles);
-        const int per_warp = (t1 - t0 + kWarps - 1) / kWarps;
-        const int tb = t0 + warp * per_warp, te = min(tb + per_warp, t1);
+        // Each warp streams its run of tiles, two per stage, through a STAGES-deep
+        // ring in shared memory; lane 0 issues the bulk copies, every lane waits on
+        // the stage's mbarrier, and a stage is refilled once the warp is done with it.
+        const int t0 = split * a.tiles_per_split;                  // even
+        const int t1 = min(t0 + a.tiles_per_split, a.n_qtiles);    // even
+        const int per_warp = (((t1 - t0 + kWarps - 1) / kWarps) + 1) & ~1;
+        const int tb = min(t0 + warp * per_warp, t1), te = min(tb + per_warp, t1);
+        const int npairs = (te - tb) / 2;
         const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
         const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
         uint8_t* ring = dyn_smem + warp * C::STAGES * C::STAGE_BYTES;
@@ -357,93 +412,120 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         }
         __syncwarp();
         auto need_ksz = [&](int T) { return T == tb || (T % C::TPB) == 0; };
-        auto issue = [&](int T, int st) {            // lane 0
+        auto issue = [&](int k, int st) {            // lane 0: stage st <- tiles tb+2k, tb+2k+1
+            const int T = tb + 2 * k;
             const int blk = T / C::TPB, tin = T % C::TPB;
             const uint8_t* kpart = slot_base + (long long)blk * a.part_bytes;
             const uint8_t* vpart = kpart + a.NB * a.part_bytes;
             uint8_t* dst = ring + st * C::STAGE_BYTES;
             const bool kz = need_ksz(T);
-            mbar_expect_tx(&bars[st], 2 * C::TILE + C::ENT + (kz ? C::KSZ : 0));
-            tma_1d(dst, kpart + tin * C::TILE, C::TILE, &bars[st]);
-            tma_1d(dst + C::TILE, vpart + tin * C::TILE, C::TILE, &bars[st]);
-            tma_1d(dst + 2 * C::TILE, vpart + tiles_bytes + tin * C::ENT, C::ENT, &bars[st]);
-            if (kz) tma_1d(dst + 2 * C::TILE + C::ENT, kpart + tiles_bytes, C::KSZ, &bars[st]);
+            mbar_expect_tx(&bars[st], 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
+            tma_1d(dst, kpart + tin * C::TILE, 2 * C::TILE, &bars[st]);
+            tma_1d(dst + 2 * C::TILE, vpart + tin * C::TILE, 2 * C::TILE, &bars[st]);
+            tma_1d(dst + 4 * C::TILE, vpart + tiles_bytes + tin * C::ENT, 2 * C::ENT, &bars[st]);
+            if (kz) tma_1d(dst + 4 * C::TILE + 2 * C::ENT, kpart + tiles_bytes, C::KSZ, &bars[st]);
         };
         if (lane == 0) {
-            for (int k = 0; k < C::STAGES && tb + k < te; ++k) issue(tb + k, k);
+            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue(k, k);
         }
-        int T = tb;
-        for (; T < te; ++T) {
-            const int k = T - tb, st = k % C::STAGES;
-            if (!__all_sync(kFull, mbar_wait(&bars[st], (uint32_t)(k / C::STAGES) & 1u))) break;
-            const uint8_t* stage = ring + st * C::STAGE_BYTES;
-            uint32_t ckw[W], cvw[W], cent[NBF][4];
+        auto lds_words = [&](const uint8_t* src, uint32_t (&w)[W]) {
             if constexpr (W % 4 == 0) {
 #pragma unroll
                 for (int v = 0; v < W / 4; ++v) {
-                    const uint4 x = reinterpret_cast<const uint4*>(stage + lane * W * 4)[v];
-                    ckw[4 * v] = x.x; ckw[4 * v + 1] = x.y; ckw[4 * v + 2] = x.z; ckw[4 * v + 3] = x.w;
-                    const uint4 y = reinterpret_cast<const uint4*>(stage + C::TILE + lane * W * 4)[v];
-                    cvw[4 * v] = y.x; cvw[4 * v + 1] = y.y; cvw[4 * v + 2] = y.z; cvw[4 * v + 3] = y.w;
+                    const uint4 x = reinterpret_cast<const uint4*>(src + lane * W * 4)[v];
+                    w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
                 }
             } else {
-                const uint2 x = *reinterpret_cast<const uint2*>(stage + lane * W * 4);
-                const uint2 y = *reinterpret_cast<const uint2*>(stage + C::TILE + lane * W * 4);
-                ckw[0] = x.x; ckw[1] = x.y; cvw[0] = y.x; cvw[1] = y.y;
+                const uint2 x = *reinterpret_cast<const uint2*>(src + lane * W * 4);
+                w[0] = x.x; w[1] = x.y;
             }
-            const uint32_t* ve = reinterpret_cast<const uint32_t*>(stage + 2 * C::TILE);
+        };
+        constexpr float kScaleEven = 1.0f / (float)(1 << C::POS_EVEN);
+        constexpr float kScaleOdd = 1.0f / (float)(1 << C::POS_ODD);
+        float cinit[4] = {0.f, 0.f, 0.f, 0.f};   // -1024 * sum_c Qt[c][n] of the current block
+        int k = 0;
+        for (; k < npairs; ++k) {
+            const int st = k % C::STAGES;
+            if (!__all_sync(kFull, mbar_wait(&bars[st], (uint32_t)(k / C::STAGES) & 1u))) break;
+            const uint8_t* stage = ring + st * C::STAGE_BYTES;
+            const int T = tb + 2 * k;
+            if (need_ksz(T)) {
+                build_q_frags<C, D, NQ>(reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + 2 * C::ENT), qf,
+                                        qfrag, lane, qb, beta);
+                cinit[0] = cinit[1] = cinit[2] = cinit[3] = 0.f;
 #pragma unroll
-            for (int f = 0; f < NBF; ++f) {
-                const int gr = f * GB + jP;
-                cent[f][0] = ve[tokA * NGRP + gr];
-                cent[f][1] = ve[(tokA + 1) * NGRP + gr];
-                cent[f][2] = ve[tokB * NGRP + gr];
-                cent[f][3] = ve[(tokB + 1) * NGRP + gr];
+                for (int kk = 0; kk < KS; ++kk) mma16816(cinit, kNeg1024, qb[2 * kk], qb[2 * kk + 1]);
             }
-            if (need_ksz(T))
-                build_q_frags<C, D, NQ>(reinterpret_cast<const uint32_t*>(stage + 2 * C::TILE + C::ENT), qf, qfrag,
-                                        lane, qb, beta);
-            // keys: scores of tokens g, g+8 for head i
-            uint32_t w8[W];
+            // keys: logits of tokens g, g+8 of both tiles for head i
+            float sc[4];
+            {
+                uint32_t wa[W], wb[W];
+                lds_words(stage, wa);
+                lds_words(stage + C::TILE, wb);
+                float ca[4] = {cinit[0], cinit[1], cinit[2], cinit[3]};
+                float cb[4] = {cinit[0], cinit[1], cinit[2], cinit[3]};
 #pragma unroll
-            for (int x = 0; x < W; ++x) w8[x] = ckw[x] >> 8;
-            float c[4] = {beta, 0.f, beta, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t af[4];
-                a_frag<BITS, W>(ckw, w8, kk, af);
-                mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t fa[4], fb[4];
+                    a_frag_raw<BITS, W>(wa, kk, fa);
+                    a_frag_raw<BITS, W>(wb, kk, fb);
+                    mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
+                    mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
+                }
+                sc[0] = fmaf(ca[0] + ca[1], kScaleEven, beta);
+                sc[1] = fmaf(ca[2] + ca[3], kScaleOdd, beta);
+                sc[2] = fmaf(cb[0] + cb[1], kScaleEven, beta);
+                sc[3] = fmaf(cb[2] + cb[3], kScaleOdd, beta);
             }
-            float pr[4];
-            softmax(c[0] + c[1], c[2] + c[3], pr);
-            uint32_t ph01, ph89, pl01, pl89;
-            split_p(pr, ph01, ph89, pl01, pl89);
-            uint32_t pb[NBF][2];
+            float p[4];
+            softmax(sc, p);
+            // values, tile by tile
 #pragma unroll
-            for (int f = 0; f < NBF; ++f) p_frag(pr, ph01, ph89, pl01, pl89, cent[f], pb[f][0], pb[f][1], zeta[f]);
-            // values
+            for (int t = 0; t < 2; ++t) {
+                float pr[4];
+                gather(p[2 * t], p[2 * t + 1], pr);
+                uint32_t ph01, ph89, pl01, pl89;
+                split_p(pr, ph01, ph89, pl01, pl89);
+                const uint32_t* ve = reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + t * C::ENT);
+                uint32_t pb[NBF][2];
 #pragma unroll
-            for (int x = 0; x < W; ++x) w8[x] = cvw[x] >> 8;
+                for (int f = 0; f < NBF; ++f) {
+                    const int gr = f * GB + jP;
+                    const uint32_t e[4] = {ve[tokA * NGRP + gr], ve[(tokA + 1) * NGRP + gr], ve[tokB * NGRP + gr],
+                                           ve[(tokB + 1) * NGRP + gr]};
+                    p_frag(pr, ph01, ph89, pl01, pl89, e, pb[f][0], pb[f][1], zeta[f]);
+                    mma16816(voff[f], kNeg1024, pb[f][0], pb[f][1]);
+                }
+                uint32_t wv[W];
+                lds_words(stage + (2 + t) * C::TILE, wv);
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                uint32_t af[4];
-                a_frag<BITS, W>(cvw, w8, mt, af);
-                const int f = (16 * mt / G) / GB;
-                mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t af[4];
+                    a_frag_raw<BITS, W>(wv, mt, af);
+                    const int f = (16 * mt / G) / GB;
+                    mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                }
             }
             __syncwarp();                              // every lane is done with this stage
-            if (lane == 0 && T + C::STAGES < te) {
+            if (lane == 0 && k + C::STAGES < npairs) {
                 fence_proxy_async();
-                issue(T + C::STAGES, st);
+                issue(k + C::STAGES, st);
             }
         }
-        if (T < te) {
+        if (k < npairs) {
             // a copy timed out: flag it, then wait (bounded) for this warp's copies in flight
             status = 1;
-            for (int U = T; U < te && U < T + C::STAGES; ++U) {
-                const int k = U - tb;
-                mbar_wait(&bars[k % C::STAGES], (uint32_t)(k / C::STAGES) & 1u);
-            }
+            for (int u = k; u < npairs && u < k + C::STAGES; ++u)
+                mbar_wait(&bars[u % C::STAGES], (uint32_t)(u / C::STAGES) & 1u);
+        }
+        // undo the code offset and the code position factor of the value accumulators
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int f = (16 * mt / G) / GB;
+            o[mt][0] = (o[mt][0] + voff[f][0]) * kScaleEven;
+            o[mt][1] = (o[mt][1] + voff[f][1]) * kScaleEven;
+            o[mt][2] = (o[mt][2] + voff[f][2]) * kScaleOdd;
+            o[mt][3] = (o[mt][3] + voff[f][3]) * kScaleOdd;
         }
     } else {
         // ------------------------------ fp16 residual rows ------------------------------
@@ -467,8 +549,11 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                 af[3] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g + 8) * D + ch + 8) : 0u;
                 mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
             }
-            float pr[4];
-            softmax(okg ? c[0] + c[1] : -INFINITY, okg8 ? c[2] + c[3] : -INFINITY, pr);
+            const float sc[4] = {okg ? c[0] + c[1] : -INFINITY, okg8 ? c[2] + c[3] : -INFINITY, -INFINITY,
+                                 -INFINITY};
+            float p[4], pr[4];
+            softmax(sc, p);
+            gather(p[0], p[1], pr);
             uint32_t ph01, ph89, pl01, pl89;
             split_p(pr, ph01, ph89, pl01, pl89);
             const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
