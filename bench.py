@@ -89,6 +89,27 @@ def _kv_tokens_per_step(w):
     return w["layers"] * w["B"] * sum(Lq + r for Lq, r in _call_counts(w))
 
 
+# ---- N > 1: each rank runs its own replica of the workload (its own batch) ----
+def replica_seed(w, layer, rank):
+    """Seed of one rank's layer cache: replicas hold different synthetic batches."""
+    return w["seed"] + 7919 * layer + 104729 * rank
+
+
+def max_over_ranks(ms, device=None):
+    """Slowest rank's timed-region milliseconds (all ranks get the same value)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(w, world, steps, t_max_ms):
+    """KV tokens/s of all ranks together: every rank processes the same
+    per-rank workload (weak scaling), timed by the slowest rank."""
+    return world * _kv_tokens_per_step(w) * steps / (t_max_ms / 1e3)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -246,7 +267,7 @@ def run_ours(args, w):
     max_tokens = w["prompt"] + S
     caches, prompts, steps = [], [], []
     for li in range(NL):
-        syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=w["seed"] + 7919 * li + 104729 * rank,
+        syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=replica_seed(w, li, rank),
                       outliers=outl, sink=w["sink"], device=dev)
         prompts.append(syn.prompt(w["prompt"]))
         steps.append([syn.step(s) for s in range(S)])
@@ -308,13 +329,8 @@ def run_ours(args, w):
     launches_per_step = _launches_in(step, K, stream, torch)
     gpu_launches = launches_per_step * args.steps
     clocks = clk.summary()
-    t_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    tokens_step = _kv_tokens_per_step(w)
-    value = world * tokens_step * args.steps / (t_max / 1e3)
+    t_max = max_over_ranks(ms, dev) if world > 1 else ms
+    value = whole_job_value(w, world, args.steps, t_max)
 
     # ---- roofline: decode calls back to back (graph), rotated across layers ----
     reps = max(4, int(200 / max(NL * 8, 1)))
