@@ -36,6 +36,14 @@ constexpr int kPartialSlots = kMaxSplits + 1;  // + one split for the fp16 resid
 // status != 0 marks a split whose cache copy did not complete (its output is NaN).
 __host__ __device__ constexpr int partial_stride(int D) { return D + 4; }
 
+// Balanced partition of the quantized work of a decode call: P tile pairs in
+// slot-major order over n CTAs; CTA c takes pairs [part_begin(c), part_begin(c+1)).
+__host__ __device__ inline long long part_begin(long long c, long long P, long long n) { return c * P / n; }
+// The CTA whose range holds pair x (needs n <= P).
+__host__ __device__ inline long long part_owner(long long x, long long P, long long n) {
+    return ((x + 1) * n + P - 1) / P - 1;
+}
+
 // ---- launchers (defined in the .cu files; return the launch status) -------
 
 // Quantize nblk whole blocks per slot.  Block j of slot s is read from
@@ -51,9 +59,10 @@ cudaError_t launch_copy_rows(const Geometry& g, uint8_t* cache, const __half* sr
                              cudaStream_t st);
 
 struct DecodePlan {
-    int tiles_per_split;   // 16-token tiles of quantized cache per split
-    int n_qsplits;         // splits over the quantized tokens
-    int n_splits;          // n_qsplits + (residual split ? 1 : 0)
+    int tiles_per_split;   // CUDA-core kernel: 16-token tiles of quantized cache per split
+    int n_qsplits;         // CUDA-core kernel: splits over the quantized tokens
+    int n_splits;          // CUDA-core kernel: n_qsplits + (residual split ? 1 : 0)
+    int num_sms;           // tensor-core kernel: sizes its persistent grid
 };
 
 DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, int num_sms);

@@ -328,32 +328,49 @@ DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, 
     p.tiles_per_split = (int)tps;
     p.n_qsplits = n_qtiles ? (int)((n_qtiles + tps - 1) / tps) : 0;
     p.n_splits = p.n_qsplits + (n_resid > 0 ? 1 : 0);
+    p.num_sms = num_sms > 0 ? num_sms : 1;
     return p;
 }
 
-cudaError_t launch_decode_mma_d128(const mma_detail::Args& a, int bits, int nq, int G, dim3 grid,
-                                   cudaStream_t st);
-cudaError_t launch_decode_mma_d64(const mma_detail::Args& a, int bits, int nq, int G, dim3 grid,
-                                  cudaStream_t st);
+// Launch the tensor-core kernel on a persistent grid; fills a.n_ctas.
+cudaError_t launch_decode_mma_d128(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_mma_d64(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+
+namespace {
+cudaError_t launch_finish(const Geometry& g, const mma_detail::FinishArgs& f, cudaStream_t st) {
+    const int nq = g.Hq / g.Hkv;
+    const unsigned grid = (unsigned)((long long)g.B * g.Hq);
+#define KIVI_FIN(DD, NN) \
+    if (g.D == DD && nq == NN) { mma_detail::finish_kernel<DD, NN><<<grid, 128, 0, st>>>(f); return cudaGetLastError(); }
+    KIVI_FIN(128, 1) KIVI_FIN(128, 2) KIVI_FIN(128, 4) KIVI_FIN(64, 1) KIVI_FIN(64, 2) KIVI_FIN(64, 4)
+#undef KIVI_FIN
+    return cudaErrorInvalidValue;
+}
+}  // namespace
 
 cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_quant,
                           long long n_resid, const __half* q, __half* out, float scale_log2,
                           float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
                           int* launches) {
     if (variant == KIVI_DECODE_TENSOR_CORE) {
-        mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
-                           g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)(n_quant / 16),
-                           (int)n_resid, plan.tiles_per_split, plan.n_qsplits, scale_log2};
-        const dim3 grid(plan.n_splits, g.B * g.Hkv);
         const int nq = g.Hq / g.Hkv;
-        cudaError_t e = g.D == 128 ? launch_decode_mma_d128(m, g.bits, nq, g.G, grid, st)
-                                   : launch_decode_mma_d64(m, g.bits, nq, g.G, grid, st);
-        *launches = 1;
+        const long long slots = (long long)g.B * g.Hkv;
+        const long long pairs = n_quant / 32;
+        mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes, g.Hq, g.Hkv,
+                           pairs, slots * pairs, 0, scale_log2};
+        *launches = 0;
+        if (pairs > 0) {
+            cudaError_t e = g.D == 128 ? launch_decode_mma_d128(m, g.bits, nq, g.G, plan.num_sms, st)
+                                       : launch_decode_mma_d64(m, g.bits, nq, g.G, plan.num_sms, st);
+            if (e != cudaSuccess) return e;
+            *launches = 1;
+        }
+        mma_detail::FinishArgs f{cache, q, workspace, out, g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv,
+                                 (int)n_resid, pairs, m.total_pairs, m.n_ctas, scale_log2};
+        cudaError_t e = launch_finish(g, f, st);
         if (e != cudaSuccess) return e;
-        if (g.D == 128) combine_kernel<128><<<g.B * g.Hq, 128, 0, st>>>(workspace, out, plan.n_splits);
-        else combine_kernel<64><<<g.B * g.Hq, 64, 0, st>>>(workspace, out, plan.n_splits);
-        *launches = 2;
-        return cudaGetLastError();
+        *launches += 1;
+        return cudaSuccess;
     }
     DecodeArgs a{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                  g.k_resid_off, g.v_resid_off, g.R, g.G, g.Hq, g.Hkv,

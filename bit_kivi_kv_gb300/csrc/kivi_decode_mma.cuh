@@ -44,10 +44,22 @@ struct Args {
     const uint8_t* cache;
     const __half* q;
     float* ws;
-    long long NB, part_bytes, slot_bytes, tile_bytes, k_resid_off, v_resid_off;
-    int R, Hq, Hkv;
-    int n_qtiles, n_resid;
-    int tiles_per_split, n_qsplits;
+    long long NB, part_bytes, slot_bytes, tile_bytes;
+    int Hq, Hkv;
+    long long pairs_per_slot;   // quantized tile pairs (32 tokens) per slot
+    long long total_pairs;      // slots * pairs_per_slot
+    long long n_ctas;           // gridDim.x
+    float scale_log2;
+};
+
+struct FinishArgs {
+    const uint8_t* cache;
+    const __half* q;
+    const float* ws;
+    __half* out;
+    long long k_resid_off, v_resid_off;
+    int R, Hq, Hkv, n_resid;
+    long long pairs_per_slot, total_pairs, n_ctas;
     float scale_log2;
 };
 
@@ -296,19 +308,18 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     __shared__ __align__(8) uint64_t full_bar[kWarps][C::STAGES];
     __shared__ uint32_t red_status;
     extern __shared__ __align__(128) uint8_t dyn_smem[];
-    uint32_t status = 0;   // 1: a bulk copy did not complete in time
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, i = lane & 3;
-    const int slot = blockIdx.y, split = blockIdx.x;
-    const int b = slot / a.Hkv, hk = slot % a.Hkv;
     uint32_t* qfrag = qfrag_all[warp];
-
-    for (int idx = tid; idx < NQ * D; idx += kThreads) {
-        const int j = idx / D, c = idx % D;
-        qf[j][c] = __half2float(a.q[((long long)b * a.Hq + hk * NQ + j) * D + c]) * a.scale_log2;
-    }
+    uint8_t* ring = dyn_smem + warp * C::STAGES * C::STAGE_BYTES;
+    uint64_t* bars = full_bar[warp];
     for (int idx = lane; idx < 32 * C::QSTRIDE; idx += 32) qfrag[idx] = 0u;   // unused columns stay 0
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < C::STAGES; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+    }
     if (tid == 0) red_status = 0u;
     __syncthreads();
 
@@ -318,19 +329,20 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     const bool col_ok = hP < NQ;
     // this lane's output columns (2i, 2i+1): head hO, group slot jO
     const int hO = i / GB, jO = i % GB;
+    const uint32_t kNeg1024[4] = {0xE400E400u, 0xE400E400u, 0xE400E400u, 0xE400E400u};
+    constexpr float kScaleEven = 1.0f / (float)(1 << C::POS_EVEN);
+    constexpr float kScaleOdd = 1.0f / (float)(1 << C::POS_ODD);
+    const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
+    const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
 
-    float m = -INFINITY, l = 0.f;
+    float m, l;
     float o[KS][4];
     float voff[NBF][4];   // -1024 * sum_t Pt[t][n]: removes the code offset of the value MMAs
     float zeta[NBF];
-#pragma unroll
-    for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-#pragma unroll
-    for (int f = 0; f < NBF; ++f) zeta[f] = voff[f][0] = voff[f][1] = voff[f][2] = voff[f][3] = 0.f;
-    const uint32_t kNeg1024[4] = {0xE400E400u, 0xE400E400u, 0xE400E400u, 0xE400E400u};
-
     uint32_t qb[2 * KS];
     float beta = 0.f;
+    uint32_t status = 0;  // 1: a bulk copy did not complete in time (sticky)
+    uint32_t item = 0;    // ring stages this warp has consumed (stage index and phase)
 
     // Online softmax step over two tiles: sc = logits of tokens g, g+8 of tile
     // A and of tile B (head i); p receives their probabilities.
@@ -367,7 +379,6 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         pr[3] = __shfl_sync(kFull, p1, src + 4);    // token 2i+9
         if (!col_ok) pr[0] = pr[1] = pr[2] = pr[3] = 0.f;
     };
-
     // B fragment of P*step for one value fragment from the 4 tokens' (s, z) entries.
     auto p_frag = [&](const float (&pr)[4], uint32_t ph01, uint32_t ph89, uint32_t pl01, uint32_t pl89,
                       const uint32_t (&e)[4], uint32_t& b0, uint32_t& b1, float& z) {
@@ -381,7 +392,6 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         const float2 z89 = unpack_f16x2(__byte_perm(e[2], e[3], 0x7632));
         z = fmaf(pr[0], z01.x, fmaf(pr[1], z01.y, fmaf(pr[2], z89.x, fmaf(pr[3], z89.y, z))));
     };
-
     auto split_p = [&](const float (&pr)[4], uint32_t& ph01, uint32_t& ph89, uint32_t& pl01, uint32_t& pl89) {
         ph01 = pack_f16x2(pr[0], pr[1]);
         ph89 = pack_f16x2(pr[2], pr[3]);
@@ -389,36 +399,56 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         pl01 = pack_f16x2(pr[0] - f01.x, pr[1] - f01.y);
         pl89 = pack_f16x2(pr[2] - f89.x, pr[3] - f89.y);
     };
-
-    const uint8_t* slot_base = a.cache + (long long)slot * a.slot_bytes;
-    if (split < a.n_qsplits) {
-        // ------------------------------ quantized tiles ------------------------------
-        // Each warp streams its run of tiles, two per stage, through a STAGES-deep
-        // ring in shared memory; lane 0 issues the bulk copies, every lane waits on
-        // the stage's mbarrier, and a stage is refilled once the warp is done with it.
-        const int t0 = split * a.tiles_per_split;                  // even
-        const int t1 = min(t0 + a.tiles_per_split, a.n_qtiles);    // even
-        const int per_warp = (((t1 - t0 + kWarps - 1) / kWarps) + 1) & ~1;
-        const int tb = min(t0 + warp * per_warp, t1), te = min(tb + per_warp, t1);
-        const int npairs = (te - tb) / 2;
-        const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
-        const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
-        uint8_t* ring = dyn_smem + warp * C::STAGES * C::STAGE_BYTES;
-        uint64_t* bars = full_bar[warp];
-        if (lane == 0) {
+    auto lds_words = [&](const uint8_t* src, uint32_t (&w)[W]) {
+        if constexpr (W % 4 == 0) {
 #pragma unroll
-            for (int st = 0; st < C::STAGES; ++st) mbar_init(&bars[st], 1);
-            fence_mbar_init();
+            for (int v = 0; v < W / 4; ++v) {
+                const uint4 x = reinterpret_cast<const uint4*>(src + lane * W * 4)[v];
+                w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+            }
+        } else {
+            const uint2 x = *reinterpret_cast<const uint2*>(src + lane * W * 4);
+            w[0] = x.x; w[1] = x.y;
         }
-        __syncwarp();
-        auto need_ksz = [&](int T) { return T == tb || (T % C::TPB) == 0; };
-        auto issue = [&](int k, int st) {            // lane 0: stage st <- tiles tb+2k, tb+2k+1
-            const int T = tb + 2 * k;
+    };
+
+    // This CTA's share of the quantized work: tile pairs [x, xe) of the
+    // slot-major sequence; it emits one partial result per slot it touches.
+    const long long P = a.pairs_per_slot, Pt = a.total_pairs, Cn = a.n_ctas, cta = blockIdx.x;
+    long long x = part_begin(cta, Pt, Cn);
+    const long long xe = part_begin(cta + 1, Pt, Cn);
+    while (x < xe) {
+        const long long slot = x / P;
+        const long long seg_end = min(xe, (slot + 1) * P);
+        const int p0 = (int)(x - slot * P), p1 = (int)(seg_end - slot * P);
+        const int part = (int)(cta - part_owner(slot * P, Pt, Cn));
+        const int b = (int)(slot / a.Hkv), hk = (int)(slot % a.Hkv);
+        const uint8_t* slot_base = a.cache + slot * a.slot_bytes;
+        for (int idx = tid; idx < NQ * D; idx += kThreads) {
+            const int j = idx / D, c = idx % D;
+            qf[j][c] = __half2float(a.q[((long long)b * a.Hq + hk * NQ + j) * D + c]) * a.scale_log2;
+        }
+        __syncthreads();
+
+        m = -INFINITY; l = 0.f;
+#pragma unroll
+        for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+#pragma unroll
+        for (int f = 0; f < NBF; ++f) zeta[f] = voff[f][0] = voff[f][1] = voff[f][2] = voff[f][3] = 0.f;
+
+        // ---- this warp's contiguous run of pairs, two tiles per ring stage ----
+        const int pw = (p1 - p0 + kWarps - 1) / kWarps;
+        const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
+        const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
+        auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
+        auto issue = [&](int pr, uint32_t it) {      // lane 0: ring stage of item it <- pair pr
+            const int T = 2 * pr;
             const int blk = T / C::TPB, tin = T % C::TPB;
             const uint8_t* kpart = slot_base + (long long)blk * a.part_bytes;
             const uint8_t* vpart = kpart + a.NB * a.part_bytes;
+            const int st = (int)(it % C::STAGES);
             uint8_t* dst = ring + st * C::STAGE_BYTES;
-            const bool kz = need_ksz(T);
+            const bool kz = need_ksz(pr);
             mbar_expect_tx(&bars[st], 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
             tma_1d(dst, kpart + tin * C::TILE, 2 * C::TILE, &bars[st]);
             tma_1d(dst + 2 * C::TILE, vpart + tin * C::TILE, 2 * C::TILE, &bars[st]);
@@ -426,30 +456,17 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             if (kz) tma_1d(dst + 4 * C::TILE + 2 * C::ENT, kpart + tiles_bytes, C::KSZ, &bars[st]);
         };
         if (lane == 0) {
-            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue(k, k);
+            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue(wb + k, item + k);
         }
-        auto lds_words = [&](const uint8_t* src, uint32_t (&w)[W]) {
-            if constexpr (W % 4 == 0) {
-#pragma unroll
-                for (int v = 0; v < W / 4; ++v) {
-                    const uint4 x = reinterpret_cast<const uint4*>(src + lane * W * 4)[v];
-                    w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
-                }
-            } else {
-                const uint2 x = *reinterpret_cast<const uint2*>(src + lane * W * 4);
-                w[0] = x.x; w[1] = x.y;
-            }
-        };
-        constexpr float kScaleEven = 1.0f / (float)(1 << C::POS_EVEN);
-        constexpr float kScaleOdd = 1.0f / (float)(1 << C::POS_ODD);
         float cinit[4] = {0.f, 0.f, 0.f, 0.f};   // -1024 * sum_c Qt[c][n] of the current block
         int k = 0;
         for (; k < npairs; ++k) {
-            const int st = k % C::STAGES;
-            if (!__all_sync(kFull, mbar_wait(&bars[st], (uint32_t)(k / C::STAGES) & 1u))) break;
+            const uint32_t it = item + k;
+            const int st = (int)(it % C::STAGES);
+            if (!__all_sync(kFull, mbar_wait(&bars[st], (it / C::STAGES) & 1u))) break;
             const uint8_t* stage = ring + st * C::STAGE_BYTES;
-            const int T = tb + 2 * k;
-            if (need_ksz(T)) {
+            const int pr = wb + k;
+            if (need_ksz(pr)) {
                 build_q_frags<C, D, NQ>(reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + 2 * C::ENT), qf,
                                         qfrag, lane, qb, beta);
                 cinit[0] = cinit[1] = cinit[2] = cinit[3] = 0.f;
@@ -459,16 +476,16 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             // keys: logits of tokens g, g+8 of both tiles for head i
             float sc[4];
             {
-                uint32_t wa[W], wb[W];
+                uint32_t wa[W], wbw[W];
                 lds_words(stage, wa);
-                lds_words(stage + C::TILE, wb);
+                lds_words(stage + C::TILE, wbw);
                 float ca[4] = {cinit[0], cinit[1], cinit[2], cinit[3]};
                 float cb[4] = {cinit[0], cinit[1], cinit[2], cinit[3]};
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     uint32_t fa[4], fb[4];
                     a_frag_raw<BITS, W>(wa, kk, fa);
-                    a_frag_raw<BITS, W>(wb, kk, fb);
+                    a_frag_raw<BITS, W>(wbw, kk, fb);
                     mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
                     mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
                 }
@@ -482,10 +499,10 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             // values, tile by tile
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                float pr[4];
-                gather(p[2 * t], p[2 * t + 1], pr);
+                float prb[4];
+                gather(p[2 * t], p[2 * t + 1], prb);
                 uint32_t ph01, ph89, pl01, pl89;
-                split_p(pr, ph01, ph89, pl01, pl89);
+                split_p(prb, ph01, ph89, pl01, pl89);
                 const uint32_t* ve = reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + t * C::ENT);
                 uint32_t pb[NBF][2];
 #pragma unroll
@@ -493,7 +510,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                     const int gr = f * GB + jP;
                     const uint32_t e[4] = {ve[tokA * NGRP + gr], ve[(tokA + 1) * NGRP + gr], ve[tokB * NGRP + gr],
                                            ve[(tokB + 1) * NGRP + gr]};
-                    p_frag(pr, ph01, ph89, pl01, pl89, e, pb[f][0], pb[f][1], zeta[f]);
+                    p_frag(prb, ph01, ph89, pl01, pl89, e, pb[f][0], pb[f][1], zeta[f]);
                     mma16816(voff[f], kNeg1024, pb[f][0], pb[f][1]);
                 }
                 uint32_t wv[W];
@@ -509,15 +526,17 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             __syncwarp();                              // every lane is done with this stage
             if (lane == 0 && k + C::STAGES < npairs) {
                 fence_proxy_async();
-                issue(k + C::STAGES, st);
+                issue(wb + k + C::STAGES, it + C::STAGES);
             }
         }
         if (k < npairs) {
-            // a copy timed out: flag it, then wait (bounded) for this warp's copies in flight
+            // a copy timed out: flag it, wait (bounded) for this warp's copies in
+            // flight, and issue no more copies in this kernel
             status = 1;
             for (int u = k; u < npairs && u < k + C::STAGES; ++u)
-                mbar_wait(&bars[u % C::STAGES], (uint32_t)(u / C::STAGES) & 1u);
+                mbar_wait(&bars[(item + u) % C::STAGES], ((item + u) / C::STAGES) & 1u);
         }
+        item += (uint32_t)npairs;
         // undo the code offset and the code position factor of the value accumulators
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
@@ -527,96 +546,156 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             o[mt][2] = (o[mt][2] + voff[f][2]) * kScaleOdd;
             o[mt][3] = (o[mt][3] + voff[f][3]) * kScaleOdd;
         }
-    } else {
-        // ------------------------------ fp16 residual rows ------------------------------
-        const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + (long long)slot * a.R * D;
-        const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + (long long)slot * a.R * D;
-        const int n = a.n_resid, ntiles = (n + 15) / 16;
-        const int per_warp = (ntiles + kWarps - 1) / kWarps;
-        const int tb = warp * per_warp, te = min(tb + per_warp, ntiles);
-        if (tb < te) build_q_frags<C, D, NQ>(nullptr, qf, qfrag, lane, qb, beta);
-        for (int T = tb; T < te; ++T) {
-            const int r0 = T * 16;
-            const bool okg = r0 + g < n, okg8 = r0 + g + 8 < n;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
+
+        // ---- merge the warps, write the slot's partial (m, l, status, o) ----
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                const int ch = 16 * kk + 2 * i;
-                uint32_t af[4];
-                af[0] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g) * D + ch) : 0u;
-                af[1] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g + 8) * D + ch) : 0u;
-                af[2] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g) * D + ch + 8) : 0u;
-                af[3] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0 + g + 8) * D + ch + 8) : 0u;
-                mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
-            }
-            const float sc[4] = {okg ? c[0] + c[1] : -INFINITY, okg8 ? c[2] + c[3] : -INFINITY, -INFINITY,
-                                 -INFINITY};
-            float p[4], pr[4];
-            softmax(sc, p);
-            gather(p[0], p[1], pr);
-            uint32_t ph01, ph89, pl01, pl89;
-            split_p(pr, ph01, ph89, pl01, pl89);
-            const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
-            const int tA = r0 + 2 * i, tB = r0 + 2 * i + 8;
+        for (int f = 0; f < NBF; ++f) {
+            zeta[f] += __shfl_xor_sync(kFull, zeta[f], 1);
+            zeta[f] += __shfl_xor_sync(kFull, zeta[f], 2);
+        }
+        float lt = l;
+        lt += __shfl_xor_sync(kFull, lt, 4);
+        lt += __shfl_xor_sync(kFull, lt, 8);
+        lt += __shfl_xor_sync(kFull, lt, 16);
+        if (g == 0 && i < NQ) { red_m[warp][i] = m; red_l[warp][i] = lt; }
+        if (status && lane == 0) atomicOr(&red_status, status);
+        if (i == 0 && !lo_col && col_ok) {
+#pragma unroll
+            for (int f = 0; f < NBF; ++f) red_z[warp][hP][f * GB + jP] = zeta[f];
+        }
+        if (hO < NQ) {
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                const int c0 = 16 * mt + g;
-                auto ld = [&](int t, int ch) -> uint32_t {
-                    return t < n ? (uint32_t)__half_as_ushort(vr[(long long)t * D + ch]) : 0u;
-                };
-                uint32_t af[4];
-                af[0] = ld(tA, c0) | (ld(tA + 1, c0) << 16);
-                af[1] = ld(tA, c0 + 8) | (ld(tA + 1, c0 + 8) << 16);
-                af[2] = ld(tB, c0) | (ld(tB + 1, c0) << 16);
-                af[3] = ld(tB, c0 + 8) | (ld(tB + 1, c0 + 8) << 16);
-                mma16816(o[mt], af, pb0, pb1);
+                const int gr = 16 * mt / G;
+                if (gr % GB == jO) {
+                    red_o[warp][hO][16 * mt + g] = o[mt][0] + o[mt][1];
+                    red_o[warp][hO][16 * mt + g + 8] = o[mt][2] + o[mt][3];
+                }
             }
         }
+        __syncthreads();
+        for (int idx = tid; idx < NQ * D; idx += kThreads) {
+            const int j = idx / D, c = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][j]);
+            float acc = 0.f, lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                if (red_m[w][j] == -INFINITY) continue;
+                const float e = exp2f(red_m[w][j] - M);
+                acc = fmaf(red_o[w][j][c] + red_z[w][j][c / G], e, acc);
+                lsum = fmaf(red_l[w][j], e, lsum);
+            }
+            float* pw = a.ws + ((long long)(b * a.Hq + hk * NQ + j) * kPartialSlots + part) * partial_stride(D);
+            if (c == 0) { pw[0] = M; pw[1] = lsum; }
+            if (c == 1) pw[2] = (float)red_status;
+            pw[4 + c] = acc;
+        }
+        __syncthreads();                               // qf and red_* are reused by the next segment
+        x = seg_end;
+    }
+}
+
+// ---- block-wide reductions for the finish kernel (128 threads) ----
+__device__ __forceinline__ float block_max128(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+}
+__device__ __forceinline__ float block_sum128(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+// One CTA (128 threads) per (batch, query head): attention over the fp16
+// residual rows (online softmax in chunks of 128 rows), then log-sum-exp merge
+// with the quantized partials of the head's kv slot -> fp16 output.  A partial
+// whose status is set makes the output NaN.
+template <int D, int NQ>
+__global__ void __launch_bounds__(128) finish_kernel(FinishArgs a) {
+    __shared__ float qs[D];
+    __shared__ float pbuf[128];
+    __shared__ float red[4];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long bh = blockIdx.x;
+    const int b = (int)(bh / a.Hq), h = (int)(bh % a.Hq), hk = h / NQ;
+    const long long slot = (long long)b * a.Hkv + hk;
+    for (int c = tid; c < D; c += 128) qs[c] = __half2float(a.q[bh * D + c]) * a.scale_log2;
+    __syncthreads();
+
+    // residual rows
+    float m = -INFINITY, l = 0.f, o = 0.f;      // thread c < D owns output channel c
+    const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + slot * a.R * D;
+    const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + slot * a.R * D;
+    constexpr int CPL = D / 32;                  // channels per lane in the row dot products
+    for (int t0 = 0; t0 < a.n_resid; t0 += 128) {
+        const int nrows = min(128, a.n_resid - t0);
+        for (int t = warp; t < nrows; t += 4) {
+            const __half* row = kr + (long long)(t0 + t) * D + lane * CPL;
+            float s = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; c += 2) {
+                const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(row + c));
+                s = fmaf(qs[lane * CPL + c], kv.x, fmaf(qs[lane * CPL + c + 1], kv.y, s));
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) s += __shfl_xor_sync(kFull, s, o2);
+            if (lane == 0) pbuf[t] = s;
+        }
+        __syncthreads();
+        const float sv = tid < nrows ? pbuf[tid] : -INFINITY;
+        const float mn = fmaxf(m, block_max128(sv, red));
+        const float pv = tid < nrows ? fast_exp2(sv - mn) : 0.f;
+        const float alpha = fast_exp2(m - mn);
+        const float ps = block_sum128(pv, red);
+        if (tid < nrows) pbuf[tid] = pv;
+        __syncthreads();
+        l = l * alpha + ps;
+        o *= alpha;
+        m = mn;
+        if (tid < D) {
+            for (int t = 0; t < nrows; ++t) o = fmaf(pbuf[t], __half2float(vr[(long long)(t0 + t) * D + tid]), o);
+        }
+        __syncthreads();
     }
 
-    // ------------------------------ merge the warps ------------------------------
-#pragma unroll
-    for (int f = 0; f < NBF; ++f) {
-        zeta[f] += __shfl_xor_sync(kFull, zeta[f], 1);
-        zeta[f] += __shfl_xor_sync(kFull, zeta[f], 2);
+    // merge with the quantized partials of this head
+    int nparts = 0;
+    long long first = 0;
+    if (a.pairs_per_slot > 0) {
+        first = part_owner(slot * a.pairs_per_slot, a.total_pairs, a.n_ctas);
+        nparts = (int)(part_owner(slot * a.pairs_per_slot + a.pairs_per_slot - 1, a.total_pairs, a.n_ctas) - first + 1);
     }
-    l += __shfl_xor_sync(kFull, l, 4);
-    l += __shfl_xor_sync(kFull, l, 8);
-    l += __shfl_xor_sync(kFull, l, 16);
-    if (g == 0 && i < NQ) { red_m[warp][i] = m; red_l[warp][i] = l; }
-    if (status && lane == 0) atomicOr(&red_status, status);
-    if (i == 0 && !lo_col && col_ok) {
-#pragma unroll
-        for (int f = 0; f < NBF; ++f) red_z[warp][hP][f * GB + jP] = zeta[f];
+    const float* base = a.ws + bh * kPartialSlots * partial_stride(D);
+    float M = m;
+    bool failed = false;
+    for (int j = 0; j < nparts; ++j) {
+        M = fmaxf(M, base[j * partial_stride(D)]);
+        failed |= base[j * partial_stride(D) + 2] != 0.f;
     }
-    if (hO < NQ) {
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int gr = 16 * mt / G;
-            if (gr % GB == jO) {
-                red_o[warp][hO][16 * mt + g] = o[mt][0] + o[mt][1];
-                red_o[warp][hO][16 * mt + g + 8] = o[mt][2] + o[mt][3];
-            }
-        }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < NQ * D; idx += kThreads) {
-        const int j = idx / D, c = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][j]);
+    if (tid < D) {
         float acc = 0.f, lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            if (red_m[w][j] == -INFINITY) continue;
-            const float e = exp2f(red_m[w][j] - M);
-            acc = fmaf(red_o[w][j][c] + red_z[w][j][c / G], e, acc);
-            lsum = fmaf(red_l[w][j], e, lsum);
+        if (m != -INFINITY) {
+            const float e = fast_exp2(m - M);
+            acc = o * e;
+            lsum = l * e;
         }
-        float* pw = a.ws + ((long long)(b * a.Hq + hk * NQ + j) * kPartialSlots + split) * partial_stride(D);
-        if (c == 0) { pw[0] = M; pw[1] = lsum; }
-        if (c == 1) pw[2] = (float)red_status;
-        pw[4 + c] = acc;
+        for (int j = 0; j < nparts; ++j) {
+            const float* ps = base + j * partial_stride(D);
+            if (ps[0] == -INFINITY) continue;
+            const float e = fast_exp2(ps[0] - M);
+            lsum = fmaf(ps[1], e, lsum);
+            acc = fmaf(ps[4 + tid], e, acc);
+        }
+        a.out[bh * D + tid] = failed ? __float2half_rn(NAN) : __float2half_rn(acc / lsum);
     }
 }
 

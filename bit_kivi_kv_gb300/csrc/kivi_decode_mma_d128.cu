@@ -5,22 +5,35 @@ namespace kivi {
 
 namespace {
 template <int BB, int NN, int GG>
-cudaError_t launch_one(const mma_detail::Args& a, dim3 grid, cudaStream_t st) {
+cudaError_t launch_one(mma_detail::Args& a, int num_sms, cudaStream_t st) {
     using namespace mma_detail;
     using C = Cfg<128, BB, NN, GG>;
-    // opt in to the dynamic shared memory of the copy ring once per instance
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        decode_mma_kernel<128, BB, NN, GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
-    if (attr != cudaSuccess) return attr;
-    decode_mma_kernel<128, BB, NN, GG><<<grid, kThreads, C::DYN_SMEM, st>>>(a);
+    // opt in to the dynamic shared memory of the copy ring and size the
+    // persistent grid from the occupancy, once per instance
+    static int per_sm = -1;
+    static cudaError_t init = [] {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<128, BB, NN, GG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<128, BB, NN, GG>,
+                                                              kThreads, C::DYN_SMEM);
+        return e;
+    }();
+    if (init != cudaSuccess) return init;
+    const long long slots = a.pairs_per_slot > 0 ? a.total_pairs / a.pairs_per_slot : 1;
+    long long n = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
+    if (n > a.total_pairs) n = a.total_pairs;
+    if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot
+    if (n < 1) n = 1;
+    a.n_ctas = n;
+    decode_mma_kernel<128, BB, NN, GG><<<(unsigned)n, kThreads, C::DYN_SMEM, st>>>(a);
     return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_decode_mma_d128(const mma_detail::Args& a, int bits, int nq, int G, dim3 grid,
-                                  cudaStream_t st) {
+cudaError_t launch_decode_mma_d128(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st) {
 #define KIVI_MMA(BB, NN, GG) \
-    if (bits == BB && nq == NN && G == GG) return launch_one<BB, NN, GG>(a, grid, st);
+    if (bits == BB && nq == NN && G == GG) return launch_one<BB, NN, GG>(a, num_sms, st);
 #define KIVI_MMA_G(BB, NN) KIVI_MMA(BB, NN, 32) KIVI_MMA(BB, NN, 64) KIVI_MMA(BB, NN, 128)
     KIVI_MMA_G(2, 1) KIVI_MMA_G(2, 2) KIVI_MMA_G(2, 4)
     KIVI_MMA_G(4, 1) KIVI_MMA_G(4, 2) KIVI_MMA_G(4, 4)
