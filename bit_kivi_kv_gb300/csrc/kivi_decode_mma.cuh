@@ -238,7 +238,7 @@ struct Cfg {
     static constexpr int TILE = 2 * D * BITS;         // bytes of one code tile
     static constexpr int ENT = 16 * NGRP * 4;         // value (step, zero) entries of one tile
     static constexpr int KSZ = 4 * D;                 // key (step, zero) entries of one block
-    static constexpr int STAGES = BITS == 2 ? 3 : 2;   // ring depth per warp (stages of 2 tiles)
+    static constexpr int STAGES = 2;                  // ring depth per warp (stages of 2 tiles)
     // a stage: key words of 2 tiles, value words of 2 tiles, their value
     // entries, and the block's key entries
     static constexpr int STAGE_BYTES = 4 * TILE + 2 * ENT + KSZ;
@@ -621,34 +621,48 @@ __device__ __forceinline__ float block_sum128(float v, float* red) {
 // whose status is set makes the output NaN.
 template <int D, int NQ>
 __global__ void __launch_bounds__(128) finish_kernel(FinishArgs a) {
+    constexpr int CH = D / 8;            // key channels per thread: 8 threads per row
+    constexpr int NCP = D / 2;           // value channel pairs
+    constexpr int NRP = 128 / NCP;       // row phases of the value sum (2 at D128, 4 at D64)
     __shared__ float qs[D];
     __shared__ float pbuf[128];
     __shared__ float red[4];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float2 osum[NRP][NCP];
+    const int tid = threadIdx.x;
     const long long bh = blockIdx.x;
     const int b = (int)(bh / a.Hq), h = (int)(bh % a.Hq), hk = h / NQ;
     const long long slot = (long long)b * a.Hkv + hk;
     for (int c = tid; c < D; c += 128) qs[c] = __half2float(a.q[bh * D + c]) * a.scale_log2;
     __syncthreads();
 
-    // residual rows
-    float m = -INFINITY, l = 0.f, o = 0.f;      // thread c < D owns output channel c
     const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + slot * a.R * D;
     const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + slot * a.R * D;
-    constexpr int CPL = D / 32;                  // channels per lane in the row dot products
+    const int rs = tid >> 3, ck = tid & 7;        // score layout: row slot, channel chunk
+    float qreg[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) qreg[c] = qs[ck * CH + c];
+    const int cp = tid % NCP, rp = tid / NCP;     // value layout: channel pair, row phase
+    float m = -INFINITY, l = 0.f;
+    float2 o = make_float2(0.f, 0.f);
     for (int t0 = 0; t0 < a.n_resid; t0 += 128) {
         const int nrows = min(128, a.n_resid - t0);
-        for (int t = warp; t < nrows; t += 4) {
-            const __half* row = kr + (long long)(t0 + t) * D + lane * CPL;
+        for (int rr = rs; rr < nrows; rr += 16) {
+            const uint4* src = reinterpret_cast<const uint4*>(kr + (long long)(t0 + rr) * D + ck * CH);
             float s = 0.f;
 #pragma unroll
-            for (int c = 0; c < CPL; c += 2) {
-                const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(row + c));
-                s = fmaf(qs[lane * CPL + c], kv.x, fmaf(qs[lane * CPL + c + 1], kv.y, s));
-            }
+            for (int v = 0; v < CH / 8; ++v) {
+                const uint4 x = src[v];
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) s += __shfl_xor_sync(kFull, s, o2);
-            if (lane == 0) pbuf[t] = s;
+                for (int e = 0; e < 4; ++e) {
+                    const float2 kv = unpack_f16x2(w[e]);
+                    s = fmaf(qreg[8 * v + 2 * e], kv.x, fmaf(qreg[8 * v + 2 * e + 1], kv.y, s));
+                }
+            }
+            s += __shfl_xor_sync(kFull, s, 1);
+            s += __shfl_xor_sync(kFull, s, 2);
+            s += __shfl_xor_sync(kFull, s, 4);
+            if (ck == 0) pbuf[rr] = s;
         }
         __syncthreads();
         const float sv = tid < nrows ? pbuf[tid] : -INFINITY;
@@ -659,19 +673,37 @@ __global__ void __launch_bounds__(128) finish_kernel(FinishArgs a) {
         if (tid < nrows) pbuf[tid] = pv;
         __syncthreads();
         l = l * alpha + ps;
-        o *= alpha;
+        o.x *= alpha;
+        o.y *= alpha;
         m = mn;
-        if (tid < D) {
-            for (int t = 0; t < nrows; ++t) o = fmaf(pbuf[t], __half2float(vr[(long long)(t0 + t) * D + tid]), o);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const uint32_t* vcol = reinterpret_cast<const uint32_t*>(vr + (long long)t0 * D) + cp;
+        int t = rp;
+        for (; t + 3 * NRP < nrows; t += 4 * NRP) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 v2 = unpack_f16x2(vcol[(long long)(t + u * NRP) * NCP]);
+                const float pt = pbuf[t + u * NRP];
+                acc[u].x = fmaf(pt, v2.x, acc[u].x);
+                acc[u].y = fmaf(pt, v2.y, acc[u].y);
+            }
         }
+        for (; t < nrows; t += NRP) {
+            const float2 v2 = unpack_f16x2(vcol[(long long)t * NCP]);
+            acc[0].x = fmaf(pbuf[t], v2.x, acc[0].x);
+            acc[0].y = fmaf(pbuf[t], v2.y, acc[0].y);
+        }
+        o.x += (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
+        o.y += (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
         __syncthreads();
     }
+    osum[rp][cp] = o;
+    __syncthreads();
 
     // merge with the quantized partials of this head
     int nparts = 0;
-    long long first = 0;
     if (a.pairs_per_slot > 0) {
-        first = part_owner(slot * a.pairs_per_slot, a.total_pairs, a.n_ctas);
+        const long long first = part_owner(slot * a.pairs_per_slot, a.total_pairs, a.n_ctas);
         nparts = (int)(part_owner(slot * a.pairs_per_slot + a.pairs_per_slot - 1, a.total_pairs, a.n_ctas) - first + 1);
     }
     const float* base = a.ws + bh * kPartialSlots * partial_stride(D);
@@ -684,8 +716,11 @@ __global__ void __launch_bounds__(128) finish_kernel(FinishArgs a) {
     if (tid < D) {
         float acc = 0.f, lsum = 0.f;
         if (m != -INFINITY) {
+            float r = 0.f;
+#pragma unroll
+            for (int q = 0; q < NRP; ++q) r += (tid & 1) ? osum[q][tid >> 1].y : osum[q][tid >> 1].x;
             const float e = fast_exp2(m - M);
-            acc = o * e;
+            acc = r * e;
             lsum = l * e;
         }
         for (int j = 0; j < nparts; ++j) {
