@@ -646,12 +646,15 @@ __global__ void __launch_bounds__(128) finish_kernel(FinishArgs a) {
     float2 o = make_float2(0.f, 0.f);
     for (int t0 = 0; t0 < a.n_resid; t0 += 128) {
         const int nrows = min(128, a.n_resid - t0);
-        for (int rr = rs; rr < nrows; rr += 16) {
-            const uint4* src = reinterpret_cast<const uint4*>(kr + (long long)(t0 + rr) * D + ck * CH);
+        // every lane runs the same trip count (the shuffles below need the whole warp)
+        for (int r16 = 0; r16 < nrows; r16 += 16) {
+            const int rr = r16 + rs;
+            const bool valid = rr < nrows;
+            const uint4* src = reinterpret_cast<const uint4*>(kr + (long long)(t0 + (valid ? rr : 0)) * D + ck * CH);
             float s = 0.f;
 #pragma unroll
             for (int v = 0; v < CH / 8; ++v) {
-                const uint4 x = src[v];
+                const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
                 const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -662,7 +665,7 @@ __global__ void __launch_bounds__(128) finish_kernel(FinishArgs a) {
             s += __shfl_xor_sync(kFull, s, 1);
             s += __shfl_xor_sync(kFull, s, 2);
             s += __shfl_xor_sync(kFull, s, 4);
-            if (ck == 0) pbuf[rr] = s;
+            if (ck == 0 && valid) pbuf[rr] = s;
         }
         __syncthreads();
         const float sv = tid < nrows ? pbuf[tid] : -INFINITY;
