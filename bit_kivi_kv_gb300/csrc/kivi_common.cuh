@@ -36,12 +36,34 @@ constexpr int kPartialSlots = kMaxSplits + 1;  // + one split for the fp16 resid
 // status != 0 marks a split whose cache copy did not complete (its output is NaN).
 __host__ __device__ constexpr int partial_stride(int D) { return D + 4; }
 
-// Balanced partition of the quantized work of a decode call: P tile pairs in
-// slot-major order over n CTAs; CTA c takes pairs [part_begin(c), part_begin(c+1)).
-__host__ __device__ inline long long part_begin(long long c, long long P, long long n) { return c * P / n; }
-// The CTA whose range holds pair x (needs n <= P).
-__host__ __device__ inline long long part_owner(long long x, long long P, long long n) {
-    return ((x + 1) * n + P - 1) / P - 1;
+// Balanced partition of a decode call's work over the CTAs of the tensor-core
+// kernel.  Per (batch, kv-head) slot the work is a row of units: P quantized
+// tile pairs (32 tokens) of weight wq, then PR fp16 residual pairs (32 rows) of
+// weight wr (weights proportional to the bytes each reads).  Slots follow each
+// other; CTA c covers weight positions [c*Wt/n, (c+1)*Wt/n) and owns the units
+// that start there.  n <= Wt / max(wq, wr) guarantees every CTA owns a unit.
+struct WorkMap {
+    long long P, PR, wq, wr, Ws, Wt, n;
+};
+__host__ __device__ inline long long unit_start(const WorkMap& m, long long u) {
+    return u < m.P ? u * m.wq : m.P * m.wq + (u - m.P) * m.wr;
+}
+// first unit of a slot starting at or after weight offset y (0 <= y <= Ws); P + PR if none
+__host__ __device__ inline long long first_unit_at(const WorkMap& m, long long y) {
+    if (y <= 0) return 0;
+    if (y <= m.P * m.wq) return (y + m.wq - 1) / m.wq;
+    return m.P + (y - m.P * m.wq + m.wr - 1) / m.wr;
+}
+__host__ __device__ inline long long map_begin(const WorkMap& m, long long c) { return c * m.Wt / m.n; }
+// the CTA whose range holds weight position x
+__host__ __device__ inline long long map_owner(const WorkMap& m, long long x) {
+    return ((x + 1) * m.n + m.Wt - 1) / m.Wt - 1;
+}
+// partials of slot s: CTAs [map_owner(s*Ws), map_owner(s*Ws + start of its last unit)]
+__host__ __device__ inline long long slot_first_cta(const WorkMap& m, long long s) { return map_owner(m, s * m.Ws); }
+__host__ __device__ inline int slot_parts(const WorkMap& m, long long s) {
+    if (m.P + m.PR == 0) return 0;
+    return (int)(map_owner(m, s * m.Ws + unit_start(m, m.P + m.PR - 1)) - slot_first_cta(m, s) + 1);
 }
 
 // ---- launchers (defined in the .cu files; return the launch status) -------

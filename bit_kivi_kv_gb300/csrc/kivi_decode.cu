@@ -332,21 +332,11 @@ DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, 
     return p;
 }
 
-// Launch the tensor-core kernel on a persistent grid; fills a.n_ctas.
+// Launch the tensor-core kernel on a persistent grid; fills a.wm.n.
 cudaError_t launch_decode_mma_d128(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_mma_d64(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 
-namespace {
-cudaError_t launch_finish(const Geometry& g, const mma_detail::FinishArgs& f, cudaStream_t st) {
-    const int nq = g.Hq / g.Hkv;
-    const unsigned grid = (unsigned)((long long)g.B * g.Hq);
-#define KIVI_FIN(DD, NN) \
-    if (g.D == DD && nq == NN) { mma_detail::finish_kernel<DD, NN><<<grid, 128, 0, st>>>(f); return cudaGetLastError(); }
-    KIVI_FIN(128, 1) KIVI_FIN(128, 2) KIVI_FIN(128, 4) KIVI_FIN(64, 1) KIVI_FIN(64, 2) KIVI_FIN(64, 4)
-#undef KIVI_FIN
-    return cudaErrorInvalidValue;
-}
-}  // namespace
+
 
 cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_quant,
                           long long n_resid, const __half* q, __half* out, float scale_log2,
@@ -355,22 +345,24 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
     if (variant == KIVI_DECODE_TENSOR_CORE) {
         const int nq = g.Hq / g.Hkv;
         const long long slots = (long long)g.B * g.Hkv;
-        const long long pairs = n_quant / 32;
-        mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes, g.Hq, g.Hkv,
-                           pairs, slots * pairs, 0, scale_log2};
-        *launches = 0;
-        if (pairs > 0) {
-            cudaError_t e = g.D == 128 ? launch_decode_mma_d128(m, g.bits, nq, g.G, plan.num_sms, st)
-                                       : launch_decode_mma_d64(m, g.bits, nq, g.G, plan.num_sms, st);
-            if (e != cudaSuccess) return e;
-            *launches = 1;
-        }
-        mma_detail::FinishArgs f{cache, q, workspace, out, g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv,
-                                 (int)n_resid, pairs, m.total_pairs, m.n_ctas, scale_log2};
-        cudaError_t e = launch_finish(g, f, st);
+        WorkMap wm{};
+        wm.P = n_quant / 32;
+        wm.PR = (n_resid + 31) / 32;
+        wm.wq = (long long)g.D * g.bits / 4 + 8LL * g.D / g.G;   // bytes of a quantized pair / 32
+        wm.wr = 4LL * g.D;                                        // bytes of a residual pair / 32
+        wm.Ws = wm.P * wm.wq + wm.PR * wm.wr;
+        wm.Wt = slots * wm.Ws;
+        mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
+                           g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2};
+        cudaError_t e = g.D == 128 ? launch_decode_mma_d128(m, g.bits, nq, g.G, plan.num_sms, st)
+                                   : launch_decode_mma_d64(m, g.bits, nq, g.G, plan.num_sms, st);
         if (e != cudaSuccess) return e;
-        *launches += 1;
-        return cudaSuccess;
+        mma_detail::FinishArgs f{workspace, out, g.Hq, g.Hkv, nq, m.wm};
+        const unsigned grid = (unsigned)((long long)g.B * g.Hq);
+        if (g.D == 128) mma_detail::finish_kernel<128><<<grid, 128, 0, st>>>(f);
+        else mma_detail::finish_kernel<64><<<grid, 64, 0, st>>>(f);
+        *launches = 2;
+        return cudaGetLastError();
     }
     DecodeArgs a{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                  g.k_resid_off, g.v_resid_off, g.R, g.G, g.Hq, g.Hkv,

@@ -44,23 +44,17 @@ struct Args {
     const uint8_t* cache;
     const __half* q;
     float* ws;
-    long long NB, part_bytes, slot_bytes, tile_bytes;
-    int Hq, Hkv;
-    long long pairs_per_slot;   // quantized tile pairs (32 tokens) per slot
-    long long total_pairs;      // slots * pairs_per_slot
-    long long n_ctas;           // gridDim.x
+    long long NB, part_bytes, slot_bytes, tile_bytes, k_resid_off, v_resid_off;
+    int R, Hq, Hkv, n_resid;
+    WorkMap wm;
     float scale_log2;
 };
 
 struct FinishArgs {
-    const uint8_t* cache;
-    const __half* q;
     const float* ws;
     __half* out;
-    long long k_resid_off, v_resid_off;
-    int R, Hq, Hkv, n_resid;
-    long long pairs_per_slot, total_pairs, n_ctas;
-    float scale_log2;
+    int Hq, Hkv, nq;
+    WorkMap wm;
 };
 
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
@@ -412,16 +406,21 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         }
     };
 
-    // This CTA's share of the quantized work: tile pairs [x, xe) of the
-    // slot-major sequence; it emits one partial result per slot it touches.
-    const long long P = a.pairs_per_slot, Pt = a.total_pairs, Cn = a.n_ctas, cta = blockIdx.x;
-    long long x = part_begin(cta, Pt, Cn);
-    const long long xe = part_begin(cta + 1, Pt, Cn);
-    while (x < xe) {
-        const long long slot = x / P;
-        const long long seg_end = min(xe, (slot + 1) * P);
-        const int p0 = (int)(x - slot * P), p1 = (int)(seg_end - slot * P);
-        const int part = (int)(cta - part_owner(slot * P, Pt, Cn));
+    // This CTA's share of the call's work: the units starting in its weight range
+    // [pos, pe); one partial result per slot it touches.
+    const WorkMap& wm = a.wm;
+    const long long cta = blockIdx.x, NU = wm.P + wm.PR;
+    long long pos = map_begin(wm, cta);
+    const long long pe = map_begin(wm, cta + 1);
+    while (pos < pe) {
+        const long long slot = pos / wm.Ws;
+        const long long u0 = first_unit_at(wm, pos - slot * wm.Ws);
+        if (u0 >= NU) { pos = (slot + 1) * wm.Ws; continue; }
+        if (slot * wm.Ws + unit_start(wm, u0) >= pe) break;
+        const long long u1 = first_unit_at(wm, min(pe - slot * wm.Ws, wm.Ws));
+        const int p0 = (int)min(u0, wm.P), p1 = (int)min(u1, wm.P);              // quantized pairs
+        const int r0 = (int)(max(u0, wm.P) - wm.P), r1 = (int)(max(u1, wm.P) - wm.P);  // residual pairs
+        const int part = (int)(cta - slot_first_cta(wm, slot));
         const int b = (int)(slot / a.Hkv), hk = (int)(slot % a.Hkv);
         const uint8_t* slot_base = a.cache + slot * a.slot_bytes;
         for (int idx = tid; idx < NQ * D; idx += kThreads) {
@@ -546,6 +545,63 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             o[mt][2] = (o[mt][2] + voff[f][2]) * kScaleOdd;
             o[mt][3] = (o[mt][3] + voff[f][3]) * kScaleOdd;
         }
+#pragma unroll
+        for (int f = 0; f < NBF; ++f) voff[f][0] = voff[f][1] = voff[f][2] = voff[f][3] = 0.f;
+
+        // ---- this warp's residual pairs: 32 fp16 rows each, A operands straight from memory ----
+        const int rw = (r1 - r0 + kWarps - 1) / kWarps;
+        const int rb = min(r0 + warp * rw, r1), re = min(rb + rw, r1);
+        if (rb < re) {
+            const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + slot * a.R * D;
+            const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + slot * a.R * D;
+            const int n = a.n_resid;
+            build_q_frags<C, D, NQ>(nullptr, qf, qfrag, lane, qb, beta);   // step 1, zero 0
+            for (int rp = rb; rp < re; ++rp) {
+                float sc[4];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int r0w = 32 * rp + 16 * t;
+                    const bool okg = r0w + g < n, okg8 = r0w + g + 8 < n;
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const int ch = 16 * kk + 2 * i;
+                        uint32_t af[4];
+                        af[0] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g) * D + ch) : 0u;
+                        af[1] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g + 8) * D + ch) : 0u;
+                        af[2] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g) * D + ch + 8) : 0u;
+                        af[3] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g + 8) * D + ch + 8) : 0u;
+                        mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
+                    }
+                    sc[2 * t] = okg ? c[0] + c[1] : -INFINITY;
+                    sc[2 * t + 1] = okg8 ? c[2] + c[3] : -INFINITY;
+                }
+                float p[4];
+                softmax(sc, p);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    float prb[4];
+                    gather(p[2 * t], p[2 * t + 1], prb);
+                    uint32_t ph01, ph89, pl01, pl89;
+                    split_p(prb, ph01, ph89, pl01, pl89);
+                    const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
+                    const int tA = 32 * rp + 16 * t + 2 * i, tB = tA + 8;
+                    auto ld = [&](int tt, int ch) -> uint32_t {
+                        return tt < n ? (uint32_t)__half_as_ushort(vr[(long long)tt * D + ch]) : 0u;
+                    };
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        const int c0 = 16 * mt + g;
+                        uint32_t af[4];
+                        af[0] = ld(tA, c0) | (ld(tA + 1, c0) << 16);
+                        af[1] = ld(tA, c0 + 8) | (ld(tA + 1, c0 + 8) << 16);
+                        af[2] = ld(tB, c0) | (ld(tB + 1, c0) << 16);
+                        af[3] = ld(tB, c0 + 8) | (ld(tB + 1, c0 + 8) << 16);
+                        mma16816(o[mt], af, pb0, pb1);
+                    }
+                }
+            }
+        }
 
         // ---- merge the warps, write the slot's partial (m, l, status, o) ----
 #pragma unroll
@@ -593,148 +649,35 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             pw[4 + c] = acc;
         }
         __syncthreads();                               // qf and red_* are reused by the next segment
-        x = seg_end;
+        pos = u1 >= NU ? (slot + 1) * wm.Ws : slot * wm.Ws + unit_start(wm, u1);
     }
 }
 
-// ---- block-wide reductions for the finish kernel (128 threads) ----
-__device__ __forceinline__ float block_max128(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-}
-__device__ __forceinline__ float block_sum128(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    return (red[0] + red[1]) + (red[2] + red[3]);
-}
-
-// One CTA (128 threads) per (batch, query head): attention over the fp16
-// residual rows (online softmax in chunks of 128 rows), then log-sum-exp merge
-// with the quantized partials of the head's kv slot -> fp16 output.  A partial
-// whose status is set makes the output NaN.
-template <int D, int NQ>
-__global__ void __launch_bounds__(128) finish_kernel(FinishArgs a) {
-    constexpr int CH = D / 8;            // key channels per thread: 8 threads per row
-    constexpr int NCP = D / 2;           // value channel pairs
-    constexpr int NRP = 128 / NCP;       // row phases of the value sum (2 at D128, 4 at D64)
-    __shared__ float qs[D];
-    __shared__ float pbuf[128];
-    __shared__ float red[4];
-    __shared__ float2 osum[NRP][NCP];
-    const int tid = threadIdx.x;
+// One CTA (D threads) per (batch, query head): log-sum-exp merge of the
+// partials of the head's kv slot -> fp16 output.  A partial whose status is
+// set (a cache copy timed out) makes the output NaN.
+template <int D>
+__global__ void __launch_bounds__(D) finish_kernel(FinishArgs a) {
+    const int c = threadIdx.x;
     const long long bh = blockIdx.x;
-    const int b = (int)(bh / a.Hq), h = (int)(bh % a.Hq), hk = h / NQ;
-    const long long slot = (long long)b * a.Hkv + hk;
-    for (int c = tid; c < D; c += 128) qs[c] = __half2float(a.q[bh * D + c]) * a.scale_log2;
-    __syncthreads();
-
-    const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + slot * a.R * D;
-    const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + slot * a.R * D;
-    const int rs = tid >> 3, ck = tid & 7;        // score layout: row slot, channel chunk
-    float qreg[CH];
-#pragma unroll
-    for (int c = 0; c < CH; ++c) qreg[c] = qs[ck * CH + c];
-    const int cp = tid % NCP, rp = tid / NCP;     // value layout: channel pair, row phase
-    float m = -INFINITY, l = 0.f;
-    float2 o = make_float2(0.f, 0.f);
-    for (int t0 = 0; t0 < a.n_resid; t0 += 128) {
-        const int nrows = min(128, a.n_resid - t0);
-        // every lane runs the same trip count (the shuffles below need the whole warp)
-        for (int r16 = 0; r16 < nrows; r16 += 16) {
-            const int rr = r16 + rs;
-            const bool valid = rr < nrows;
-            const uint4* src = reinterpret_cast<const uint4*>(kr + (long long)(t0 + (valid ? rr : 0)) * D + ck * CH);
-            float s = 0.f;
-#pragma unroll
-            for (int v = 0; v < CH / 8; ++v) {
-                const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 kv = unpack_f16x2(w[e]);
-                    s = fmaf(qreg[8 * v + 2 * e], kv.x, fmaf(qreg[8 * v + 2 * e + 1], kv.y, s));
-                }
-            }
-            s += __shfl_xor_sync(kFull, s, 1);
-            s += __shfl_xor_sync(kFull, s, 2);
-            s += __shfl_xor_sync(kFull, s, 4);
-            if (ck == 0 && valid) pbuf[rr] = s;
-        }
-        __syncthreads();
-        const float sv = tid < nrows ? pbuf[tid] : -INFINITY;
-        const float mn = fmaxf(m, block_max128(sv, red));
-        const float pv = tid < nrows ? fast_exp2(sv - mn) : 0.f;
-        const float alpha = fast_exp2(m - mn);
-        const float ps = block_sum128(pv, red);
-        if (tid < nrows) pbuf[tid] = pv;
-        __syncthreads();
-        l = l * alpha + ps;
-        o.x *= alpha;
-        o.y *= alpha;
-        m = mn;
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const uint32_t* vcol = reinterpret_cast<const uint32_t*>(vr + (long long)t0 * D) + cp;
-        int t = rp;
-        for (; t + 3 * NRP < nrows; t += 4 * NRP) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 v2 = unpack_f16x2(vcol[(long long)(t + u * NRP) * NCP]);
-                const float pt = pbuf[t + u * NRP];
-                acc[u].x = fmaf(pt, v2.x, acc[u].x);
-                acc[u].y = fmaf(pt, v2.y, acc[u].y);
-            }
-        }
-        for (; t < nrows; t += NRP) {
-            const float2 v2 = unpack_f16x2(vcol[(long long)t * NCP]);
-            acc[0].x = fmaf(pbuf[t], v2.x, acc[0].x);
-            acc[0].y = fmaf(pbuf[t], v2.y, acc[0].y);
-        }
-        o.x += (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
-        o.y += (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
-        __syncthreads();
-    }
-    osum[rp][cp] = o;
-    __syncthreads();
-
-    // merge with the quantized partials of this head
-    int nparts = 0;
-    if (a.pairs_per_slot > 0) {
-        const long long first = part_owner(slot * a.pairs_per_slot, a.total_pairs, a.n_ctas);
-        nparts = (int)(part_owner(slot * a.pairs_per_slot + a.pairs_per_slot - 1, a.total_pairs, a.n_ctas) - first + 1);
-    }
+    const long long slot = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.nq;
+    const int nparts = slot_parts(a.wm, slot);
     const float* base = a.ws + bh * kPartialSlots * partial_stride(D);
-    float M = m;
+    float M = -INFINITY;
     bool failed = false;
     for (int j = 0; j < nparts; ++j) {
         M = fmaxf(M, base[j * partial_stride(D)]);
         failed |= base[j * partial_stride(D) + 2] != 0.f;
     }
-    if (tid < D) {
-        float acc = 0.f, lsum = 0.f;
-        if (m != -INFINITY) {
-            float r = 0.f;
-#pragma unroll
-            for (int q = 0; q < NRP; ++q) r += (tid & 1) ? osum[q][tid >> 1].y : osum[q][tid >> 1].x;
-            const float e = fast_exp2(m - M);
-            acc = r * e;
-            lsum = l * e;
-        }
-        for (int j = 0; j < nparts; ++j) {
-            const float* ps = base + j * partial_stride(D);
-            if (ps[0] == -INFINITY) continue;
-            const float e = fast_exp2(ps[0] - M);
-            lsum = fmaf(ps[1], e, lsum);
-            acc = fmaf(ps[4 + tid], e, acc);
-        }
-        a.out[bh * D + tid] = failed ? __float2half_rn(NAN) : __float2half_rn(acc / lsum);
+    float acc = 0.f, lsum = 0.f;
+    for (int j = 0; j < nparts; ++j) {
+        const float* ps = base + j * partial_stride(D);
+        if (ps[0] == -INFINITY) continue;
+        const float e = fast_exp2(ps[0] - M);
+        lsum = fmaf(ps[1], e, lsum);
+        acc = fmaf(ps[4 + c], e, acc);
     }
+    a.out[bh * D + c] = failed ? __float2half_rn(NAN) : __float2half_rn(acc / lsum);
 }
 
 }  // namespace mma_detail

@@ -20,12 +20,13 @@ cudaError_t launch_one(mma_detail::Args& a, int num_sms, cudaStream_t st) {
         return e;
     }();
     if (init != cudaSuccess) return init;
-    const long long slots = a.pairs_per_slot > 0 ? a.total_pairs / a.pairs_per_slot : 1;
+    const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;
     long long n = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
-    if (n > a.total_pairs) n = a.total_pairs;
+    const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
+    if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every CTA owns a unit
     if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot
     if (n < 1) n = 1;
-    a.n_ctas = n;
+    a.wm.n = n;
     decode_mma_kernel<64, BB, NN, GG><<<(unsigned)n, kThreads, C::DYN_SMEM, st>>>(a);
     return cudaGetLastError();
 }
