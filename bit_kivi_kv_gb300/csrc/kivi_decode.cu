@@ -358,10 +358,20 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
                                    : launch_decode_mma_d64(m, g.bits, nq, g.G, plan.num_sms, st);
         if (e != cudaSuccess) return e;
         mma_detail::FinishArgs f{workspace, out, g.Hq, g.Hkv, nq, m.wm};
-        const unsigned grid = (unsigned)((long long)g.B * g.Hq);
-        if (g.D == 128) mma_detail::finish_kernel<128><<<grid, 128, 0, st>>>(f);
-        else mma_detail::finish_kernel<64><<<grid, 64, 0, st>>>(f);
+        // the merge may start while the main kernel drains; it waits for it on the GPU
+        cudaLaunchConfig_t lc{};
+        lc.gridDim = dim3((unsigned)((long long)g.B * g.Hq));
+        lc.blockDim = dim3((unsigned)g.D);
+        lc.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        e = g.D == 128 ? cudaLaunchKernelEx(&lc, mma_detail::finish_kernel<128>, f)
+                       : cudaLaunchKernelEx(&lc, mma_detail::finish_kernel<64>, f);
         *launches = 2;
+        if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
     DecodeArgs a{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,

@@ -121,6 +121,14 @@ __device__ __forceinline__ void tma_1d(void* dst, const void* src, uint32_t byte
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+__device__ __forceinline__ void mbar_expect_tx_u32(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma_1d_u32(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -242,44 +250,57 @@ struct Cfg {
     static constexpr int POS_ODD = 6;
 };
 
-// Build this warp's Qt B fragments (hi/lo of q_h * step) and its beta, from
-// the block's key (step, zero) entries; entries == nullptr means step 1,
-// zero 0 (the fp16 residual).
+// Build this warp's Qt B fragments (fp16 hi + lo parts of q_h * step) and
+// its beta = sum_c q_h[c] * zero_c, from the block's key (step, zero) entries;
+// entries == nullptr means step 1, zero 0 (the fp16 residual).  qh/ql hold the
+// fp16 hi/lo parts of the scaled query per channel pair; with s exact in fp16,
+// hi = rn(qh*s) and lo = rn(ql*s + (qh*s - hi)) (the inner residual is exact),
+// so hi + lo = q*s to about 22 bits.  off[j] is the lane's table offset of
+// channel pair lane + 32j (head 0, hi column).
 template <class C, int D, int NQ>
 __device__ __forceinline__ void build_q_frags(const uint32_t* entries, const float (*qf)[D],
-                                              uint32_t* qfrag, int lane, uint32_t (&qb)[2 * C::KSTEPS],
-                                              float& beta) {
+                                              const uint32_t (*qh)[D / 2], const uint32_t (*ql)[D / 2],
+                                              const int (&off)[D / 64], uint32_t* qfrag, int lane,
+                                              uint32_t (&qb)[2 * C::KSTEPS], float& beta) {
+    constexpr int HEAD = 8 * C::QSTRIDE;      // table distance between heads' hi columns
+    constexpr int LOC = 4 * C::QSTRIDE;       // hi column -> lo column
     float bp[NQ];
 #pragma unroll
     for (int h = 0; h < NQ; ++h) bp[h] = 0.f;
     __syncwarp();
 #pragma unroll
-    for (int cp = lane; cp < D / 2; cp += 32) {
-        float s0 = 1.f, s1 = 1.f, z0 = 0.f, z1 = 0.f;
+    for (int j = 0; j < D / 64; ++j) {
+        const int cp = lane + 32 * j;
         if (entries) {
             const uint2 e = *reinterpret_cast<const uint2*>(entries + 2 * cp);
-            const float2 a = unpack_f16x2(e.x), b = unpack_f16x2(e.y);
-            s0 = a.x; z0 = a.y; s1 = b.x; z1 = b.y;
-        }
-        const int kk = cp >> 3, cc = (2 * cp) & 15, reg = cc >> 3, ii = (cc & 7) >> 1;
+            const uint32_t s2 = __byte_perm(e.x, e.y, 0x5410);
+            const float2 z = unpack_f16x2(__byte_perm(e.x, e.y, 0x7632));
 #pragma unroll
-        for (int h = 0; h < NQ; ++h) {
-            const float x0 = qf[h][2 * cp] * s0, x1 = qf[h][2 * cp + 1] * s1;
-            bp[h] = fmaf(qf[h][2 * cp], z0, fmaf(qf[h][2 * cp + 1], z1, bp[h]));
-            const uint32_t hi = pack_f16x2(x0, x1);
-            const float2 hf = unpack_f16x2(hi);
-            const uint32_t lo = pack_f16x2(x0 - hf.x, x1 - hf.y);
-            qfrag[(4 * (2 * h) + ii) * C::QSTRIDE + 2 * kk + reg] = hi;
-            qfrag[(4 * (2 * h + 1) + ii) * C::QSTRIDE + 2 * kk + reg] = lo;
+            for (int h = 0; h < NQ; ++h) {
+                const uint32_t hi = hmul2(qh[h][cp], s2);
+                const uint32_t lo = hfma2(ql[h][cp], s2, hfma2(qh[h][cp], s2, neg_f16x2(hi)));
+                const float2 q2 = *reinterpret_cast<const float2*>(&qf[h][2 * cp]);
+                bp[h] = fmaf(q2.x, z.x, fmaf(q2.y, z.y, bp[h]));
+                qfrag[off[j] + h * HEAD] = hi;
+                qfrag[off[j] + h * HEAD + LOC] = lo;
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < NQ; ++h) {
+                qfrag[off[j] + h * HEAD] = qh[h][cp];
+                qfrag[off[j] + h * HEAD + LOC] = ql[h][cp];
+            }
         }
     }
     const int i = lane & 3;
     beta = 0.f;
+    if (entries) {
 #pragma unroll
-    for (int h = 0; h < NQ; ++h) {
+        for (int h = 0; h < NQ; ++h) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) bp[h] += __shfl_xor_sync(kFull, bp[h], o);
-        if (i == h) beta = bp[h];
+            for (int o = 16; o > 0; o >>= 1) bp[h] += __shfl_xor_sync(kFull, bp[h], o);
+            if (i == h) beta = bp[h];
+        }
     }
     __syncwarp();
     const uint4* row = reinterpret_cast<const uint4*>(qfrag + lane * C::QSTRIDE);
@@ -294,7 +315,8 @@ template <int D, int BITS, int NQ, int G>
 __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     using C = Cfg<D, BITS, NQ, G>;
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
-    __shared__ float qf[NQ][D];
+    __shared__ __align__(16) float qf[NQ][D];
+    __shared__ uint32_t qh_s[NQ][D / 2], ql_s[NQ][D / 2];   // fp16 hi / lo of the scaled query
     __shared__ __align__(16) uint32_t qfrag_all[kWarps][32 * C::QSTRIDE];
     __shared__ float red_m[kWarps][NQ], red_l[kWarps][NQ];
     __shared__ float red_o[kWarps][NQ][D];
@@ -317,6 +339,14 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     if (tid == 0) red_status = 0u;
     __syncthreads();
 
+    int qoff[D / 64];     // this lane's Qt table offsets (channel pairs lane + 32j)
+#pragma unroll
+    for (int j = 0; j < D / 64; ++j) {
+        const int cp = lane + 32 * j, cc = (2 * cp) & 15;
+        qoff[j] = ((cc & 7) >> 1) * C::QSTRIDE + 2 * (cp >> 3) + (cc >> 3);
+    }
+    const uint32_t ring_u32 = smem_u32(ring), bars_u32 = smem_u32(bars);
+    const long long vdelta = a.NB * a.part_bytes;    // key part -> value part of a block
     // this lane's B column for the values: head hP, group slot jP, hi/lo
     const int colP = g >> 1, hP = colP / GB, jP = colP % GB;
     const bool lo_col = (g & 1) != 0;
@@ -423,9 +453,17 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         const int part = (int)(cta - slot_first_cta(wm, slot));
         const int b = (int)(slot / a.Hkv), hk = (int)(slot % a.Hkv);
         const uint8_t* slot_base = a.cache + slot * a.slot_bytes;
-        for (int idx = tid; idx < NQ * D; idx += kThreads) {
-            const int j = idx / D, c = idx % D;
-            qf[j][c] = __half2float(a.q[((long long)b * a.Hq + hk * NQ + j) * D + c]) * a.scale_log2;
+        for (int idx = tid; idx < NQ * D / 2; idx += kThreads) {
+            const int j = idx / (D / 2), cp = idx % (D / 2);
+            const float2 qv = __half22float2(
+                *reinterpret_cast<const __half2*>(a.q + ((long long)b * a.Hq + hk * NQ + j) * D + 2 * cp));
+            const float x0 = qv.x * a.scale_log2, x1 = qv.y * a.scale_log2;
+            qf[j][2 * cp] = x0;
+            qf[j][2 * cp + 1] = x1;
+            const uint32_t hi = pack_f16x2(x0, x1);
+            const float2 hf = unpack_f16x2(hi);
+            qh_s[j][cp] = hi;
+            ql_s[j][cp] = pack_f16x2(x0 - hf.x, x1 - hf.y);
         }
         __syncthreads();
 
@@ -440,22 +478,26 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
         const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
         auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
-        auto issue = [&](int pr, uint32_t it) {      // lane 0: ring stage of item it <- pair pr
-            const int T = 2 * pr;
-            const int blk = T / C::TPB, tin = T % C::TPB;
-            const uint8_t* kpart = slot_base + (long long)blk * a.part_bytes;
-            const uint8_t* vpart = kpart + a.NB * a.part_bytes;
-            const int st = (int)(it % C::STAGES);
-            uint8_t* dst = ring + st * C::STAGE_BYTES;
-            const bool kz = need_ksz(pr);
-            mbar_expect_tx(&bars[st], 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
-            tma_1d(dst, kpart + tin * C::TILE, 2 * C::TILE, &bars[st]);
-            tma_1d(dst + 2 * C::TILE, vpart + tin * C::TILE, 2 * C::TILE, &bars[st]);
-            tma_1d(dst + 4 * C::TILE, vpart + tiles_bytes + tin * C::ENT, 2 * C::ENT, &bars[st]);
-            if (kz) tma_1d(dst + 4 * C::TILE + 2 * C::ENT, kpart + tiles_bytes, C::KSZ, &bars[st]);
+        // lane 0's copy cursor: key part of the block of the next pair to fetch, tile in block
+        const uint8_t* kcur = slot_base + (long long)((2 * wb) / C::TPB) * a.part_bytes;
+        int tcur = (2 * wb) % C::TPB;
+        bool first = true;
+        auto issue_next = [&](uint32_t it) {          // lane 0: next pair -> ring stage of item it
+            const uint32_t st = it % C::STAGES;
+            const uint32_t dst = ring_u32 + st * C::STAGE_BYTES, bar = bars_u32 + 8 * st;
+            const bool kz = first || tcur == 0;
+            const uint8_t* vcur = kcur + vdelta;
+            mbar_expect_tx_u32(bar, 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
+            tma_1d_u32(dst, kcur + tcur * C::TILE, 2 * C::TILE, bar);
+            tma_1d_u32(dst + 2 * C::TILE, vcur + tcur * C::TILE, 2 * C::TILE, bar);
+            tma_1d_u32(dst + 4 * C::TILE, vcur + tiles_bytes + tcur * C::ENT, 2 * C::ENT, bar);
+            if (kz) tma_1d_u32(dst + 4 * C::TILE + 2 * C::ENT, kcur + tiles_bytes, C::KSZ, bar);
+            first = false;
+            tcur += 2;
+            if (tcur == C::TPB) { tcur = 0; kcur += a.part_bytes; }
         };
         if (lane == 0) {
-            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue(wb + k, item + k);
+            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
         }
         float cinit[4] = {0.f, 0.f, 0.f, 0.f};   // -1024 * sum_c Qt[c][n] of the current block
         int k = 0;
@@ -467,7 +509,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             const int pr = wb + k;
             if (need_ksz(pr)) {
                 build_q_frags<C, D, NQ>(reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + 2 * C::ENT), qf,
-                                        qfrag, lane, qb, beta);
+                                        qh_s, ql_s, qoff, qfrag, lane, qb, beta);
                 cinit[0] = cinit[1] = cinit[2] = cinit[3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) mma16816(cinit, kNeg1024, qb[2 * kk], qb[2 * kk + 1]);
@@ -525,7 +567,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             __syncwarp();                              // every lane is done with this stage
             if (lane == 0 && k + C::STAGES < npairs) {
                 fence_proxy_async();
-                issue(wb + k + C::STAGES, it + C::STAGES);
+                issue_next(it + C::STAGES);
             }
         }
         if (k < npairs) {
@@ -555,7 +597,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + slot * a.R * D;
             const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + slot * a.R * D;
             const int n = a.n_resid;
-            build_q_frags<C, D, NQ>(nullptr, qf, qfrag, lane, qb, beta);   // step 1, zero 0
+            build_q_frags<C, D, NQ>(nullptr, qf, qh_s, ql_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
             for (int rp = rb; rp < re; ++rp) {
                 float sc[4];
 #pragma unroll
@@ -658,6 +700,9 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 // set (a cache copy timed out) makes the output NaN.
 template <int D>
 __global__ void __launch_bounds__(D) finish_kernel(FinishArgs a) {
+    // launched as a programmatic dependent of the main kernel: wait until its
+    // partial results are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int c = threadIdx.x;
     const long long bh = blockIdx.x;
     const long long slot = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.nq;
