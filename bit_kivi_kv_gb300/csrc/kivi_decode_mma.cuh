@@ -17,16 +17,15 @@
 //            one fragment per 16-token tile; a lane keeps the accumulators of
 //            the column pair that matches its channels' group.
 //
-// Codes enter the MMA without arithmetic: each tile word is shifted so a code
-// field sits at bit 6 or 8 of an fp16 mantissa whose exponent is 2^10, which
-// reads as 1024 + 2^pos * code (exact).  The 1024 offset is removed exactly by
-// MMAs with a constant -1024 A operand (keys: once per block, as the
-// accumulator's start; values: a side accumulator), and the 2^-pos factor is
-// applied to the results.  Offset and value stay within a factor ~10 of each
-// other, so fp32 accumulation keeps ~20 bits of the result.
-// Online softmax per warp in the log2 domain; each warp owns a contiguous run
-// of the split's tiles, taken two tiles (32 tokens) per ring stage; warps and
-// splits merge by log-sum-exp.
+// Codes come out of the tile words exactly: a code field masked into an fp16
+// mantissa whose exponent is 2^10 reads as 1024 + 4^u * code, and one f16x2 FMA
+// with (4^-u, -1024 * 4^-u) returns the code (all values exact in fp16).  This
+// keeps the integer (ALU) pipe, the busiest one, at one mask per code pair plus
+// one shift per word; the FMA pipe takes the normalization.
+// Online softmax per warp in the log2 domain; each CTA of a persistent grid
+// owns a balanced, weight-proportional share of the call's work (tile pairs of
+// 32 tokens, then fp16 residual pairs); warps split it and merge by
+// log-sum-exp, one partial result per slot; a merge kernel combines them.
 #pragma once
 
 #include <math.h>
@@ -94,6 +93,23 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 __device__ __forceinline__ uint2 ldg_stream2(const void* p) {
     uint2 v;
     asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// ---- shared-memory loads through 32-bit shared addresses ----
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
 }
 
@@ -177,32 +193,6 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int u) {
     return hfma2(x, sc | (sc << 16), bi | (bi << 16));
 }
 
-// f16x2 pair of codes of slot u, left as 1024 + 2^pos * code: the word is
-// shifted so the field lands at mantissa bits [pos, pos + BITS).  For 2-bit
-// codes even slots land at pos 8 and odd slots at pos 6; 4-bit codes at pos 6.
-template <int BITS>
-__device__ __forceinline__ uint32_t code_pair_raw(uint32_t w, int u) {
-    if constexpr (BITS == 2) {
-        const int sh = u == 0 ? 8 : u <= 2 ? 4 : u <= 4 ? 0 : u <= 6 ? -4 : -8;
-        const uint32_t src = sh > 0 ? (w << sh) : sh < 0 ? (w >> (-sh)) : w;
-        return (src & ((u & 1) ? 0x00C000C0u : 0x03000300u)) | 0x64006400u;
-    } else {
-        const int sh = 6 - 4 * u;
-        const uint32_t src = sh > 0 ? (w << sh) : (w >> (-sh));
-        return (src & 0x03C003C0u) | 0x64006400u;
-    }
-}
-
-template <int BITS, int W>
-__device__ __forceinline__ void a_frag_raw(const uint32_t (&w)[W], int kk, uint32_t (&a)[4]) {
-    constexpr int PER = 16 / BITS;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int p = 4 * kk + r;
-        a[r] = code_pair_raw<BITS>(w[p / PER], p % PER);
-    }
-}
-
 // A fragment (4 registers) of k-step / m-tile kk from a lane's tile words.
 template <int BITS, int W>
 __device__ __forceinline__ void a_frag(const uint32_t (&w)[W], const uint32_t (&w8)[W], int kk, uint32_t (&a)[4]) {
@@ -245,9 +235,6 @@ struct Cfg {
     // entries, and the block's key entries
     static constexpr int STAGE_BYTES = 4 * TILE + 2 * ENT + KSZ;
     static constexpr int DYN_SMEM = kWarps * STAGES * STAGE_BYTES;
-    // mantissa position of the codes of A rows g (even slots) and g+8 (odd slots)
-    static constexpr int POS_EVEN = BITS == 2 ? 8 : 6;
-    static constexpr int POS_ODD = 6;
 };
 
 // Build this warp's Qt B fragments (fp16 hi + lo parts of q_h * step) and
@@ -353,15 +340,21 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     const bool col_ok = hP < NQ;
     // this lane's output columns (2i, 2i+1): head hO, group slot jO
     const int hO = i / GB, jO = i % GB;
-    const uint32_t kNeg1024[4] = {0xE400E400u, 0xE400E400u, 0xE400E400u, 0xE400E400u};
-    constexpr float kScaleEven = 1.0f / (float)(1 << C::POS_EVEN);
-    constexpr float kScaleOdd = 1.0f / (float)(1 << C::POS_ODD);
     const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
+    // byte offsets, inside a stage's value entries, of this lane's 4 tokens x NBF groups
+    uint32_t eoff[NBF][4];
+#pragma unroll
+    for (int f = 0; f < NBF; ++f) {
+        const int gr = f * GB + jP;
+        eoff[f][0] = 4u * (tokA * NGRP + gr);
+        eoff[f][1] = 4u * ((tokA + 1) * NGRP + gr);
+        eoff[f][2] = 4u * (tokB * NGRP + gr);
+        eoff[f][3] = 4u * ((tokB + 1) * NGRP + gr);
+    }
     const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
 
     float m, l;
     float o[KS][4];
-    float voff[NBF][4];   // -1024 * sum_t Pt[t][n]: removes the code offset of the value MMAs
     float zeta[NBF];
     uint32_t qb[2 * KS];
     float beta = 0.f;
@@ -382,8 +375,6 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             const float ao = __shfl_sync(kFull, alpha, (lane & ~3) | (hO < NQ ? hO : 0));
 #pragma unroll
             for (int t = 0; t < KS; ++t) { o[t][0] *= ao; o[t][1] *= ao; o[t][2] *= ao; o[t][3] *= ao; }
-#pragma unroll
-            for (int f = 0; f < NBF; ++f) { voff[f][0] *= ao; voff[f][1] *= ao; voff[f][2] *= ao; voff[f][3] *= ao; }
             const float az = __shfl_sync(kFull, alpha, col_ok ? hP : 0);
 #pragma unroll
             for (int f = 0; f < NBF; ++f) zeta[f] *= az;
@@ -423,15 +414,16 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         pl01 = pack_f16x2(pr[0] - f01.x, pr[1] - f01.y);
         pl89 = pack_f16x2(pr[2] - f89.x, pr[3] - f89.y);
     };
-    auto lds_words = [&](const uint8_t* src, uint32_t (&w)[W]) {
+    const uint32_t lane_words = (uint32_t)(lane * W * 4);
+    auto lds_words = [&](uint32_t src, uint32_t (&w)[W]) {   // this lane's words of a tile at src
         if constexpr (W % 4 == 0) {
 #pragma unroll
             for (int v = 0; v < W / 4; ++v) {
-                const uint4 x = reinterpret_cast<const uint4*>(src + lane * W * 4)[v];
+                const uint4 x = lds128(src + lane_words + 16 * v);
                 w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
             }
         } else {
-            const uint2 x = *reinterpret_cast<const uint2*>(src + lane * W * 4);
+            const uint2 x = lds64(src + lane_words);
             w[0] = x.x; w[1] = x.y;
         }
     };
@@ -471,7 +463,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 #pragma unroll
         for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
 #pragma unroll
-        for (int f = 0; f < NBF; ++f) zeta[f] = voff[f][0] = voff[f][1] = voff[f][2] = voff[f][3] = 0.f;
+        for (int f = 0; f < NBF; ++f) zeta[f] = 0.f;
 
         // ---- this warp's contiguous run of pairs, two tiles per ring stage ----
         const int pw = (p1 - p0 + kWarps - 1) / kWarps;
@@ -499,41 +491,39 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         if (lane == 0) {
             for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
         }
-        float cinit[4] = {0.f, 0.f, 0.f, 0.f};   // -1024 * sum_c Qt[c][n] of the current block
         int k = 0;
         for (; k < npairs; ++k) {
             const uint32_t it = item + k;
             const int st = (int)(it % C::STAGES);
             if (!__all_sync(kFull, mbar_wait(&bars[st], (it / C::STAGES) & 1u))) break;
             const uint8_t* stage = ring + st * C::STAGE_BYTES;
+            const uint32_t stage_u32 = ring_u32 + st * C::STAGE_BYTES;
             const int pr = wb + k;
-            if (need_ksz(pr)) {
+            if (need_ksz(pr))
                 build_q_frags<C, D, NQ>(reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + 2 * C::ENT), qf,
                                         qh_s, ql_s, qoff, qfrag, lane, qb, beta);
-                cinit[0] = cinit[1] = cinit[2] = cinit[3] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < KS; ++kk) mma16816(cinit, kNeg1024, qb[2 * kk], qb[2 * kk + 1]);
-            }
             // keys: logits of tokens g, g+8 of both tiles for head i
             float sc[4];
             {
-                uint32_t wa[W], wbw[W];
-                lds_words(stage, wa);
-                lds_words(stage + C::TILE, wbw);
-                float ca[4] = {cinit[0], cinit[1], cinit[2], cinit[3]};
-                float cb[4] = {cinit[0], cinit[1], cinit[2], cinit[3]};
+                uint32_t wa[W], wbw[W], wa8[W], wb8[W];
+                lds_words(stage_u32, wa);
+                lds_words(stage_u32 + C::TILE, wbw);
+#pragma unroll
+                for (int x = 0; x < W; ++x) { wa8[x] = wa[x] >> 8; wb8[x] = wbw[x] >> 8; }
+                float ca[4] = {beta, 0.f, beta, 0.f};
+                float cb[4] = {beta, 0.f, beta, 0.f};
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     uint32_t fa[4], fb[4];
-                    a_frag_raw<BITS, W>(wa, kk, fa);
-                    a_frag_raw<BITS, W>(wbw, kk, fb);
+                    a_frag<BITS, W>(wa, wa8, kk, fa);
+                    a_frag<BITS, W>(wbw, wb8, kk, fb);
                     mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
                     mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
                 }
-                sc[0] = fmaf(ca[0] + ca[1], kScaleEven, beta);
-                sc[1] = fmaf(ca[2] + ca[3], kScaleOdd, beta);
-                sc[2] = fmaf(cb[0] + cb[1], kScaleEven, beta);
-                sc[3] = fmaf(cb[2] + cb[3], kScaleOdd, beta);
+                sc[0] = ca[0] + ca[1];
+                sc[1] = ca[2] + ca[3];
+                sc[2] = cb[0] + cb[1];
+                sc[3] = cb[2] + cb[3];
             }
             float p[4];
             softmax(sc, p);
@@ -544,22 +534,22 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                 gather(p[2 * t], p[2 * t + 1], prb);
                 uint32_t ph01, ph89, pl01, pl89;
                 split_p(prb, ph01, ph89, pl01, pl89);
-                const uint32_t* ve = reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + t * C::ENT);
+                const uint32_t ve = stage_u32 + 4 * C::TILE + t * C::ENT;
                 uint32_t pb[NBF][2];
 #pragma unroll
                 for (int f = 0; f < NBF; ++f) {
-                    const int gr = f * GB + jP;
-                    const uint32_t e[4] = {ve[tokA * NGRP + gr], ve[(tokA + 1) * NGRP + gr], ve[tokB * NGRP + gr],
-                                           ve[(tokB + 1) * NGRP + gr]};
+                    const uint32_t e[4] = {lds32(ve + eoff[f][0]), lds32(ve + eoff[f][1]), lds32(ve + eoff[f][2]),
+                                           lds32(ve + eoff[f][3])};
                     p_frag(prb, ph01, ph89, pl01, pl89, e, pb[f][0], pb[f][1], zeta[f]);
-                    mma16816(voff[f], kNeg1024, pb[f][0], pb[f][1]);
                 }
-                uint32_t wv[W];
-                lds_words(stage + (2 + t) * C::TILE, wv);
+                uint32_t wv[W], wv8[W];
+                lds_words(stage_u32 + (2 + t) * C::TILE, wv);
+#pragma unroll
+                for (int x = 0; x < W; ++x) wv8[x] = wv[x] >> 8;
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t af[4];
-                    a_frag_raw<BITS, W>(wv, mt, af);
+                    a_frag<BITS, W>(wv, wv8, mt, af);
                     const int f = (16 * mt / G) / GB;
                     mma16816(o[mt], af, pb[f][0], pb[f][1]);
                 }
@@ -578,18 +568,6 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                 mbar_wait(&bars[(item + u) % C::STAGES], ((item + u) / C::STAGES) & 1u);
         }
         item += (uint32_t)npairs;
-        // undo the code offset and the code position factor of the value accumulators
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int f = (16 * mt / G) / GB;
-            o[mt][0] = (o[mt][0] + voff[f][0]) * kScaleEven;
-            o[mt][1] = (o[mt][1] + voff[f][1]) * kScaleEven;
-            o[mt][2] = (o[mt][2] + voff[f][2]) * kScaleOdd;
-            o[mt][3] = (o[mt][3] + voff[f][3]) * kScaleOdd;
-        }
-#pragma unroll
-        for (int f = 0; f < NBF; ++f) voff[f][0] = voff[f][1] = voff[f][2] = voff[f][3] = 0.f;
-
         // ---- this warp's residual pairs: 32 fp16 rows each, A operands straight from memory ----
         const int rw = (r1 - r0 + kWarps - 1) / kWarps;
         const int rb = min(r0 + warp * rw, r1), re = min(rb + rw, r1);
