@@ -177,30 +177,50 @@ __device__ __forceinline__ float fast_exp2(float x) {   // hardware 2^x (ex2.app
     return y;
 }
 
+// Constants of the code unpack, kept in registers for the whole kernel (made
+// opaque so the compiler does not rebuild them per use): the fp16 pair
+// 1024|1024, and per field position e = 0..4 the scale 2^-(2e) and the bias
+// -2^(10-2e) (2-bit codes; 4-bit codes use positions 0 and 1, e = 0 and 4).
+struct UnpackConsts {
+    uint32_t magic;
+    uint32_t sc[5], bi[5];
+};
+template <int BITS>
+__device__ __forceinline__ UnpackConsts make_unpack_consts() {
+    UnpackConsts k;
+    asm volatile("mov.b32 %0, 0x64006400;" : "=r"(k.magic));
+#pragma unroll
+    for (int pos = 0; pos < 5; ++pos) {
+        const uint32_t e = (uint32_t)(BITS * pos) < 15u ? (uint32_t)(BITS * pos) : 14u;
+        const uint32_t sc = (15u - e) << 10, bi = 0x8000u | ((25u - e) << 10);
+        asm volatile("mov.b32 %0, %1;" : "=r"(k.sc[pos]) : "r"(sc | (sc << 16)));
+        asm volatile("mov.b32 %0, %1;" : "=r"(k.bi[pos]) : "r"(bi | (bi << 16)));
+    }
+    return k;
+}
+
 // Exact f16x2 pair of codes of slot u of a tile word (w8 = w >> 8).
 template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int u) {
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int u, const UnpackConsts& k) {
     constexpr int PER = 16 / BITS;
     constexpr int DIRECT = BITS == 2 ? 5 : 2;          // slots whose field sits in mantissa bits 0..9
     const int pos = u < DIRECT ? u : u - PER / 2;       // position after the optional 8-bit shift
     const uint32_t src = u < DIRECT ? w : w8;
     const uint32_t field = (BITS == 2 ? 0x00030003u : 0x000F000Fu) << (BITS * pos);
-    const uint32_t x = (src & field) | 0x64006400u;     // 1024 + code * 2^(BITS*pos)
-    // scale 2^(-BITS*pos), bias -1024 * 2^(-BITS*pos); fp16 exponent field shifts by BITS*pos
-    const uint32_t e = (uint32_t)(BITS * pos);
-    const uint32_t sc = (uint32_t)(15 - e) << 10;               // 2^-e
-    const uint32_t bi = 0x8000u | ((uint32_t)(25 - e) << 10);   // -2^(10-e)
-    return hfma2(x, sc | (sc << 16), bi | (bi << 16));
+    uint32_t x;                                          // (src & field) | 1024|1024
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x) : "r"(src), "r"(field), "r"(k.magic));
+    return hfma2(x, k.sc[pos], k.bi[pos]);              // code = x * 2^-(BITS*pos) - 1024 * 2^-(BITS*pos)
 }
 
 // A fragment (4 registers) of k-step / m-tile kk from a lane's tile words.
 template <int BITS, int W>
-__device__ __forceinline__ void a_frag(const uint32_t (&w)[W], const uint32_t (&w8)[W], int kk, uint32_t (&a)[4]) {
+__device__ __forceinline__ void a_frag(const uint32_t (&w)[W], const uint32_t (&w8)[W], int kk, uint32_t (&a)[4],
+                                       const UnpackConsts& k) {
     constexpr int PER = 16 / BITS;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int p = 4 * kk + r;
-        a[r] = code_pair<BITS>(w[p / PER], w8[p / PER], p % PER);
+        a[r] = code_pair<BITS>(w[p / PER], w8[p / PER], p % PER, k);
     }
 }
 
@@ -340,6 +360,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     const bool col_ok = hP < NQ;
     // this lane's output columns (2i, 2i+1): head hO, group slot jO
     const int hO = i / GB, jO = i % GB;
+    const UnpackConsts ukc = make_unpack_consts<BITS>();
     const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
     // byte offsets, inside a stage's value entries, of this lane's 4 tokens x NBF groups
     uint32_t eoff[NBF][4];
@@ -515,8 +536,8 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     uint32_t fa[4], fb[4];
-                    a_frag<BITS, W>(wa, wa8, kk, fa);
-                    a_frag<BITS, W>(wbw, wb8, kk, fb);
+                    a_frag<BITS, W>(wa, wa8, kk, fa, ukc);
+                    a_frag<BITS, W>(wbw, wb8, kk, fb, ukc);
                     mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
                     mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
                 }
@@ -549,7 +570,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t af[4];
-                    a_frag<BITS, W>(wv, wv8, mt, af);
+                    a_frag<BITS, W>(wv, wv8, mt, af, ukc);
                     const int f = (16 * mt / G) / GB;
                     mma16816(o[mt], af, pb[f][0], pb[f][1]);
                 }
