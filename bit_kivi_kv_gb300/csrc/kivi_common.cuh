@@ -36,6 +36,29 @@ constexpr int kPartialSlots = kMaxSplits + 1;  // + one split for the fp16 resid
 // status != 0 marks a split whose cache copy did not complete (its output is NaN).
 __host__ __device__ constexpr int partial_stride(int D) { return D + 4; }
 
+// ---- code-tile placement (kivi.h, "Code tile") ----
+// A lane's code pair (k, r) has class c and order h; it sits in lane word
+// c / P, P = 8 / BITS, at bit 8*h + BITS*(c % P) of each 16-bit half.  Keys:
+// c = 2k + r/2, h = r%2; values: c = 2k + r%2, h = r/2.  In both cases
+// c = channel / 8, so a code masked in place is the fp16 value
+// code * 2^(BITS*((channel/8) % P) - 24).
+template <int BITS, bool VALUES>
+struct PairPlace {
+    static constexpr int P = 8 / BITS;
+    __host__ __device__ static constexpr int cls(int k, int r) { return 2 * k + (VALUES ? (r & 1) : (r >> 1)); }
+    __host__ __device__ static constexpr int order(int r) { return VALUES ? (r >> 1) : (r & 1); }
+    __host__ __device__ static constexpr int word(int k, int r) { return cls(k, r) / P; }
+    __host__ __device__ static constexpr int bit(int k, int r) { return 8 * order(r) + BITS * (cls(k, r) % P); }
+    // inverse: the pair in lane word wl, slot u (byte u / P, position u % P)
+    __host__ __device__ static constexpr int k_of(int wl, int u) { return (wl * P + u % P) >> 1; }
+    __host__ __device__ static constexpr int r_of(int wl, int u) {
+        return VALUES ? ((wl * P + u % P) & 1) + 2 * (u / P) : 2 * ((wl * P + u % P) & 1) + u / P;
+    }
+};
+
+// Position of token t (0..15) of a tile inside a row of its value entry tile.
+__host__ __device__ constexpr int entry_pos(int t) { return 4 * ((t & 7) >> 1) + 2 * (t >> 3) + (t & 1); }
+
 // Balanced partition of a decode call's work over the CTAs of the tensor-core
 // kernel.  Per (batch, kv-head) slot the work is a row of units: P quantized
 // tile pairs (32 tokens) of weight wq, then PR fp16 residual pairs (32 rows) of

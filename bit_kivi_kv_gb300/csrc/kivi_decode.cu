@@ -82,7 +82,6 @@ template <int D, int BITS, int NQ>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     constexpr int L = (1 << BITS) - 1;
     constexpr int W = D * BITS / 64;
-    constexpr int PER = 16 / BITS;
     constexpr int PAIRS = D / 4;
     constexpr int VCH = D / 8;           // value channels per lane
     __shared__ float qf[NQ][D];
@@ -124,12 +123,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
             if (blk != cur_blk) {            // fold this block's key steps into q
                 cur_blk = blk;
                 __syncwarp();                // all lanes are done reading the previous block's qt
-                const __half2* ksz = reinterpret_cast<const __half2*>(kpart + tiles_bytes);
+                const __half* ks = reinterpret_cast<const __half*>(kpart + tiles_bytes);   // D steps, D zeros
                 float bp[NQ];
 #pragma unroll
                 for (int j = 0; j < NQ; ++j) bp[j] = 0.f;
                 for (int c = lane; c < D; c += 32) {
-                    const float2 sz = __half22float2(ksz[c]);
+                    const float2 sz = make_float2(__half2float(ks[c]), __half2float(ks[D + c]));
 #pragma unroll
                     for (int j = 0; j < NQ; ++j) {
                         qt[warp][j][c] = qf[j][c] * sz.x;
@@ -152,10 +151,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
             for (int j = 0; j < NQ; ++j) part[j][0] = part[j][1] = 0.f;
 #pragma unroll
             for (int p = 0; p < PAIRS; ++p) {
-                const int k = p >> 2, r = p & 3, u = p % PER;
-                const uint32_t w = kw[p / PER];
-                const float c0 = (float)((w >> (BITS * u)) & L);
-                const float c1 = (float)((w >> (16 + BITS * u)) & L);
+                using PP = PairPlace<BITS, false>;
+                const int k = p >> 2, r = p & 3, bit = PP::bit(k, r);
+                const uint32_t w = kw[PP::word(k, r)];
+                const float c0 = (float)((w >> bit) & L);
+                const float c1 = (float)((w >> (16 + bit)) & L);
                 const int ch = 16 * k + 2 * i + 8 * (r >> 1);
 #pragma unroll
                 for (int j = 0; j < NQ; ++j) {
@@ -176,17 +176,19 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
             // ---- weighted values ----
             uint32_t vw[W];
             load_words(reinterpret_cast<const uint32_t*>(vpart + tin * a.tile_bytes) + lane * W, vw);
-            const __half2* vsz = reinterpret_cast<const __half2*>(vpart + tiles_bytes);
+            // this tile's entry tile: ngrp rows of 16 steps, then the zeros
+            const __half* vse = reinterpret_cast<const __half*>(vpart + tiles_bytes + (long long)tin * 64 * ngrp);
 #pragma unroll
             for (int p = 0; p < PAIRS; ++p) {
-                const int k = p >> 2, r = p & 3, u = p % PER;
-                const uint32_t w = vw[p / PER];
-                const float c0 = (float)((w >> (BITS * u)) & L);
-                const float c1 = (float)((w >> (16 + BITS * u)) & L);
+                using PP = PairPlace<BITS, true>;
+                const int k = p >> 2, r = p & 3, bit = PP::bit(k, r);
+                const uint32_t w = vw[PP::word(k, r)];
+                const float c0 = (float)((w >> bit) & L);
+                const float c1 = (float)((w >> (16 + bit)) & L);
                 const int ch = 16 * k + g + 8 * (r & 1);
-                const int tok0 = tin * 16 + 2 * i + 8 * (r >> 1);
-                const float2 sz0 = __half22float2(vsz[tok0 * ngrp + ch / G]);
-                const float2 sz1 = __half22float2(vsz[(tok0 + 1) * ngrp + ch / G]);
+                const int e0 = (ch / G) * 16 + entry_pos(2 * i + 8 * (r >> 1)), e1 = e0 + 1;   // tokens tau, tau+1
+                const float2 sz0 = make_float2(__half2float(vse[e0]), __half2float(vse[16 * ngrp + e0]));
+                const float2 sz1 = make_float2(__half2float(vse[e1]), __half2float(vse[16 * ngrp + e1]));
                 const float v0 = fmaf(c0, sz0.x, sz0.y), v1 = fmaf(c1, sz1.x, sz1.y);
                 const int vl = 2 * k + (r & 1), ts = 2 * (r >> 1);
 #pragma unroll

@@ -17,11 +17,14 @@
 //            one fragment per 16-token tile; a lane keeps the accumulators of
 //            the column pair that matches its channels' group.
 //
-// Codes come out of the tile words exactly: a code field masked into an fp16
-// mantissa whose exponent is 2^10 reads as 1024 + 4^u * code, and one f16x2 FMA
-// with (4^-u, -1024 * 4^-u) returns the code (all values exact in fp16).  This
-// keeps the integer (ALU) pipe, the busiest one, at one mask per code pair plus
-// one shift per word; the FMA pipe takes the normalization.
+// Codes enter the MMA straight from the tile words: a code pair masked in
+// place (one AND per A register, plus one 8-bit shift per word for the pairs
+// in the upper byte) is a pair of fp16 subnormals code * 2^(BITS*pos - 24),
+// exact, with pos = (channel / 8) % (8 / BITS) set by the cache layout.  For
+// keys the channel is the MMA's k index, so 2^-(BITS*pos) is folded into the
+// query side once per slot and the 2^-24 into the softmax; for values it is
+// the output row, so the accumulators are rescaled once after the quantized
+// tiles.  The integer pipe, the busiest one, does one mask per code pair.
 // Online softmax per warp in the log2 domain; each CTA of a persistent grid
 // owns a balanced, weight-proportional share of the call's work (tile pairs of
 // 32 tokens, then fp16 residual pairs); warps split it and merge by
@@ -74,7 +77,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
     return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
-__device__ __forceinline__ uint32_t neg_f16x2(uint32_t v) { return v ^ 0x80008000u; }
+__device__ __forceinline__ uint32_t neg_f16x2(uint32_t v) {
+    uint32_t d;
+    asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(v));
+    return d;
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -171,56 +178,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
     return false;
 }
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }   // 2^e, |e| < 127
 __device__ __forceinline__ float fast_exp2(float x) {   // hardware 2^x (ex2.approx, rel. err ~2^-22)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-// Constants of the code unpack, kept in registers for the whole kernel (made
-// opaque so the compiler does not rebuild them per use): the fp16 pair
-// 1024|1024, and per field position e = 0..4 the scale 2^-(2e) and the bias
-// -2^(10-2e) (2-bit codes; 4-bit codes use positions 0 and 1, e = 0 and 4).
-struct UnpackConsts {
-    uint32_t magic;
-    uint32_t sc[5], bi[5];
-};
-template <int BITS>
-__device__ __forceinline__ UnpackConsts make_unpack_consts() {
-    UnpackConsts k;
-    asm volatile("mov.b32 %0, 0x64006400;" : "=r"(k.magic));
-#pragma unroll
-    for (int pos = 0; pos < 5; ++pos) {
-        const uint32_t e = (uint32_t)(BITS * pos) < 15u ? (uint32_t)(BITS * pos) : 14u;
-        const uint32_t sc = (15u - e) << 10, bi = 0x8000u | ((25u - e) << 10);
-        asm volatile("mov.b32 %0, %1;" : "=r"(k.sc[pos]) : "r"(sc | (sc << 16)));
-        asm volatile("mov.b32 %0, %1;" : "=r"(k.bi[pos]) : "r"(bi | (bi << 16)));
-    }
-    return k;
-}
-
-// Exact f16x2 pair of codes of slot u of a tile word (w8 = w >> 8).
-template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int u, const UnpackConsts& k) {
-    constexpr int PER = 16 / BITS;
-    constexpr int DIRECT = BITS == 2 ? 5 : 2;          // slots whose field sits in mantissa bits 0..9
-    const int pos = u < DIRECT ? u : u - PER / 2;       // position after the optional 8-bit shift
-    const uint32_t src = u < DIRECT ? w : w8;
-    const uint32_t field = (BITS == 2 ? 0x00030003u : 0x000F000Fu) << (BITS * pos);
-    uint32_t x;                                          // (src & field) | 1024|1024
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x) : "r"(src), "r"(field), "r"(k.magic));
-    return hfma2(x, k.sc[pos], k.bi[pos]);              // code = x * 2^-(BITS*pos) - 1024 * 2^-(BITS*pos)
-}
-
-// A fragment (4 registers) of k-step / m-tile kk from a lane's tile words.
-template <int BITS, int W>
-__device__ __forceinline__ void a_frag(const uint32_t (&w)[W], const uint32_t (&w8)[W], int kk, uint32_t (&a)[4],
-                                       const UnpackConsts& k) {
-    constexpr int PER = 16 / BITS;
+// A fragment (4 registers) of k-step / m-tile t from a lane's tile words
+// (w8 = w >> 8): each register is one code pair masked in place, i.e. two fp16
+// subnormals code * 2^(BITS*pos - 24), pos = (channel / 8) % (8 / BITS).
+template <int BITS, bool VALUES, int W>
+__device__ __forceinline__ void a_frag(const uint32_t (&w)[W], const uint32_t (&w8)[W], int t, uint32_t (&a)[4]) {
+    using PP = PairPlace<BITS, VALUES>;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const int p = 4 * kk + r;
-        a[r] = code_pair<BITS>(w[p / PER], w8[p / PER], p % PER, k);
+        const int x = PP::word(t, r);
+        const uint32_t field = ((1u << BITS) - 1u) * 0x00010001u << (BITS * (PP::cls(t, r) % PP::P));
+        a[r] = (PP::order(r) ? w8[x] : w[x]) & field;
     }
 }
 
@@ -258,40 +233,55 @@ struct Cfg {
 };
 
 // Build this warp's Qt B fragments (fp16 hi + lo parts of q_h * step) and
-// its beta = sum_c q_h[c] * zero_c, from the block's key (step, zero) entries;
-// entries == nullptr means step 1, zero 0 (the fp16 residual).  qh/ql hold the
-// fp16 hi/lo parts of the scaled query per channel pair; with s exact in fp16,
-// hi = rn(qh*s) and lo = rn(ql*s + (qh*s - hi)) (the inner residual is exact),
-// so hi + lo = q*s to about 22 bits.  off[j] is the lane's table offset of
-// channel pair lane + 32j (head 0, hi column).
+// its beta = sum_c q_h[c] * zero_c, from the block's key steps and zeros
+// (D fp16 steps, then D fp16 zeros); entries == nullptr means step 1, zero 0
+// (the fp16 residual).  qh/ql hold the fp16 hi/lo parts of the scaled query
+// per channel pair (for the quantized tiles already multiplied by the
+// channel's code scale 2^-(BITS*pos)); with s exact in fp16, hi = rn(qh*s)
+// and lo = rn(ql*s + (qh*s - hi)), the inner residual exact, so hi + lo =
+// q*s to about 22 bits.  Lane l handles channel pairs CPL*l + j; off[j] is
+// the table offset of pair CPL*l + j (head 0, hi column).  With entries,
+// beta is returned times 2^-24, the unit of the masked codes.
 template <class C, int D, int NQ>
-__device__ __forceinline__ void build_q_frags(const uint32_t* entries, const float (*qf)[D],
+__device__ __forceinline__ void build_q_frags(const uint8_t* entries, const float (*qf)[D],
                                               const uint32_t (*qh)[D / 2], const uint32_t (*ql)[D / 2],
                                               const int (&off)[D / 64], uint32_t* qfrag, int lane,
                                               uint32_t (&qb)[2 * C::KSTEPS], float& beta) {
+    constexpr int CPL = D / 64;               // channel pairs per lane
     constexpr int HEAD = 8 * C::QSTRIDE;      // table distance between heads' hi columns
     constexpr int LOC = 4 * C::QSTRIDE;       // hi column -> lo column
     float bp[NQ];
 #pragma unroll
     for (int h = 0; h < NQ; ++h) bp[h] = 0.f;
     __syncwarp();
+    if (entries) {
+        uint32_t sw[CPL], zw[CPL];             // steps / zeros of channels 2*CPL*l ..
+        if constexpr (CPL == 2) {
+            const uint2 sv = *reinterpret_cast<const uint2*>(entries + 8 * lane);
+            const uint2 zv = *reinterpret_cast<const uint2*>(entries + 2 * D + 8 * lane);
+            sw[0] = sv.x; sw[1] = sv.y; zw[0] = zv.x; zw[1] = zv.y;
+        } else {
+            sw[0] = *reinterpret_cast<const uint32_t*>(entries + 4 * lane);
+            zw[0] = *reinterpret_cast<const uint32_t*>(entries + 2 * D + 4 * lane);
+        }
 #pragma unroll
-    for (int j = 0; j < D / 64; ++j) {
-        const int cp = lane + 32 * j;
-        if (entries) {
-            const uint2 e = *reinterpret_cast<const uint2*>(entries + 2 * cp);
-            const uint32_t s2 = __byte_perm(e.x, e.y, 0x5410);
-            const float2 z = unpack_f16x2(__byte_perm(e.x, e.y, 0x7632));
+        for (int j = 0; j < CPL; ++j) {
+            const int cp = CPL * lane + j;
+            const float2 z = unpack_f16x2(zw[j]);
 #pragma unroll
             for (int h = 0; h < NQ; ++h) {
-                const uint32_t hi = hmul2(qh[h][cp], s2);
-                const uint32_t lo = hfma2(ql[h][cp], s2, hfma2(qh[h][cp], s2, neg_f16x2(hi)));
+                const uint32_t hi = hmul2(qh[h][cp], sw[j]);
+                const uint32_t lo = hfma2(ql[h][cp], sw[j], hfma2(qh[h][cp], sw[j], neg_f16x2(hi)));
                 const float2 q2 = *reinterpret_cast<const float2*>(&qf[h][2 * cp]);
                 bp[h] = fmaf(q2.x, z.x, fmaf(q2.y, z.y, bp[h]));
                 qfrag[off[j] + h * HEAD] = hi;
                 qfrag[off[j] + h * HEAD + LOC] = lo;
             }
-        } else {
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int cp = CPL * lane + j;
 #pragma unroll
             for (int h = 0; h < NQ; ++h) {
                 qfrag[off[j] + h * HEAD] = qh[h][cp];
@@ -306,7 +296,7 @@ __device__ __forceinline__ void build_q_frags(const uint32_t* entries, const flo
         for (int h = 0; h < NQ; ++h) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) bp[h] += __shfl_xor_sync(kFull, bp[h], o);
-            if (i == h) beta = bp[h];
+            if (i == h) beta = bp[h] * 0x1p-24f;
         }
     }
     __syncwarp();
@@ -324,6 +314,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
     __shared__ __align__(16) float qf[NQ][D];
     __shared__ uint32_t qh_s[NQ][D / 2], ql_s[NQ][D / 2];   // fp16 hi / lo of the scaled query
+    __shared__ uint32_t qhc_s[NQ][D / 2], qlc_s[NQ][D / 2]; // the same times the code scale 2^-(BITS*pos)
     __shared__ __align__(16) uint32_t qfrag_all[kWarps][32 * C::QSTRIDE];
     __shared__ float red_m[kWarps][NQ], red_l[kWarps][NQ];
     __shared__ float red_o[kWarps][NQ][D];
@@ -346,10 +337,10 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     if (tid == 0) red_status = 0u;
     __syncthreads();
 
-    int qoff[D / 64];     // this lane's Qt table offsets (channel pairs lane + 32j)
+    int qoff[D / 64];     // this lane's Qt table offsets (channel pairs (D/64)*lane + j)
 #pragma unroll
     for (int j = 0; j < D / 64; ++j) {
-        const int cp = lane + 32 * j, cc = (2 * cp) & 15;
+        const int cp = (D / 64) * lane + j, cc = (2 * cp) & 15;
         qoff[j] = ((cc & 7) >> 1) * C::QSTRIDE + 2 * (cp >> 3) + (cc >> 3);
     }
     const uint32_t ring_u32 = smem_u32(ring), bars_u32 = smem_u32(bars);
@@ -360,21 +351,13 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     const bool col_ok = hP < NQ;
     // this lane's output columns (2i, 2i+1): head hO, group slot jO
     const int hO = i / GB, jO = i % GB;
-    const UnpackConsts ukc = make_unpack_consts<BITS>();
-    const int tokA = 2 * i, tokB = 2 * i + 8;    // this lane's value tokens (and +1)
-    // byte offsets, inside a stage's value entries, of this lane's 4 tokens x NBF groups
-    uint32_t eoff[NBF][4];
-#pragma unroll
-    for (int f = 0; f < NBF; ++f) {
-        const int gr = f * GB + jP;
-        eoff[f][0] = 4u * (tokA * NGRP + gr);
-        eoff[f][1] = 4u * ((tokA + 1) * NGRP + gr);
-        eoff[f][2] = 4u * (tokB * NGRP + gr);
-        eoff[f][3] = 4u * ((tokB + 1) * NGRP + gr);
-    }
+    // byte offset, inside an entry tile, of the steps of this lane's tokens
+    // 2i, 2i+1, 2i+8, 2i+9 (adjacent in the row order) for group fragment 0;
+    // the zeros follow 32*NGRP bytes later, fragment f adds 32*f*GB
+    const uint32_t eoff = 32u * jP + 8u * i;
     const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
 
-    float m, l;
+    float m = -INFINITY, l = 0.f;
     float o[KS][4];
     float zeta[NBF];
     uint32_t qb[2 * KS];
@@ -382,14 +365,14 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     uint32_t status = 0;  // 1: a bulk copy did not complete in time (sticky)
     uint32_t item = 0;    // ring stages this warp has consumed (stage index and phase)
 
-    // Online softmax step over two tiles: sc = logits of tokens g, g+8 of tile
-    // A and of tile B (head i); p receives their probabilities.
-    auto softmax = [&](const float (&sc)[4], float (&p)[4]) {
+    // Online softmax step over two tiles: sc * unit = logits of tokens g, g+8
+    // of tile A and of tile B (head i); p receives their probabilities.
+    auto softmax = [&](const float (&sc)[4], float (&p)[4], float unit) {
         float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
-        const float mn = fmaxf(m, mt);
+        const float mn = fmaxf(m, mt * unit);
         if (__any_sync(kFull, mn > m)) {
             const float alpha = fast_exp2(m - mn);
             l *= alpha;
@@ -402,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             m = mn;
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) p[j] = fast_exp2(sc[j] - m);
+        for (int j = 0; j < 4; ++j) p[j] = fast_exp2(fmaf(sc[j], unit, -m));
         l += (p[0] + p[1]) + (p[2] + p[3]);
     };
     // probabilities of tokens 2i, 2i+1, 2i+8, 2i+9 of head hP from (p0, p1) =
@@ -417,15 +400,15 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     };
     // B fragment of P*step for one value fragment from the 4 tokens' (s, z) entries.
     auto p_frag = [&](const float (&pr)[4], uint32_t ph01, uint32_t ph89, uint32_t pl01, uint32_t pl89,
-                      const uint32_t (&e)[4], uint32_t& b0, uint32_t& b1, float& z) {
-        const uint32_t s01 = __byte_perm(e[0], e[1], 0x5410), s89 = __byte_perm(e[2], e[3], 0x5410);
+                      uint2 sv, uint2 zv, uint32_t& b0, uint32_t& b1, float& z) {
+        const uint32_t s01 = sv.x, s89 = sv.y;
         const uint32_t h01 = hmul2(ph01, s01), h89 = hmul2(ph89, s89);
         const uint32_t l01 = hfma2(pl01, s01, hfma2(ph01, s01, neg_f16x2(h01)));
         const uint32_t l89 = hfma2(pl89, s89, hfma2(ph89, s89, neg_f16x2(h89)));
         b0 = lo_col ? l01 : h01;
         b1 = lo_col ? l89 : h89;
-        const float2 z01 = unpack_f16x2(__byte_perm(e[0], e[1], 0x7632));
-        const float2 z89 = unpack_f16x2(__byte_perm(e[2], e[3], 0x7632));
+        const float2 z01 = unpack_f16x2(zv.x);
+        const float2 z89 = unpack_f16x2(zv.y);
         z = fmaf(pr[0], z01.x, fmaf(pr[1], z01.y, fmaf(pr[2], z89.x, fmaf(pr[3], z89.y, z))));
     };
     auto split_p = [&](const float (&pr)[4], uint32_t& ph01, uint32_t& ph89, uint32_t& pl01, uint32_t& pl89) {
@@ -477,6 +460,13 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             const float2 hf = unpack_f16x2(hi);
             qh_s[j][cp] = hi;
             ql_s[j][cp] = pack_f16x2(x0 - hf.x, x1 - hf.y);
+            // channels 2cp, 2cp+1 have class cp / 4: their codes read as code * 2^(BITS*pos - 24)
+            const float cs = pow2i(-BITS * ((cp >> 2) % (8 / BITS)));
+            const float y0 = x0 * cs, y1 = x1 * cs;
+            const uint32_t hic = pack_f16x2(y0, y1);
+            const float2 hcf = unpack_f16x2(hic);
+            qhc_s[j][cp] = hic;
+            qlc_s[j][cp] = pack_f16x2(y0 - hcf.x, y1 - hcf.y);
         }
         __syncthreads();
 
@@ -521,8 +511,8 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
             const uint32_t stage_u32 = ring_u32 + st * C::STAGE_BYTES;
             const int pr = wb + k;
             if (need_ksz(pr))
-                build_q_frags<C, D, NQ>(reinterpret_cast<const uint32_t*>(stage + 4 * C::TILE + 2 * C::ENT), qf,
-                                        qh_s, ql_s, qoff, qfrag, lane, qb, beta);
+                build_q_frags<C, D, NQ>(stage + 4 * C::TILE + 2 * C::ENT, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb,
+                                        beta);
             // keys: logits of tokens g, g+8 of both tiles for head i
             float sc[4];
             {
@@ -536,8 +526,8 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     uint32_t fa[4], fb[4];
-                    a_frag<BITS, W>(wa, wa8, kk, fa, ukc);
-                    a_frag<BITS, W>(wbw, wb8, kk, fb, ukc);
+                    a_frag<BITS, false, W>(wa, wa8, kk, fa);
+                    a_frag<BITS, false, W>(wbw, wb8, kk, fb);
                     mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
                     mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
                 }
@@ -547,7 +537,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                 sc[3] = cb[2] + cb[3];
             }
             float p[4];
-            softmax(sc, p);
+            softmax(sc, p, 0x1p24f);                   // scores are in units of 2^-24
             // values, tile by tile
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -555,13 +545,12 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                 gather(p[2 * t], p[2 * t + 1], prb);
                 uint32_t ph01, ph89, pl01, pl89;
                 split_p(prb, ph01, ph89, pl01, pl89);
-                const uint32_t ve = stage_u32 + 4 * C::TILE + t * C::ENT;
+                const uint32_t ve = stage_u32 + 4 * C::TILE + t * C::ENT + eoff;
                 uint32_t pb[NBF][2];
 #pragma unroll
                 for (int f = 0; f < NBF; ++f) {
-                    const uint32_t e[4] = {lds32(ve + eoff[f][0]), lds32(ve + eoff[f][1]), lds32(ve + eoff[f][2]),
-                                           lds32(ve + eoff[f][3])};
-                    p_frag(prb, ph01, ph89, pl01, pl89, e, pb[f][0], pb[f][1], zeta[f]);
+                    const uint2 sv = lds64(ve + 32u * GB * f), zv = lds64(ve + 32u * (NGRP + GB * f));
+                    p_frag(prb, ph01, ph89, pl01, pl89, sv, zv, pb[f][0], pb[f][1], zeta[f]);
                 }
                 uint32_t wv[W], wv8[W];
                 lds_words(stage_u32 + (2 + t) * C::TILE, wv);
@@ -570,7 +559,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t af[4];
-                    a_frag<BITS, W>(wv, wv8, mt, af, ukc);
+                    a_frag<BITS, true, W>(wv, wv8, mt, af);
                     const int f = (16 * mt / G) / GB;
                     mma16816(o[mt], af, pb[f][0], pb[f][1]);
                 }
@@ -589,6 +578,15 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                 mbar_wait(&bars[(item + u) % C::STAGES], ((item + u) / C::STAGES) & 1u);
         }
         item += (uint32_t)npairs;
+        // the quantized tiles' value sums are in units of 2^(BITS*pos - 24),
+        // pos = (channel / 8) % (8 / BITS): rows g and g+8 of m-tile mt have
+        // classes 2mt and 2mt+1
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const float u0 = pow2i(24 - BITS * ((2 * mt) % (8 / BITS)));
+            const float u1 = pow2i(24 - BITS * ((2 * mt + 1) % (8 / BITS)));
+            o[mt][0] *= u0; o[mt][1] *= u0; o[mt][2] *= u1; o[mt][3] *= u1;
+        }
         // ---- this warp's residual pairs: 32 fp16 rows each, A operands straight from memory ----
         const int rw = (r1 - r0 + kWarps - 1) / kWarps;
         const int rb = min(r0 + warp * rw, r1), re = min(rb + rw, r1);
@@ -618,7 +616,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
                     sc[2 * t + 1] = okg8 ? c[2] + c[3] : -INFINITY;
                 }
                 float p[4];
-                softmax(sc, p);
+                softmax(sc, p, 1.f);
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     float prb[4];

@@ -16,7 +16,7 @@ constexpr int kQuantThreads = 128;
 // Step and zero of one group from its fp32 min / max (fp16 inputs, exact).
 // A -0 min or max becomes +0; every operation is a separately rounded RN op.
 __device__ __forceinline__ void group_step_zero(float mn, float mx, int L, float* s, float* z,
-                                                __half2* entry) {
+                                                __half* s_out, __half* z_out) {
     mn = __fadd_rn(mn, 0.0f);
     mx = __fadd_rn(mx, 0.0f);
     const float s32 = __fdiv_rn(__fsub_rn(mx, mn), (float)L);
@@ -24,7 +24,8 @@ __device__ __forceinline__ void group_step_zero(float mn, float mx, int L, float
     const __half z16 = __float2half_rn(mn);
     *s = __half2float(s16);
     *z = __half2float(z16);
-    *entry = __halves2half2(s16, z16);   // .x = step (bytes 0-1), .y = zero (bytes 2-3)
+    *s_out = s16;
+    *z_out = z16;
 }
 
 // Nearest level of the stored grid: clamp(rint((x - z) / s), 0, L); 0 when s == 0.
@@ -78,9 +79,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
             mn = fminf(mn, v);
             mx = fmaxf(mx, v);
         }
-        __half2 e;
-        group_step_zero(mn, mx, L, &sf[c], &zf[c], &e);
-        reinterpret_cast<__half2*>(part_k + tiles_bytes)[c] = e;
+        __half* ent = reinterpret_cast<__half*>(part_k + tiles_bytes);   // D steps, then D zeros
+        group_step_zero(mn, mx, L, &sf[c], &zf[c], &ent[c], &ent[D + c]);
     }
     __syncthreads();
     for (int w = tid; w < (G / 16) * TILE_WORDS; w += kQuantThreads) {
@@ -89,12 +89,13 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
         uint32_t word = 0;
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
-            const int p = wl * PER + u, k = p >> 2, r = p & 3;
+            using PP = PairPlace<BITS, false>;
+            const int k = PP::k_of(wl, u), r = PP::r_of(wl, u), bit = PP::bit(k, r);
             const int tok = tt * 16 + g + 8 * (r & 1);
             const int ch = 16 * k + 2 * i + 8 * (r >> 1);
             const uint32_t c0 = nearest_code(__half2float(xs[tok * D + ch]), sf[ch], zf[ch], L);
             const uint32_t c1 = nearest_code(__half2float(xs[tok * D + ch + 1]), sf[ch + 1], zf[ch + 1], L);
-            word |= (c0 << (BITS * u)) | (c1 << (16 + BITS * u));
+            word |= (c0 << bit) | (c1 << (16 + bit));
         }
         reinterpret_cast<uint32_t*>(part_k)[w] = word;
     }
@@ -116,9 +117,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
             mn = fminf(mn, v);
             mx = fmaxf(mx, v);
         }
-        __half2 en;
-        group_step_zero(mn, mx, L, &sf[e], &zf[e], &en);
-        reinterpret_cast<__half2*>(part_v + tiles_bytes)[e] = en;
+        // entry tile of the token's code tile: ngrp rows of 16 steps, then the zeros
+        __half* ent = reinterpret_cast<__half*>(part_v + tiles_bytes + (long long)(t / 16) * 64 * ngrp);
+        const int at = gr * 16 + entry_pos(t % 16);
+        group_step_zero(mn, mx, L, &sf[e], &zf[e], &ent[at], &ent[16 * ngrp + at]);
     }
     __syncthreads();
     for (int w = tid; w < (G / 16) * TILE_WORDS; w += kQuantThreads) {
@@ -127,13 +129,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
         uint32_t word = 0;
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
-            const int p = wl * PER + u, k = p >> 2, r = p & 3;
+            using PP = PairPlace<BITS, true>;
+            const int k = PP::k_of(wl, u), r = PP::r_of(wl, u), bit = PP::bit(k, r);
             const int ch = 16 * k + g + 8 * (r & 1);
             const int tok0 = tt * 16 + 2 * i + 8 * (r >> 1);
             const int e0 = tok0 * ngrp + ch / G, e1 = e0 + ngrp;
             const uint32_t c0 = nearest_code(__half2float(xs[tok0 * D + ch]), sf[e0], zf[e0], L);
             const uint32_t c1 = nearest_code(__half2float(xs[(tok0 + 1) * D + ch]), sf[e1], zf[e1], L);
-            word |= (c0 << (BITS * u)) | (c1 << (16 + BITS * u));
+            word |= (c0 << bit) | (c1 << (16 + bit));
         }
         reinterpret_cast<uint32_t*>(part_v)[w] = word;
     }

@@ -107,25 +107,33 @@ typedef struct {
  *
  * Block n of a slot holds that slot's tokens [n*G, (n+1)*G).  Residual row j
  * holds token Lq + j.
- *   key part  : G/16 code tiles (tokens in order), then D entries (s, z);
- *               entry c is the step and zero of channel c over the block.
- *   value part: G/16 code tiles, then G*(D/G) entries (s, z); entry
- *               t*(D/G) + j is the step and zero of the block's token t over
- *               channels [j*G, (j+1)*G).
- *   An entry (s, z) is two fp16: s at bytes 0-1, z at bytes 2-3.
+ *   key part  : G/16 code tiles (tokens in order), then the D channel steps
+ *               s[c] (fp16), then the D channel zeros z[c] (fp16); s[c], z[c]
+ *               hold for channel c over the block's G tokens.
+ *   value part: G/16 code tiles, then G/16 entry tiles of 64*(D/G) bytes,
+ *               one per code tile: the steps of the tile's 16 tokens as D/G
+ *               rows of 16 fp16 (row j: channels [j*G, (j+1)*G)), then their
+ *               zeros in the same form.  Inside a row, token t (0..15) of the
+ *               tile sits at position 4*((t%8)/2) + 2*(t/8) + t%2, i.e. the
+ *               order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15.
  *
  * Code tile: 16 tokens x D channels of b-bit codes in D*b/2 little-endian
  * 32-bit words.  Lane l (0..31) owns words [l*W, (l+1)*W), W = D*b/64.
- * Write l = 4*g + i.  The lane's D/4 code pairs are numbered p = 0..D/4-1;
- * pair p is in the lane's word p / (16/b), slot u = p % (16/b): its first
- * code at bits [b*u, b*u + b), its second at bits [16 + b*u, 16 + b*u + b).
- * With k = p / 4 and r = p % 4:
+ * Write l = 4*g + i and P = 8/b.  The lane's D/4 code pairs are (k, r),
+ * k = 0..D/16-1, r = 0..3:
  *   key tile  : both codes are token g + 8*(r%2); the first is channel
- *               16k + 2i + 8*(r/2), the second the next channel.
+ *               16k + 2i + 8*(r/2), the second the next channel;
+ *               class c = 2k + r/2, order h = r%2.
  *   value tile: both codes are channel 16k + g + 8*(r%2); the first is token
- *               2i + 8*(r/2), the second the next token.
+ *               2i + 8*(r/2), the second the next token;
+ *               class c = 2k + r%2, order h = r/2.
+ * Pair (k, r) is in the lane's word c/P, in byte h of each 16-bit half, at
+ * bits [b*(c%P), b*(c%P) + b) of that byte: the first code in the low half
+ * (bits 0-15), the second in the high half.
  * (Each lane's words are thereby the fragments of a 16x16 fp16 A operand of
- * an m16n8k16 MMA: keys as [token][channel], values as [channel][token].)
+ * an m16n8k16 MMA: keys as [token][channel], values as [channel][token].
+ * The class of a code is its channel / 8, so a code masked in place reads as
+ * the fp16 value code * 2^(b*((ch/8)%P) - 24), a scale set by the channel.)
  */
 typedef struct {
     size_t total_bytes;       /* == kivi_cache_bytes() */

@@ -8,16 +8,26 @@ the CUDA sources, the layout documented in the library header (include/kivi.h,
 
   * a slot's quantized tokens are in blocks of G tokens; each block has a key
     part and a value part of PART = (G/16)*TILE + 4*D bytes, TILE = 2*D*b;
-  * a part is G/16 code tiles followed by fp16 (s, z) entries;
+  * a key part is G/16 code tiles, then the D channel steps (fp16), then the
+    D channel zeros (fp16);
+  * a value part is G/16 code tiles, then G/16 entry tiles: the steps of a
+    code tile's 16 tokens as D/G rows of 16 fp16 (one row per channel group),
+    then their zeros in the same form; inside a row, token t of the tile sits
+    at position 4*((t % 8) // 2) + 2*(t // 8) + t % 2;
   * a code tile is 16 tokens x D channels in D*b/2 little-endian uint32
-    words; lane l = 4g + i owns W = D*b/64 consecutive words; its pair p
-    lives in word p // (16/b), slot u = p % (16/b), first code at bit b*u,
-    second at bit 16 + b*u; with k = p // 4, r = p % 4:
-      keys  : token g + 8(r%2), channels 16k + 2i + 8(r//2) (+1)
-      values: channel 16k + g + 8(r%2), tokens 2i + 8(r//2) (+1)
+    words; lane l = 4g + i owns W = D*b/64 consecutive words.  Its code pairs
+    are (k, r), k < D/16, r < 4:
+      keys  : token g + 8(r%2), channels 16k + 2i + 8(r//2) (+1);
+              class c = 2k + r//2, order h = r%2
+      values: channel 16k + g + 8(r%2), tokens 2i + 8(r//2) (+1);
+              class c = 2k + r%2, order h = r//2
+    With P = 8/b, the pair lives in lane word c // P, byte h of each 16-bit
+    half, bits b*(c % P) of that byte: the first code in the low half, the
+    second in the high half.
 
 Parity status: pinned (pack/unpack round trip covers every bit exactly once;
-single-code tiles land on the hand-computed word and bit).
+single-code tiles and single entries land on hand-computed words, bits and
+bytes).
 """
 from __future__ import annotations
 
@@ -30,61 +40,75 @@ def sizes(D: int, b: int, G: int):
     return tile, (G // 16) * tile + 4 * D
 
 
-def _maps(D: int, b: int, kind: str):
-    """Index maps over [lane 32][pair D/4]: (tok0, ch0, tok1, ch1, shift)."""
+def _pair_coords(D: int, kind: str):
+    """Coordinates of every code pair, indexed [lane 32][k D/16][r 4].
+
+    Returns (tok0, ch0, tok1, ch1, cls, order): the first and second code's
+    token and channel, the pair's class and order.
+    """
     if kind not in ("key", "value"):
         raise ValueError(kind)
-    l, p = np.meshgrid(np.arange(32), np.arange(D // 4), indexing="ij")
-    g, i = l // 4, l % 4
-    k, r = p // 4, p % 4
-    shift = b * (p % (16 // b))
+    lane, k, r = np.meshgrid(np.arange(32), np.arange(D // 16), np.arange(4), indexing="ij")
+    g, i = lane // 4, lane % 4
     if kind == "key":
         tok0 = g + 8 * (r % 2)
-        tok1 = tok0
         ch0 = 16 * k + 2 * i + 8 * (r // 2)
-        ch1 = ch0 + 1
+        tok1, ch1 = tok0, ch0 + 1
+        cls, order = 2 * k + r // 2, r % 2
     else:
         ch0 = 16 * k + g + 8 * (r % 2)
-        ch1 = ch0
         tok0 = 2 * i + 8 * (r // 2)
-        tok1 = tok0 + 1
-    return tok0, ch0, tok1, ch1, shift
+        tok1, ch1 = tok0 + 1, ch0
+        cls, order = 2 * k + r % 2, r // 2
+    return tok0, ch0, tok1, ch1, cls, order
+
+
+def _placement(D: int, b: int, kind: str):
+    """Per pair: (lane, lane word, bit of the first code) as flat int arrays,
+    plus the pair coordinates flattened alike."""
+    tok0, ch0, tok1, ch1, cls, order = _pair_coords(D, kind)
+    P = 8 // b
+    lane = np.broadcast_to(np.arange(32)[:, None, None], cls.shape)
+    word = cls // P
+    bit = 8 * order + b * (cls % P)
+    flat = lambda a: np.ascontiguousarray(a).reshape(-1)
+    return tuple(map(flat, (lane, word, bit, tok0, ch0, tok1, ch1)))
 
 
 def pack_tiles(codes: np.ndarray, b: int, kind: str) -> np.ndarray:
     """codes uint8 [..., 16, D] -> uint32 [..., D*b/2] (one code tile each)."""
     *lead, T, D = codes.shape
     assert T == 16
-    tok0, ch0, tok1, ch1, shift = _maps(D, b, kind)
-    c0 = codes[..., tok0, ch0].astype(np.uint32)        # [..., 32, D/4]
-    c1 = codes[..., tok1, ch1].astype(np.uint32)
-    contrib = (c0 << shift.astype(np.uint32)) | (c1 << (shift + 16).astype(np.uint32))
-    W, per = D * b // 64, 16 // b
-    contrib = contrib.reshape(*lead, 32, W, per)
-    words = np.bitwise_or.reduce(contrib, axis=-1)     # [..., 32, W]
-    return np.ascontiguousarray(words.reshape(*lead, 32 * W).astype("<u4"))
+    W = D * b // 64
+    lane, word, bit, tok0, ch0, tok1, ch1 = _placement(D, b, kind)
+    c0 = codes[..., tok0, ch0].astype(np.uint64)                 # [..., npairs]
+    c1 = codes[..., tok1, ch1].astype(np.uint64)
+    contrib = (c0 << bit.astype(np.uint64)) | (c1 << (bit + 16).astype(np.uint64))
+    dest = lane * W + word                                       # each word receives 16/b pairs
+    order = np.argsort(dest, kind="stable")
+    per = 16 // b
+    assert np.array_equal(dest[order].reshape(32 * W, per), np.repeat(np.arange(32 * W), per).reshape(-1, per))
+    words = np.bitwise_or.reduce(contrib[..., order].reshape(*lead, 32 * W, per), axis=-1)
+    return np.ascontiguousarray(words.astype("<u4"))
 
 
 def unpack_tiles(words: np.ndarray, D: int, b: int, kind: str) -> np.ndarray:
     """Inverse of pack_tiles: uint32 [..., D*b/2] -> uint8 [..., 16, D]."""
     *lead, n = words.shape
-    W, per = D * b // 64, 16 // b
+    W = D * b // 64
     assert n == 32 * W
-    tok0, ch0, tok1, ch1, shift = _maps(D, b, kind)
-    w = words.astype(np.uint32).reshape(*lead, 32, W, 1)
-    w = np.broadcast_to(w, (*lead, 32, W, per)).reshape(*lead, 32, W * per)   # [..., 32, D/4]
-    mask = np.uint32((1 << b) - 1)
-    v0 = ((w >> shift.astype(np.uint32)) & mask).astype(np.uint8)
-    v1 = ((w >> (shift + 16).astype(np.uint32)) & mask).astype(np.uint8)
+    lane, word, bit, tok0, ch0, tok1, ch1 = _placement(D, b, kind)
+    w = words.astype(np.uint64)[..., lane * W + word]            # [..., npairs]
+    mask = np.uint64((1 << b) - 1)
     out = np.zeros((*lead, 16, D), np.uint8)
-    out[..., tok0, ch0] = v0
-    out[..., tok1, ch1] = v1
+    out[..., tok0, ch0] = ((w >> bit.astype(np.uint64)) & mask).astype(np.uint8)
+    out[..., tok1, ch1] = ((w >> (bit + 16).astype(np.uint64)) & mask).astype(np.uint8)
     return out
 
 
-def _entries(s: np.ndarray, z: np.ndarray) -> np.ndarray:
-    """(s, z) fp16 pairs as bytes, s first."""
-    return np.stack([s, z], axis=-1).astype("<f2").view(np.uint8)
+def entry_position(t: int) -> int:
+    """Position of token t (0..15 of a tile) inside a row of an entry tile."""
+    return 4 * ((t % 8) // 2) + 2 * (t // 8) + t % 2
 
 
 def pack_key_parts(codes: np.ndarray, s: np.ndarray, z: np.ndarray, b: int, G: int) -> np.ndarray:
@@ -96,8 +120,25 @@ def pack_key_parts(codes: np.ndarray, s: np.ndarray, z: np.ndarray, b: int, G: i
     nblk = T // G
     tiles = pack_tiles(codes.reshape(nblk, G // 16, 16, D), b, "key")   # [nblk, G/16, D*b/2]
     tb = tiles.view(np.uint8).reshape(nblk, -1)
-    ent = _entries(s, z).reshape(nblk, -1)
-    return np.concatenate([tb, ent], axis=1)
+    sb = np.ascontiguousarray(s.astype("<f2")).view(np.uint8).reshape(nblk, -1)
+    zb = np.ascontiguousarray(z.astype("<f2")).view(np.uint8).reshape(nblk, -1)
+    return np.concatenate([tb, sb, zb], axis=1)
+
+
+def _entry_tiles(s: np.ndarray, z: np.ndarray, G: int) -> np.ndarray:
+    """Value (s, z) [nblk*G, D/G] -> entry tiles, uint8 [nblk, G/16 * 64*(D/G)]."""
+    T, ngrp = s.shape
+    nblk, ntile = T // G, G // 16
+    perm = np.array([entry_position(t) for t in range(16)])
+    rows_s = np.zeros((nblk, ntile, ngrp, 16), np.float16)
+    rows_z = np.zeros((nblk, ntile, ngrp, 16), np.float16)
+    st = s.reshape(nblk, ntile, 16, ngrp)
+    zt = z.reshape(nblk, ntile, 16, ngrp)
+    for t in range(16):
+        rows_s[:, :, :, perm[t]] = st[:, :, t, :]
+        rows_z[:, :, :, perm[t]] = zt[:, :, t, :]
+    ent = np.concatenate([rows_s.reshape(nblk, ntile, -1), rows_z.reshape(nblk, ntile, -1)], axis=2)
+    return np.ascontiguousarray(ent.astype("<f2")).view(np.uint8).reshape(nblk, -1)
 
 
 def pack_value_parts(codes: np.ndarray, s: np.ndarray, z: np.ndarray, b: int, G: int) -> np.ndarray:
@@ -109,8 +150,7 @@ def pack_value_parts(codes: np.ndarray, s: np.ndarray, z: np.ndarray, b: int, G:
     nblk = T // G
     tiles = pack_tiles(codes.reshape(nblk, G // 16, 16, D), b, "value")
     tb = tiles.view(np.uint8).reshape(nblk, -1)
-    ent = _entries(s, z).reshape(nblk, -1)      # token-major, group-minor
-    return np.concatenate([tb, ent], axis=1)
+    return np.concatenate([tb, _entry_tiles(s, z, G)], axis=1)
 
 
 def unpack_key_parts(parts: np.ndarray, D: int, b: int, G: int):
@@ -120,16 +160,21 @@ def unpack_key_parts(parts: np.ndarray, D: int, b: int, G: int):
     nt = G // 16
     words = np.ascontiguousarray(parts[:, : nt * tile]).view("<u4").reshape(nblk, nt, -1)
     codes = unpack_tiles(words, D, b, "key").reshape(nblk * G, D)
-    ent = np.ascontiguousarray(parts[:, nt * tile:]).view("<f2").reshape(nblk, D, 2)
-    return codes, ent[..., 0], ent[..., 1]
+    ent = np.ascontiguousarray(parts[:, nt * tile:]).view("<f2").reshape(nblk, 2, D)
+    return codes, ent[:, 0], ent[:, 1]
 
 
 def unpack_value_parts(parts: np.ndarray, D: int, b: int, G: int):
     """uint8 [nblk, PART] -> (codes [nblk*G, D], s [nblk*G, D/G], z [nblk*G, D/G])."""
     nblk = parts.shape[0]
     tile, _ = sizes(D, b, G)
-    nt = G // 16
+    nt, ngrp = G // 16, D // G
     words = np.ascontiguousarray(parts[:, : nt * tile]).view("<u4").reshape(nblk, nt, -1)
     codes = unpack_tiles(words, D, b, "value").reshape(nblk * G, D)
-    ent = np.ascontiguousarray(parts[:, nt * tile:]).view("<f2").reshape(nblk * G, D // G, 2)
-    return codes, ent[..., 0], ent[..., 1]
+    ent = np.ascontiguousarray(parts[:, nt * tile:]).view("<f2").reshape(nblk, nt, 2, ngrp, 16)
+    perm = np.array([entry_position(t) for t in range(16)])
+    s = ent[:, :, 0][..., perm]                                  # [nblk, nt, ngrp, 16 tokens]
+    z = ent[:, :, 1][..., perm]
+    s = np.moveaxis(s, -1, -2).reshape(nblk * G, ngrp)
+    z = np.moveaxis(z, -1, -2).reshape(nblk * G, ngrp)
+    return codes, s, z

@@ -50,17 +50,40 @@ def test_part_sizes_and_part_round_trip():
     assert parts.shape == (nblk, 1536)
     c2, s2, z2 = layout.unpack_key_parts(parts, D, b, G)
     assert np.array_equal(c2, kc) and s2.tobytes() == ks.tobytes() and z2.tobytes() == kz.tobytes()
-    # entry c = (s, z) of channel c at byte offset tiles + 4c, s first
-    assert parts[1, 1024 + 4 * 9: 1024 + 4 * 9 + 2].tobytes() == ks[1, 9].tobytes()
-    assert parts[1, 1024 + 4 * 9 + 2: 1024 + 4 * 9 + 4].tobytes() == kz[1, 9].tobytes()
+    # steps of the D channels after the tiles, then their zeros
+    assert parts[1, 1024 + 2 * 9: 1024 + 2 * 9 + 2].tobytes() == ks[1, 9].tobytes()
+    assert parts[1, 1024 + 256 + 2 * 9: 1024 + 256 + 2 * 9 + 2].tobytes() == kz[1, 9].tobytes()
     vs = rng.standard_normal((nblk * G, D // G)).astype(np.float16)
     vz = rng.standard_normal((nblk * G, D // G)).astype(np.float16)
     vparts = layout.pack_value_parts(kc, vs, vz, b, G)
     c3, s3, z3 = layout.unpack_value_parts(vparts, D, b, G)
     assert np.array_equal(c3, kc) and s3.tobytes() == vs.tobytes() and z3.tobytes() == vz.tobytes()
-    # entry t*(D/G)+j of block 2: token 5, group 3
-    off = 1024 + 4 * (5 * 4 + 3)
+    # block 2, token 5 (tile 0, row position 9), group 3
+    off = 1024 + 2 * (3 * 16 + 9)
     assert vparts[2, off:off + 2].tobytes() == vs[2 * G + 5, 3].tobytes()
+    assert vparts[2, off + 128:off + 130].tobytes() == vz[2 * G + 5, 3].tobytes()
+
+
+def test_entry_positions(golden):
+    """Single entries land on the hand-worked byte offsets."""
+    assert [layout.entry_position(t) for t in range(16)] == [0, 1, 4, 5, 8, 9, 12, 13, 2, 3, 6, 7, 10, 11, 14, 15]
+    for line in golden("layout_entries.txt"):
+        kind, D, b, G, idx, grp, sb, zb = line.split()
+        D, b, G, idx, sb, zb = map(int, (D, b, G, idx, sb, zb))
+        s_mark, z_mark = np.float16(1.5), np.float16(-2.25)
+        codes = np.zeros((G, D), np.uint8)
+        if kind == "key":
+            s = np.zeros((1, D), np.float16); z = np.zeros((1, D), np.float16)
+            s[0, idx], z[0, idx] = s_mark, z_mark
+            part = layout.pack_key_parts(codes, s, z, b, G)[0]
+        else:
+            s = np.zeros((G, D // G), np.float16); z = np.zeros((G, D // G), np.float16)
+            s[idx, int(grp)], z[idx, int(grp)] = s_mark, z_mark
+            part = layout.pack_value_parts(codes, s, z, b, G)[0]
+        nz = np.flatnonzero(part)
+        assert part[sb:sb + 2].tobytes() == s_mark.tobytes(), line
+        assert part[zb:zb + 2].tobytes() == z_mark.tobytes(), line
+        assert set(nz) <= {sb, sb + 1, zb, zb + 1}, line
 
 
 def test_accounting(golden):
