@@ -178,6 +178,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
     return false;
 }
+// programmatic dependent launch: wait for the preceding kernel's completion
+// and memory; let the next kernel in the stream start launching
+__device__ __forceinline__ void griddepcontrol_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddepcontrol_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }   // 2^e, |e| < 127
 __device__ __forceinline__ float fast_exp2(float x) {   // hardware 2^x (ex2.approx, rel. err ~2^-22)
     float y;
@@ -308,8 +314,15 @@ __device__ __forceinline__ void build_q_frags(const uint8_t* entries, const floa
     }
 }
 
+// Register budget: four CTAs per SM (128 registers a thread); at head_dim 128
+// with four query heads per kv head three, which leaves enough registers.
+template <int D, int NQ>
+struct MinCtas {
+    static constexpr int value = (D == 128 && NQ == 4) ? 3 : 4;
+};
+
 template <int D, int BITS, int NQ, int G>
-__global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
+__global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_kernel(Args a) {
     using C = Cfg<D, BITS, NQ, G>;
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
     __shared__ __align__(16) float qf[NQ][D];
@@ -438,6 +451,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
     const long long cta = blockIdx.x, NU = wm.P + wm.PR;
     long long pos = map_begin(wm, cta);
     const long long pe = map_begin(wm, cta + 1);
+    bool first_seg = true;
     while (pos < pe) {
         const long long slot = pos / wm.Ws;
         const long long u0 = first_unit_at(wm, pos - slot * wm.Ws);
@@ -449,6 +463,41 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
         const int part = (int)(cta - slot_first_cta(wm, slot));
         const int b = (int)(slot / a.Hkv), hk = (int)(slot % a.Hkv);
         const uint8_t* slot_base = a.cache + slot * a.slot_bytes;
+        // ---- this warp's contiguous run of pairs, two tiles per ring stage ----
+        const int pw = (p1 - p0 + kWarps - 1) / kWarps;
+        const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
+        const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
+        auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
+        // lane 0's copy cursor: key part of the block of the next pair to fetch, tile in block
+        const uint8_t* kcur = slot_base + (long long)((2 * wb) / C::TPB) * a.part_bytes;
+        int tcur = (2 * wb) % C::TPB;
+        bool first = true;
+        auto issue_next = [&](uint32_t it) {          // lane 0: next pair -> ring stage of item it
+            const uint32_t st = it % C::STAGES;
+            const uint32_t dst = ring_u32 + st * C::STAGE_BYTES, bar = bars_u32 + 8 * st;
+            const bool kz = first || tcur == 0;
+            const uint8_t* vcur = kcur + vdelta;
+            mbar_expect_tx_u32(bar, 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
+            tma_1d_u32(dst, kcur + tcur * C::TILE, 2 * C::TILE, bar);
+            tma_1d_u32(dst + 2 * C::TILE, vcur + tcur * C::TILE, 2 * C::TILE, bar);
+            tma_1d_u32(dst + 4 * C::TILE, vcur + tiles_bytes + tcur * C::ENT, 2 * C::ENT, bar);
+            if (kz) tma_1d_u32(dst + 4 * C::TILE + 2 * C::ENT, kcur + tiles_bytes, C::KSZ, bar);
+            first = false;
+            tcur += 2;
+            if (tcur == C::TPB) { tcur = 0; kcur += a.part_bytes; }
+        };
+        if (lane == 0) {
+            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
+        }
+        if (first_seg) {
+            // launched as a programmatic dependent: the copies above read only
+            // quantized blocks, which the preceding kernel never writes (the
+            // library's last kernel on a cache copies residual rows); the query,
+            // the residual rows and the workspace are touched only after this
+            griddepcontrol_wait();
+            griddepcontrol_launch_dependents();       // the merge kernel may start launching
+            first_seg = false;
+        }
         for (int idx = tid; idx < NQ * D / 2; idx += kThreads) {
             const int j = idx / (D / 2), cp = idx % (D / 2);
             const float2 qv = __half22float2(
@@ -476,32 +525,6 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(Args a) {
 #pragma unroll
         for (int f = 0; f < NBF; ++f) zeta[f] = 0.f;
 
-        // ---- this warp's contiguous run of pairs, two tiles per ring stage ----
-        const int pw = (p1 - p0 + kWarps - 1) / kWarps;
-        const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
-        const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
-        auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
-        // lane 0's copy cursor: key part of the block of the next pair to fetch, tile in block
-        const uint8_t* kcur = slot_base + (long long)((2 * wb) / C::TPB) * a.part_bytes;
-        int tcur = (2 * wb) % C::TPB;
-        bool first = true;
-        auto issue_next = [&](uint32_t it) {          // lane 0: next pair -> ring stage of item it
-            const uint32_t st = it % C::STAGES;
-            const uint32_t dst = ring_u32 + st * C::STAGE_BYTES, bar = bars_u32 + 8 * st;
-            const bool kz = first || tcur == 0;
-            const uint8_t* vcur = kcur + vdelta;
-            mbar_expect_tx_u32(bar, 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
-            tma_1d_u32(dst, kcur + tcur * C::TILE, 2 * C::TILE, bar);
-            tma_1d_u32(dst + 2 * C::TILE, vcur + tcur * C::TILE, 2 * C::TILE, bar);
-            tma_1d_u32(dst + 4 * C::TILE, vcur + tiles_bytes + tcur * C::ENT, 2 * C::ENT, bar);
-            if (kz) tma_1d_u32(dst + 4 * C::TILE + 2 * C::ENT, kcur + tiles_bytes, C::KSZ, bar);
-            first = false;
-            tcur += 2;
-            if (tcur == C::TPB) { tcur = 0; kcur += a.part_bytes; }
-        };
-        if (lane == 0) {
-            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
-        }
         int k = 0;
         for (; k < npairs; ++k) {
             const uint32_t it = item + k;
@@ -699,7 +722,8 @@ template <int D>
 __global__ void __launch_bounds__(D) finish_kernel(FinishArgs a) {
     // launched as a programmatic dependent of the main kernel: wait until its
     // partial results are complete and visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    griddepcontrol_wait();
+    griddepcontrol_launch_dependents();   // the next decode call may start its prologue
     const int c = threadIdx.x;
     const long long bh = blockIdx.x;
     const long long slot = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.nq;

@@ -27,8 +27,19 @@ cudaError_t launch_one(mma_detail::Args& a, int num_sms, cudaStream_t st) {
     if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot
     if (n < 1) n = 1;
     a.wm.n = n;
-    decode_mma_kernel<64, BB, NN, GG><<<(unsigned)n, kThreads, C::DYN_SMEM, st>>>(a);
-    return cudaGetLastError();
+    // a programmatic dependent of the preceding kernel: the kernel's prologue
+    // and first cache copies overlap that kernel's tail
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3((unsigned)n);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = C::DYN_SMEM;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, decode_mma_kernel<64, BB, NN, GG>, a);
 }
 }  // namespace
 

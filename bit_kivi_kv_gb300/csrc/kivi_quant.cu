@@ -148,6 +148,9 @@ __global__ void __launch_bounds__(128) copy_rows_kernel(uint8_t* cache, const __
                                                         long long k_off, long long v_off,
                                                         long long resid_slot_bytes, int D, int row0,
                                                         int nrows) {
+    // a following decode launched as a programmatic dependent may start its
+    // prologue now; it waits for this kernel before it reads residual rows
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long slot = blockIdx.x;
     const int n_vec = nrows * D / 8;
     const uint4* sk = reinterpret_cast<const uint4*>(src_k + slot * src_slot_elems);
