@@ -368,8 +368,9 @@ def run_ours(args, w):
                         "steps_per_s": 1e3 / dec_ms},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": f"decode attention call ({args.decode_kernel}: "
-                     "split-KV kernel + log-sum-exp combine)"},
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "decode attention call: " + (
+                         "decode_split_kernel + combine_kernel" if args.decode_kernel == "cuda-core"
+                         else "decode_mma_kernel + finish_kernel (tensor cores)")},
         "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -398,7 +399,8 @@ def _launches_in(step, K, stream, torch):
 def _decode_source_sha1():
     import hashlib
     h = hashlib.sha1()
-    for f in ("kivi_decode.cu", "kivi_common.cuh"):
+    for f in ("kivi_decode.cu", "kivi_common.cuh", "kivi_decode_mma.cuh", "kivi_decode_mma_d128.cu",
+              "kivi_decode_mma_d64.cu"):
         with open(os.path.join(ROOT, "bit_kivi_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
