@@ -283,8 +283,11 @@ def run_ours(args, w):
         for s in range(S):
             for li in range(NL):
                 q, k, v = steps[li][s]
-                caches[li].append(k, v)
-                caches[li].decode_attn(q, out=outs[li])
+                if args.separate_append:
+                    caches[li].append(k, v)
+                    caches[li].decode_attn(q, out=outs[li])
+                else:
+                    caches[li].append_decode(k, v, q, out=outs[li])
 
     def decode_only():
         for li in range(NL):
@@ -361,6 +364,7 @@ def run_ours(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; key outlier channels, attention sink)",
         "config": dict(_config(w, args.workload), parallelism=f"replicas x{world}",
+                       step_calls="kivi_append + kivi_decode_attn" if args.separate_append else "kivi_append_decode",
                        l2="inputs larger than L2: each step rotates layer caches "
                           f"({NL} x ~{bytes_call / 1e6:.0f} MB read per decode round)"),
         "decode_call": {"us": dec_ms * 1e3, "bytes": bytes_call, "gbs": achieved,
@@ -472,8 +476,11 @@ def _e2e(args, w, caches, prompts, steps, torch, dev):
                 q, k, v = d_qkv[li]
                 hq, hk, hv = h_steps[li][s]
                 q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
-                caches[li].append(k, v)
-                caches[li].decode_attn(q, out=d_out[li])
+                if args.separate_append:
+                    caches[li].append(k, v)
+                    caches[li].decode_attn(q, out=d_out[li])
+                else:
+                    caches[li].append_decode(k, v, q, out=d_out[li])
                 h_out[li].copy_(d_out[li], non_blocking=True)
 
     n = max(3, min(args.steps, 10))
@@ -499,6 +506,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true", help="small eager run for ncu captures")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="decode steps as kivi_append + kivi_decode_attn instead of kivi_append_decode")
     ap.add_argument("--decode-kernel", choices=["auto", "cuda-core", "tensor-core"], default="auto")
     ap.add_argument("--profile-calls", type=int, default=4)
     args = ap.parse_args()

@@ -215,17 +215,26 @@ size_t kivi_decode_workspace_bytes(const kivi_config* cfg) {
     return (size_t)g.B * g.Hq * kivi::kPartialSlots * kivi::partial_stride(g.D) * sizeof(float);
 }
 
-kivi_status kivi_decode_attn(kivi_cache_t c, const void* q, void* out, float softmax_scale,
-                             void* workspace, size_t ws_bytes, kivi_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks of a decode call that do not depend on the cache's token counts.
+kivi_status decode_checks(kivi_cache_t c, const void* q, void* out, float softmax_scale, void* workspace,
+                          size_t ws_bytes) {
     if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
     if (!q || !out || !workspace) return fail(KIVI_ERR_INVALID_ARG, "null q, out or workspace");
     if (!aligned(q, 16) || !aligned(out, 16)) return fail(KIVI_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
     if (!aligned(workspace, 256)) return fail(KIVI_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     if (!(softmax_scale == softmax_scale) || isinf(softmax_scale)) return fail(KIVI_ERR_INVALID_ARG, "softmax_scale must be finite");
     const kivi::Geometry& g = c->geo;
-    if (c->n_quant + c->n_resid == 0) return fail(KIVI_ERR_STATE, "decode on an empty cache");
     const size_t need = (size_t)g.B * g.Hq * kivi::kPartialSlots * kivi::partial_stride(g.D) * sizeof(float);
     if (ws_bytes < need) return fail(KIVI_ERR_CAPACITY, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return KIVI_OK;
+}
+
+// The device and its SM count, queried once per handle.
+kivi_status ensure_device(kivi_cache_t c) {
     if (c->device < 0) {
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
@@ -234,16 +243,79 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void* q, void* out, float sof
         c->device = dev;
         c->num_sms = sms;
     }
+    return KIVI_OK;
+}
+
+// Launch a decode call over n_resid residual rows (fa.row < n_resid: a fused append's row).
+kivi_status decode_launch(kivi_cache_t c, const void* q, void* out, float softmax_scale, void* workspace,
+                          long long n_resid, int variant, kivi_stream_t stream, const kivi::FusedAppend& fa) {
+    const kivi::Geometry& g = c->geo;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)g.D);
     const float scale_log2 = scale * 1.4426950408889634f;
-    const kivi::DecodePlan plan = kivi::plan_decode(g, c->n_quant, c->n_resid, c->num_sms);
+    const kivi::DecodePlan plan = kivi::plan_decode(g, c->n_quant, n_resid, c->num_sms);
     int launches = 0;
-    const int variant = c->decode_kernel == KIVI_DECODE_AUTO ? KIVI_DECODE_TENSOR_CORE : c->decode_kernel;
-    const cudaError_t e = kivi::launch_decode(g, c->buf, c->n_quant, c->n_resid, static_cast<const __half*>(q),
+    const cudaError_t e = kivi::launch_decode(g, c->buf, c->n_quant, n_resid, static_cast<const __half*>(q),
                                               static_cast<__half*>(out), scale_log2, static_cast<float*>(workspace),
-                                              plan, variant, reinterpret_cast<cudaStream_t>(stream), &launches);
+                                              plan, variant, reinterpret_cast<cudaStream_t>(stream), &launches, fa);
     g_launches += (unsigned long long)launches;
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+kivi_status kivi_decode_attn(kivi_cache_t c, const void* q, void* out, float softmax_scale,
+                             void* workspace, size_t ws_bytes, kivi_stream_t stream) {
+    const kivi_status st = decode_checks(c, q, out, softmax_scale, workspace, ws_bytes);
+    if (st != KIVI_OK) return st;
+    if (c->n_quant + c->n_resid == 0) return fail(KIVI_ERR_STATE, "decode on an empty cache");
+    const kivi_status sdev = ensure_device(c);
+    if (sdev != KIVI_OK) return sdev;
+    const int variant = c->decode_kernel == KIVI_DECODE_AUTO ? KIVI_DECODE_TENSOR_CORE : c->decode_kernel;
+    return decode_launch(c, q, out, softmax_scale, workspace, c->n_resid, variant, stream, kivi::FusedAppend{});
+}
+
+kivi_status kivi_append_decode(kivi_cache_t c, const void* k, const void* v, const void* q, void* out,
+                               float softmax_scale, void* workspace, size_t ws_bytes, kivi_stream_t stream) {
+    const kivi_status st = decode_checks(c, q, out, softmax_scale, workspace, ws_bytes);
+    if (st != KIVI_OK) return st;
+    if (!k || !v) return fail(KIVI_ERR_INVALID_ARG, "null k or v");
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(KIVI_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    const kivi::Geometry& g = c->geo;
+    if (c->n_quant + c->n_resid + 1 > g.max_tokens)
+        return fail(KIVI_ERR_CAPACITY, "cache already holds max_tokens (%lld) tokens", g.max_tokens);
+    const int variant = c->decode_kernel == KIVI_DECODE_AUTO ? KIVI_DECODE_TENSOR_CORE : c->decode_kernel;
+    if (variant != KIVI_DECODE_TENSOR_CORE) {
+        // the CUDA-core kernel has no fused form: append, then decode
+        const kivi_status sa = kivi_append(c, k, v, stream);
+        if (sa != KIVI_OK) return sa;
+        return kivi_decode_attn(c, q, out, softmax_scale, workspace, ws_bytes, stream);
+    }
+    const kivi_status sdev = ensure_device(c);
+    if (sdev != KIVI_OK) return sdev;
+    cudaStream_t sp = reinterpret_cast<cudaStream_t>(stream);
+    bool flushed = false;
+    if (c->n_resid == g.R) {
+        const __half* rk = reinterpret_cast<const __half*>(c->buf + g.k_resid_off);
+        const __half* rv = reinterpret_cast<const __half*>(c->buf + g.v_resid_off);
+        const cudaError_t e = kivi::launch_quantize_blocks(g, c->buf, rk, rv, (long long)g.R * g.D,
+                                                           c->n_quant / g.G, g.R / g.G, sp);
+        if (e != cudaSuccess) return cuda_fail(e, "residual flush launch");
+        g_launches++;
+        c->n_quant += g.R;
+        c->n_resid = 0;
+        flushed = true;
+    }
+    kivi::FusedAppend fa;
+    fa.k = static_cast<const __half*>(k);
+    fa.v = static_cast<const __half*>(v);
+    fa.row = (int)c->n_resid;
+    fa.early_ok = flushed ? 0 : 1;   // the flush writes blocks right before the decode
+    const kivi_status sd = decode_launch(c, q, out, softmax_scale, workspace, c->n_resid + 1, variant, stream, fa);
+    if (sd != KIVI_OK) return sd;
+    c->n_resid += 1;
     return ok();
 }
 

@@ -112,11 +112,23 @@ struct DecodePlan {
 
 DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, int num_sms);
 
+// An append fused into a decode call (tensor-core kernel only): residual row
+// `row` of every slot is the token k / v ([B*Hkv][D] fp16); the decode kernel
+// reads it from there and stores it in the cache.  row < 0: none.  early_ok: the
+// kernel preceding the decode on the stream writes no quantized block.
+struct FusedAppend {
+    const __half* k = nullptr;
+    const __half* v = nullptr;
+    int row = -1;
+    int early_ok = 1;
+};
+
 // variant: KIVI_DECODE_CUDA_CORE or KIVI_DECODE_TENSOR_CORE (resolved, never AUTO).
+// n_resid counts the fused append's row, if any.
 cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_quant,
                           long long n_resid, const __half* q, __half* out, float scale_log2,
                           float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
-                          int* launches);
+                          int* launches, const FusedAppend& fa = FusedAppend{});
 
 // Host-side helpers of the C ABI (kivi_api.cu): set the calling thread's
 // error string and return st; the decode workspace bytes a handle needs.

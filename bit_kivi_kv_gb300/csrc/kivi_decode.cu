@@ -337,13 +337,16 @@ DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, 
 // Launch the tensor-core kernel on a persistent grid; fills a.wm.n.
 cudaError_t launch_decode_mma_d128(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_mma_d64(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_mma_d128f(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_mma_d64f(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 
 
 
 cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_quant,
                           long long n_resid, const __half* q, __half* out, float scale_log2,
                           float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
-                          int* launches) {
+                          int* launches, const FusedAppend& fa) {
+    if (fa.row >= 0 && variant != KIVI_DECODE_TENSOR_CORE) return cudaErrorInvalidValue;   // fused: tensor cores only
     if (variant == KIVI_DECODE_TENSOR_CORE) {
         const int nq = g.Hq / g.Hkv;
         const long long slots = (long long)g.B * g.Hkv;
@@ -355,9 +358,13 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         wm.Ws = wm.P * wm.wq + wm.PR * wm.wr;
         wm.Wt = slots * wm.Ws;
         mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
-                           g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2};
-        cudaError_t e = g.D == 128 ? launch_decode_mma_d128(m, g.bits, nq, g.G, plan.num_sms, st)
-                                   : launch_decode_mma_d64(m, g.bits, nq, g.G, plan.num_sms, st);
+                           g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2,
+                           fa.k, fa.v, fa.row, fa.early_ok};
+        const bool fused = fa.row >= 0;
+        cudaError_t e = g.D == 128 ? (fused ? launch_decode_mma_d128f : launch_decode_mma_d128)(m, g.bits, nq, g.G,
+                                                                                             plan.num_sms, st)
+                                   : (fused ? launch_decode_mma_d64f : launch_decode_mma_d64)(m, g.bits, nq, g.G,
+                                                                                           plan.num_sms, st);
         if (e != cudaSuccess) return e;
         mma_detail::FinishArgs f{workspace, out, g.Hq, g.Hkv, nq, m.wm};
         // the merge may start while the main kernel drains; it waits for it on the GPU

@@ -50,6 +50,15 @@ struct Args {
     int R, Hq, Hkv, n_resid;
     WorkMap wm;
     float scale_log2;
+    // append fused into the call: residual row new_row (< n_resid) of every
+    // slot is the token new_k / new_v [slot][D]; the kernel reads it from there
+    // and writes it into the cache.  new_row < 0: no fused append.
+    const __half* new_k;
+    const __half* new_v;
+    int new_row;
+    // 1: the preceding kernel writes no quantized block, so the first bulk
+    // copies may go out before waiting for it
+    int early_ok;
 };
 
 struct FinishArgs {
@@ -321,7 +330,10 @@ struct MinCtas {
     static constexpr int value = (D == 128 && NQ == 4) ? 3 : 4;
 };
 
-template <int D, int BITS, int NQ, int G>
+// FUSED: the call appends a token (Args::new_row) the kernel reads from its
+// inputs and stores in the cache; a separate instance so that plain decode
+// calls carry none of that code.
+template <int D, int BITS, int NQ, int G, bool FUSED>
 __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_kernel(Args a) {
     using C = Cfg<D, BITS, NQ, G>;
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
@@ -486,17 +498,34 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
             tcur += 2;
             if (tcur == C::TPB) { tcur = 0; kcur += a.part_bytes; }
         };
+        if (first_seg && !a.early_ok) griddepcontrol_wait();   // the preceding kernel wrote blocks
         if (lane == 0) {
             for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
         }
         if (first_seg) {
-            // launched as a programmatic dependent: the copies above read only
-            // quantized blocks, which the preceding kernel never writes (the
-            // library's last kernel on a cache copies residual rows); the query,
-            // the residual rows and the workspace are touched only after this
+            // launched as a programmatic dependent: with early_ok the copies above
+            // read only quantized blocks, which the preceding kernel never writes
+            // (the library's last kernel on a cache copies residual rows, or is
+            // a decode); the query, the residual rows and the workspace are
+            // touched only after this
             griddepcontrol_wait();
             griddepcontrol_launch_dependents();       // the merge kernel may start launching
             first_seg = false;
+            if (FUSED && a.new_row >= 0) {
+                // the fused append: store every slot's new row in the cache, 16
+                // bytes a thread over the grid (this call reads that row from the
+                // inputs, never from the cache)
+                constexpr int CPR = D * 2 / 16;       // 16-byte chunks per row
+                const long long nslots = (long long)(wm.Wt / wm.Ws);
+                for (long long idx = cta * kThreads + tid; idx < nslots * 2 * CPR;
+                     idx += (long long)gridDim.x * kThreads) {
+                    const long long sl = idx / (2 * CPR);
+                    const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
+                    const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
+                    uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
+                    reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + (sl * a.R + a.new_row) * D)[c16] = *src;
+                }
+            }
         }
         for (int idx = tid; idx < NQ * D / 2; idx += kThreads) {
             const int j = idx / (D / 2), cp = idx % (D / 2);
@@ -617,6 +646,13 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
             const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + slot * a.R * D;
             const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + slot * a.R * D;
             const int n = a.n_resid;
+            // row rr of the residual: the fused append's token comes from its input
+            auto krow = [&](int rr) {
+                return FUSED && rr == a.new_row ? a.new_k + slot * D : kr + (long long)rr * D;
+            };
+            auto vrow = [&](int rr) {
+                return FUSED && rr == a.new_row ? a.new_v + slot * D : vr + (long long)rr * D;
+            };
             build_q_frags<C, D, NQ>(nullptr, qf, qh_s, ql_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
             for (int rp = rb; rp < re; ++rp) {
                 float sc[4];
@@ -624,15 +660,17 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
                 for (int t = 0; t < 2; ++t) {
                     const int r0w = 32 * rp + 16 * t;
                     const bool okg = r0w + g < n, okg8 = r0w + g + 8 < n;
+                    const __half* kg = FUSED ? krow(r0w + g) : kr + (long long)(r0w + g) * D;
+                    const __half* kg8 = FUSED ? krow(r0w + g + 8) : kr + (long long)(r0w + g + 8) * D;
                     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int kk = 0; kk < KS; ++kk) {
                         const int ch = 16 * kk + 2 * i;
                         uint32_t af[4];
-                        af[0] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g) * D + ch) : 0u;
-                        af[1] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g + 8) * D + ch) : 0u;
-                        af[2] = okg ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g) * D + ch + 8) : 0u;
-                        af[3] = okg8 ? *reinterpret_cast<const uint32_t*>(kr + (long long)(r0w + g + 8) * D + ch + 8) : 0u;
+                        af[0] = okg ? *reinterpret_cast<const uint32_t*>(kg + ch) : 0u;
+                        af[1] = okg8 ? *reinterpret_cast<const uint32_t*>(kg8 + ch) : 0u;
+                        af[2] = okg ? *reinterpret_cast<const uint32_t*>(kg + ch + 8) : 0u;
+                        af[3] = okg8 ? *reinterpret_cast<const uint32_t*>(kg8 + ch + 8) : 0u;
                         mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
                     }
                     sc[2 * t] = okg ? c[0] + c[1] : -INFINITY;
@@ -648,18 +686,39 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
                     split_p(prb, ph01, ph89, pl01, pl89);
                     const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
                     const int tA = 32 * rp + 16 * t + 2 * i, tB = tA + 8;
-                    auto ld = [&](int tt, int ch) -> uint32_t {
-                        return tt < n ? (uint32_t)__half_as_ushort(vr[(long long)tt * D + ch]) : 0u;
-                    };
+                    if constexpr (FUSED) {
+                        const __half* vA0 = vrow(tA);
+                        const __half* vA1 = vrow(tA + 1);
+                        const __half* vB0 = vrow(tB);
+                        const __half* vB1 = vrow(tB + 1);
+                        const bool okA0 = tA < n, okA1 = tA + 1 < n, okB0 = tB < n, okB1 = tB + 1 < n;
+                        auto ld = [&](bool ok, const __half* row, int ch) -> uint32_t {
+                            return ok ? (uint32_t)__half_as_ushort(row[ch]) : 0u;
+                        };
 #pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        const int c0 = 16 * mt + g;
-                        uint32_t af[4];
-                        af[0] = ld(tA, c0) | (ld(tA + 1, c0) << 16);
-                        af[1] = ld(tA, c0 + 8) | (ld(tA + 1, c0 + 8) << 16);
-                        af[2] = ld(tB, c0) | (ld(tB + 1, c0) << 16);
-                        af[3] = ld(tB, c0 + 8) | (ld(tB + 1, c0 + 8) << 16);
-                        mma16816(o[mt], af, pb0, pb1);
+                        for (int mt = 0; mt < KS; ++mt) {
+                            const int c0 = 16 * mt + g;
+                            uint32_t af[4];
+                            af[0] = ld(okA0, vA0, c0) | (ld(okA1, vA1, c0) << 16);
+                            af[1] = ld(okA0, vA0, c0 + 8) | (ld(okA1, vA1, c0 + 8) << 16);
+                            af[2] = ld(okB0, vB0, c0) | (ld(okB1, vB1, c0) << 16);
+                            af[3] = ld(okB0, vB0, c0 + 8) | (ld(okB1, vB1, c0 + 8) << 16);
+                            mma16816(o[mt], af, pb0, pb1);
+                        }
+                    } else {
+                        auto ld = [&](int tt, int ch) -> uint32_t {
+                            return tt < n ? (uint32_t)__half_as_ushort(vr[(long long)tt * D + ch]) : 0u;
+                        };
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            const int c0 = 16 * mt + g;
+                            uint32_t af[4];
+                            af[0] = ld(tA, c0) | (ld(tA + 1, c0) << 16);
+                            af[1] = ld(tA, c0 + 8) | (ld(tA + 1, c0 + 8) << 16);
+                            af[2] = ld(tB, c0) | (ld(tB + 1, c0) << 16);
+                            af[3] = ld(tB, c0 + 8) | (ld(tB + 1, c0 + 8) << 16);
+                            mma16816(o[mt], af, pb0, pb1);
+                        }
                     }
                 }
             }

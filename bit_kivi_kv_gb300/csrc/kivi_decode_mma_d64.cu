@@ -1,57 +1,10 @@
-// Instantiations of the tensor-core decode kernel for head_dim 64.
-#include "kivi_decode_mma.cuh"
+// Instantiations of the tensor-core decode kernel: head_dim 64, plain decode calls.
+#include "kivi_decode_mma_launch.cuh"
 
 namespace kivi {
 
-namespace {
-template <int BB, int NN, int GG>
-cudaError_t launch_one(mma_detail::Args& a, int num_sms, cudaStream_t st) {
-    using namespace mma_detail;
-    using C = Cfg<64, BB, NN, GG>;
-    // opt in to the dynamic shared memory of the copy ring and size the
-    // persistent grid from the occupancy, once per instance
-    static int per_sm = -1;
-    static cudaError_t init = [] {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<64, BB, NN, GG>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<64, BB, NN, GG>,
-                                                              kThreads, C::DYN_SMEM);
-        return e;
-    }();
-    if (init != cudaSuccess) return init;
-    const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;
-    long long n = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
-    const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
-    if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every CTA owns a unit
-    if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot
-    if (n < 1) n = 1;
-    a.wm.n = n;
-    // a programmatic dependent of the preceding kernel: the kernel's prologue
-    // and first cache copies overlap that kernel's tail
-    cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3((unsigned)n);
-    lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = C::DYN_SMEM;
-    lc.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, decode_mma_kernel<64, BB, NN, GG>, a);
-}
-}  // namespace
-
 cudaError_t launch_decode_mma_d64(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st) {
-#define KIVI_MMA(BB, NN, GG) \
-    if (bits == BB && nq == NN && G == GG) return launch_one<BB, NN, GG>(a, num_sms, st);
-#define KIVI_MMA_G(BB, NN) KIVI_MMA(BB, NN, 32) KIVI_MMA(BB, NN, 64) 
-    KIVI_MMA_G(2, 1) KIVI_MMA_G(2, 2) KIVI_MMA_G(2, 4)
-    KIVI_MMA_G(4, 1) KIVI_MMA_G(4, 2) KIVI_MMA_G(4, 4)
-#undef KIVI_MMA_G
-#undef KIVI_MMA
-    return cudaErrorInvalidValue;
+    return mma_launch::dispatch<64, false>(a, bits, nq, G, num_sms, st);
 }
 
 }  // namespace kivi

@@ -1,0 +1,63 @@
+// Launch of one tensor-core decode kernel instance (persistent grid, dynamic
+// shared memory, programmatic dependent launch) and the dispatch over the
+// instances of one head_dim; included by the per-head_dim instantiation files.
+#pragma once
+
+#include "kivi_decode_mma.cuh"
+
+namespace kivi {
+namespace mma_launch {
+
+template <int D, int BB, int NN, int GG, bool FUSED>
+cudaError_t launch_one(mma_detail::Args& a, int num_sms, cudaStream_t st) {
+    using namespace mma_detail;
+    using C = Cfg<D, BB, NN, GG>;
+    // opt in to the dynamic shared memory of the copy ring and size the
+    // persistent grid from the occupancy, once per instance
+    static int per_sm = -1;
+    static cudaError_t init = [] {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BB, NN, GG, FUSED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BB, NN, GG, FUSED>,
+                                                              kThreads, C::DYN_SMEM);
+        return e;
+    }();
+    if (init != cudaSuccess) return init;
+    const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;
+    long long n = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
+    const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
+    if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every CTA owns a unit
+    if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot
+    if (n < 1) n = 1;
+    a.wm.n = n;
+    // a programmatic dependent of the preceding kernel: the kernel's prologue
+    // and first cache copies overlap that kernel's tail
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3((unsigned)n);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = C::DYN_SMEM;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, decode_mma_kernel<D, BB, NN, GG, FUSED>, a);
+}
+
+// every (bits, q heads per kv head, G) instance of head_dim D
+template <int D, bool FUSED>
+cudaError_t dispatch(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st) {
+#define KIVI_MMA(BB, NN, GG) \
+    if (bits == BB && nq == NN && G == GG) return launch_one<D, BB, NN, GG, FUSED>(a, num_sms, st);
+#define KIVI_MMA_G(BB, NN) KIVI_MMA(BB, NN, 32) KIVI_MMA(BB, NN, 64) if constexpr (D >= 128) { KIVI_MMA(BB, NN, 128) }
+    KIVI_MMA_G(2, 1) KIVI_MMA_G(2, 2) KIVI_MMA_G(2, 4)
+    KIVI_MMA_G(4, 1) KIVI_MMA_G(4, 2) KIVI_MMA_G(4, 4)
+#undef KIVI_MMA_G
+#undef KIVI_MMA
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mma_launch
+}  // namespace kivi

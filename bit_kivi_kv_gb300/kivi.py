@@ -54,6 +54,7 @@ def _load():
         "kivi_append": (I, [P, P, P, P]),
         "kivi_decode_workspace_bytes": (SZ, [cfgp]),
         "kivi_decode_attn": (I, [P, P, P, F, P, SZ, P]),
+        "kivi_append_decode": (I, [P, P, P, P, P, F, P, SZ, P]),
         "kivi_last_error_string": (ctypes.c_char_p, []),
         "kivi_launch_count": (ctypes.c_ulonglong, []),
         "kivi_cache_set_decode_kernel": (I, [P, I]),
@@ -122,6 +123,11 @@ def kivi_decode_workspace_bytes(cfg: kivi_config) -> int:
 
 def kivi_decode_attn(h: int, q: int, out: int, softmax_scale: float, workspace: int, ws_bytes: int, stream: int):
     _check(lib.kivi_decode_attn(h, q, out, softmax_scale, workspace, ws_bytes, stream))
+
+
+def kivi_append_decode(h: int, k: int, v: int, q: int, out: int, softmax_scale: float, workspace: int,
+                       ws_bytes: int, stream: int):
+    _check(lib.kivi_append_decode(h, k, v, q, out, softmax_scale, workspace, ws_bytes, stream))
 
 
 def kivi_decode_attn_static_ws(h: int, q: int, out: int, softmax_scale: float, stream: int):
@@ -198,4 +204,13 @@ class KiviCache:
             out = torch.empty_like(q)
         kivi_decode_attn(self.handle, self._ptr(q), self._ptr(out), softmax_scale,
                          self.workspace.data_ptr(), self.workspace.numel(), self._stream(stream))
+        return out
+
+    def append_decode(self, k, v, q, out=None, softmax_scale=0.0, stream=None):
+        """append(k, v) then decode_attn(q) in one call (one launch fewer)."""
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        kivi_append_decode(self.handle, self._ptr(k), self._ptr(v), self._ptr(q), self._ptr(out), softmax_scale,
+                           self.workspace.data_ptr(), self.workspace.numel(), self._stream(stream))
         return out

@@ -209,6 +209,20 @@ kivi_status kivi_decode_attn(kivi_cache_t cache, const void* q, void* out, float
                              void* workspace, size_t ws_bytes, kivi_stream_t stream);
 
 /*
+ * Append one token, then decode attention over the cache holding it, in one
+ * call: the same arguments, result and cache state as kivi_append(cache, k, v)
+ * followed by kivi_decode_attn(cache, q, out, softmax_scale, workspace,
+ * ws_bytes, stream) (the method's description has them as two steps; this
+ * fuses them).  With the tensor-core decode kernel the new token's residual
+ * row is written by the decode kernel itself, one launch fewer than the two
+ * calls; with the CUDA-core kernel selected the two calls run in sequence.
+ * Errors as for those two calls; every check runs before anything is
+ * launched.
+ */
+kivi_status kivi_append_decode(kivi_cache_t cache, const void* k, const void* v, const void* q, void* out,
+                               float softmax_scale, void* workspace, size_t ws_bytes, kivi_stream_t stream);
+
+/*
  * Which decode kernel kivi_decode_attn uses.  Both compute the same result
  * within the same tolerance: the CUDA-core kernel accumulates fp32 products of
  * the codes with q * step; the tensor-core kernel feeds exact fp16 codes and

@@ -16,8 +16,9 @@ RTOL_L2 = 1e-3   # ||out - oracle||_2 / ||oracle||_2
 
 
 def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RANGE_2_6_X10_50,
-            sink=True, max_tokens=None, prompt=None, decode_kernel=0):
-    """Prefill L tokens, then n_app x append (decoding at the steps in decode_at).
+            sink=True, max_tokens=None, prompt=None, decode_kernel=0, fused=False):
+    """Prefill L tokens, then n_app x append (decoding at the steps in decode_at;
+    with fused, those steps append and decode in one kivi_append_decode call).
 
     Returns dict(cache, K, V, steps=[(q,k,v)], outs={step: out fp16 cpu}).
     """
@@ -30,6 +31,9 @@ def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RA
     for s in range(n_app):
         q, k, v = syn.step(s)
         steps.append((q, k, v))
+        if fused and s in decode_at:
+            outs[s] = cache.append_decode(k, v, q).cpu()
+            continue
         cache.append(k, v)
         if s in decode_at:
             outs[s] = cache.decode_attn(q).cpu()

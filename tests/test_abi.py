@@ -89,6 +89,18 @@ def test_host_side_checks_without_gpu(K):
         with pytest.raises(K.KiviError) as e:
             K.kivi_append(h, fake + 8, fake, 0)     # misaligned
         assert e.value.status == K.KIVI_ERR_INVALID_ARG
+        ws_need = K.kivi_decode_workspace_bytes(cfg)
+        # fused append + decode: argument checks run before anything is launched
+        for args, status in [((0, fake, fake, fake, 0.0, fake, ws_need), K.KIVI_ERR_INVALID_ARG),
+                             ((fake + 8, fake, fake, fake, 0.0, fake, ws_need), K.KIVI_ERR_INVALID_ARG),
+                             ((fake, fake, 0, fake, 0.0, fake, ws_need), K.KIVI_ERR_INVALID_ARG),
+                             ((fake, fake, fake, fake, 0.0, fake + 64, ws_need), K.KIVI_ERR_INVALID_ARG),
+                             ((fake, fake, fake, fake, float("nan"), fake, ws_need), K.KIVI_ERR_INVALID_ARG),
+                             ((fake, fake, fake, fake, 0.0, fake, ws_need - 1), K.KIVI_ERR_CAPACITY)]:
+            with pytest.raises(K.KiviError) as e:
+                K.kivi_append_decode(h, *args, 0)
+            assert e.value.status == status, (args, e.value.status)
+        assert K.kivi_cache_counts(h) == (0, 0)
         K.kivi_cache_reset(h)
     finally:
         K.kivi_cache_destroy(h)

@@ -52,6 +52,19 @@ def test_small_full_check(case, kernel):
     check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+@pytest.mark.parametrize("case", SMALL, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}D{c[3]}b{c[4]}G{c[5]}R{c[6]}L{c[7]}n{c[8]}" for c in SMALL])
+def test_fused_append_decode(case, kernel):
+    """kivi_append_decode at every step (through residual fills and flushes)
+    equals append + decode: outputs against the oracle at every step, then the
+    cache bytes, including the residual rows the decode kernel stored."""
+    B, Hq, Hkv, D, bits, G, R, L, n = case
+    steps = set(range(n))
+    run = run_gpu(B, Hq, Hkv, D, bits, G, R, L, n, seed=29 + sum(case), decode_at=steps,
+                  decode_kernel=KERNELS[kernel], fused=True)
+    check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
+
+
 def test_degenerate_groups():
     """Constant key channels / value groups (step 0) and signed zeros: codes 0, zero +0."""
     B, H, D, G, R, L = 1, 2, 128, 32, 32, 160
@@ -86,6 +99,14 @@ def test_capacity_and_state_errors():
 
 def _slots(B, Hkv):
     return sorted({(0, 0), (B - 1, Hkv - 1), (B // 2, Hkv // 3)})
+
+
+def test_llama2_7b_layer_fused_full_size():
+    """The 7B-shaped layer decoded with kivi_append_decode at every one of 64 steps."""
+    steps = set(range(64))
+    run = run_gpu(8, 32, 32, 128, 2, 32, 128, 4096, 64, seed=1011, decode_at=steps,
+                  decode_kernel=KIVI_DECODE_TENSOR_CORE, fused=True)
+    check_slots(run, [(0, 0), (7, 31), (3, 17)], {0, 1, 31, 32, 63})
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
