@@ -35,6 +35,22 @@ __device__ __forceinline__ uint32_t nearest_code(float x, float s, float z, int 
     return (uint32_t)min(max(c, 0), L);
 }
 
+// The same code as nearest_code with the division done as a multiply by
+// r = rn(1/s) plus one FMA correction, which lands within 1.5 ulp of the IEEE
+// quotient rn((x - z) / s).  Rounding to the nearest level can then differ
+// only when the quotient is within 2^-17 of a half-integer (ulp <= 2^-19 below
+// 16); those elements, and no others, take the IEEE division.  Quotients
+// >= L + 1 round to L either way.
+__device__ __forceinline__ uint32_t nearest_code_r(float x, float s, float r, float z, int L) {
+    if (s == 0.0f) return 0u;
+    const float d = __fsub_rn(x, z);
+    const float q0 = __fmul_rn(d, r);
+    const float q = __fmaf_rn(__fmaf_rn(-s, q0, d), r, q0);
+    if (q >= (float)L + 1.0f) return (uint32_t)L;
+    if (fabsf(__fsub_rn(q, floorf(q)) - 0.5f) <= 0x1p-17f) return nearest_code(x, s, z, L);
+    return (uint32_t)min(max(__float2int_rn(q), 0), L);
+}
+
 struct QuantArgs {
     uint8_t* cache;
     const __half* src_k;
@@ -46,71 +62,92 @@ struct QuantArgs {
 };
 
 // One CTA quantizes one block (G tokens x D channels) of keys and of values.
+// The block's rows are staged in shared memory with a stride of D + 8 halves,
+// so lanes reading one channel of different tokens hit different banks.  A
+// thread packs the same word position of every 16-token tile, so the
+// coordinates of its codes (and, for keys, their steps and zeros) are fixed
+// once per block.
 template <int D, int BITS>
 __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArgs a) {
     constexpr int L = (1 << BITS) - 1;
     constexpr int W = D * BITS / 64;        // words per lane per tile
     constexpr int PER = 16 / BITS;          // code pairs per word
     constexpr int TILE_WORDS = 32 * W;
+    constexpr int DP = D + 8;               // staged row stride, halves
     extern __shared__ __align__(16) unsigned char smem[];
     const int G = a.G;
-    __half* xs = reinterpret_cast<__half*>(smem);            // [G][D]
-    float* sf = reinterpret_cast<float*>(xs + G * D);         // [D] steps
-    float* zf = sf + D;                                       // [D] zeros
+    const int TPB = G / 16;
+    __half* xs = reinterpret_cast<__half*>(smem);            // [G][DP]
+    // per group: (step, rn(1 / step), zero, unused); D groups for keys and for values
+    float4* szr = reinterpret_cast<float4*>(xs + G * DP);
 
     const int tid = threadIdx.x;
     const long long slot = blockIdx.y;
     const long long j = blockIdx.x;
     uint8_t* part_k = a.cache + slot * a.slot_bytes + (a.first_block + j) * a.part_bytes;
     uint8_t* part_v = part_k + a.NB * a.part_bytes;
-    const long long tiles_bytes = (long long)(G / 16) * a.tile_bytes;
-    const int n_vec = G * D / 8;
+    const long long tiles_bytes = (long long)TPB * a.tile_bytes;
+    auto stage_rows = [&](const __half* src) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + slot * a.src_slot_elems + j * G * D);
+        for (int v = tid; v < G * D / 8; v += kQuantThreads) {
+            const int row = v / (D / 8), c8 = v - row * (D / 8);
+            *reinterpret_cast<uint4*>(xs + row * DP + 8 * c8) = s4[v];
+        }
+    };
 
     // ---------------- keys: per channel over the block's G tokens ----------------
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(a.src_k + slot * a.src_slot_elems + j * G * D);
-        for (int v = tid; v < n_vec; v += kQuantThreads) reinterpret_cast<uint4*>(xs)[v] = src[v];
-    }
+    stage_rows(a.src_k);
     __syncthreads();
     for (int c = tid; c < D; c += kQuantThreads) {
         float mn = INFINITY, mx = -INFINITY;
         for (int t = 0; t < G; ++t) {
-            const float v = __half2float(xs[t * D + c]);
+            const float v = __half2float(xs[t * DP + c]);
             mn = fminf(mn, v);
             mx = fmaxf(mx, v);
         }
         __half* ent = reinterpret_cast<__half*>(part_k + tiles_bytes);   // D steps, then D zeros
-        group_step_zero(mn, mx, L, &sf[c], &zf[c], &ent[c], &ent[D + c]);
+        float sc, zc;
+        group_step_zero(mn, mx, L, &sc, &zc, &ent[c], &ent[D + c]);
+        szr[c] = make_float4(sc, sc != 0.0f ? __frcp_rn(sc) : 0.0f, zc, 0.0f);
     }
     __syncthreads();
-    for (int w = tid; w < (G / 16) * TILE_WORDS; w += kQuantThreads) {
-        const int tt = w / TILE_WORDS, lane = (w % TILE_WORDS) / W, wl = w % W;
+    for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
+        using PP = PairPlace<BITS, false>;
+        const int lane = wt / W, wl = wt - lane * W;
         const int g = lane >> 2, i = lane & 3;
-        uint32_t word = 0;
+        int off[PER], bit[PER];
+        float s0[PER], z0[PER], s1[PER], z1[PER], q0r[PER], q1r[PER];
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
-            using PP = PairPlace<BITS, false>;
-            const int k = PP::k_of(wl, u), r = PP::r_of(wl, u), bit = PP::bit(k, r);
-            const int tok = tt * 16 + g + 8 * (r & 1);
+            const int k = PP::k_of(wl, u), r = PP::r_of(wl, u);
             const int ch = 16 * k + 2 * i + 8 * (r >> 1);
-            const uint32_t c0 = nearest_code(__half2float(xs[tok * D + ch]), sf[ch], zf[ch], L);
-            const uint32_t c1 = nearest_code(__half2float(xs[tok * D + ch + 1]), sf[ch + 1], zf[ch + 1], L);
-            word |= (c0 << bit) | (c1 << (16 + bit));
+            off[u] = (g + 8 * (r & 1)) * DP + ch;
+            bit[u] = PP::bit(k, r);
+            const float4 e0 = szr[ch], e1 = szr[ch + 1];
+            s0[u] = e0.x; q0r[u] = e0.y; z0[u] = e0.z;
+            s1[u] = e1.x; q1r[u] = e1.y; z1[u] = e1.z;
         }
-        reinterpret_cast<uint32_t*>(part_k)[w] = word;
+        for (int tt = 0; tt < TPB; ++tt) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const float2 x = __half22float2(*reinterpret_cast<const __half2*>(xs + tt * 16 * DP + off[u]));
+                const uint32_t c0 = nearest_code_r(x.x, s0[u], q0r[u], z0[u], L);
+                const uint32_t c1 = nearest_code_r(x.y, s1[u], q1r[u], z1[u], L);
+                word |= (c0 << bit[u]) | (c1 << (16 + bit[u]));
+            }
+            reinterpret_cast<uint32_t*>(part_k)[tt * TILE_WORDS + wt] = word;
+        }
     }
     __syncthreads();
 
     // ---------------- values: per token over groups of G channels ----------------
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(a.src_v + slot * a.src_slot_elems + j * G * D);
-        for (int v = tid; v < n_vec; v += kQuantThreads) reinterpret_cast<uint4*>(xs)[v] = src[v];
-    }
+    stage_rows(a.src_v);
     __syncthreads();
     const int ngrp = D / G;                 // channel groups per token; G * ngrp == D entries
     for (int e = tid; e < D; e += kQuantThreads) {
         const int t = e / ngrp, gr = e % ngrp;
-        const __half* row = xs + t * D + gr * G;
+        const __half* row = xs + t * DP + gr * G;
         float mn = INFINITY, mx = -INFINITY;
         for (int jj = 0; jj < G; ++jj) {
             const float v = __half2float(row[(jj + tid) & (G - 1)]);   // rotated start: fewer bank conflicts
@@ -120,25 +157,38 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
         // entry tile of the token's code tile: ngrp rows of 16 steps, then the zeros
         __half* ent = reinterpret_cast<__half*>(part_v + tiles_bytes + (long long)(t / 16) * 64 * ngrp);
         const int at = gr * 16 + entry_pos(t % 16);
-        group_step_zero(mn, mx, L, &sf[e], &zf[e], &ent[at], &ent[16 * ngrp + at]);
+        float se, ze;
+        group_step_zero(mn, mx, L, &se, &ze, &ent[at], &ent[16 * ngrp + at]);
+        szr[e] = make_float4(se, se != 0.0f ? __frcp_rn(se) : 0.0f, ze, 0.0f);
     }
     __syncthreads();
-    for (int w = tid; w < (G / 16) * TILE_WORDS; w += kQuantThreads) {
-        const int tt = w / TILE_WORDS, lane = (w % TILE_WORDS) / W, wl = w % W;
+    for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
+        using PP = PairPlace<BITS, true>;
+        const int lane = wt / W, wl = wt - lane * W;
         const int g = lane >> 2, i = lane & 3;
-        uint32_t word = 0;
+        int off[PER], bit[PER], ent0[PER];
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
-            using PP = PairPlace<BITS, true>;
-            const int k = PP::k_of(wl, u), r = PP::r_of(wl, u), bit = PP::bit(k, r);
+            const int k = PP::k_of(wl, u), r = PP::r_of(wl, u);
             const int ch = 16 * k + g + 8 * (r & 1);
-            const int tok0 = tt * 16 + 2 * i + 8 * (r >> 1);
-            const int e0 = tok0 * ngrp + ch / G, e1 = e0 + ngrp;
-            const uint32_t c0 = nearest_code(__half2float(xs[tok0 * D + ch]), sf[e0], zf[e0], L);
-            const uint32_t c1 = nearest_code(__half2float(xs[(tok0 + 1) * D + ch]), sf[e1], zf[e1], L);
-            word |= (c0 << bit) | (c1 << (16 + bit));
+            const int tok0 = 2 * i + 8 * (r >> 1);
+            off[u] = tok0 * DP + ch;
+            bit[u] = PP::bit(k, r);
+            ent0[u] = tok0 * ngrp + ch / G;   // (step, zero) entry of the first token; the second's is ngrp on
         }
-        reinterpret_cast<uint32_t*>(part_v)[w] = word;
+        for (int tt = 0; tt < TPB; ++tt) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const __half* xp = xs + tt * 16 * DP + off[u];
+                const int e0 = tt * 16 * ngrp + ent0[u], e1 = e0 + ngrp;
+                const float4 f0 = szr[e0], f1 = szr[e1];
+                const uint32_t c0 = nearest_code_r(__half2float(xp[0]), f0.x, f0.y, f0.z, L);
+                const uint32_t c1 = nearest_code_r(__half2float(xp[DP]), f1.x, f1.y, f1.z, L);
+                word |= (c0 << bit[u]) | (c1 << (16 + bit[u]));
+            }
+            reinterpret_cast<uint32_t*>(part_v)[tt * TILE_WORDS + wt] = word;
+        }
     }
 }
 
@@ -171,7 +221,7 @@ cudaError_t launch_quantize_blocks(const Geometry& g, uint8_t* cache, const __ha
     QuantArgs a{cache, src_k, src_v, src_slot_elems, first_block, g.NB, g.part_bytes,
                 g.slot_bytes, g.tile_bytes, g.G};
     const dim3 grid((unsigned)nblk, (unsigned)(g.B * g.Hkv));
-    const size_t smem = (size_t)g.G * g.D * 2 + 2 * (size_t)g.D * 4;
+    const size_t smem = (size_t)g.G * (g.D + 8) * 2 + 16 * (size_t)g.D;   // staged rows + (step, 1/step, zero) per group
     if (g.D == 128 && g.bits == 2) quantize_blocks_kernel<128, 2><<<grid, kQuantThreads, smem, st>>>(a);
     else if (g.D == 128 && g.bits == 4) quantize_blocks_kernel<128, 4><<<grid, kQuantThreads, smem, st>>>(a);
     else if (g.D == 64 && g.bits == 2) quantize_blocks_kernel<64, 2><<<grid, kQuantThreads, smem, st>>>(a);

@@ -65,6 +65,40 @@ def test_fused_append_decode(case, kernel):
     check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantizer_near_ties(bits):
+    """Groups whose elements sit exactly on half-steps (power-of-two steps make
+    (x - z) / s = k + 1/2 exact, so rint breaks ties to even) or one fp16 ulp
+    either side of them: the GPU codes must equal the oracle's fp32 formula."""
+    L_b = (1 << bits) - 1
+    B, H, D, G, R, L = 1, 1, 64, 32, 32, 32 * 9
+    rng = np.random.default_rng(bits)
+    def groups(n_groups, n):
+        """n values per group: min 0, max L_b * s, then half-steps and their neighbours."""
+        out = np.zeros((n_groups, n), np.float32)
+        for gi in range(n_groups):
+            s = np.float32(2.0 ** int(rng.integers(-6, 3)))           # exact fp16 power of two
+            z = np.float32(rng.choice([0.0, -1.0, 0.5, -3.25]))
+            vals = [z, z + L_b * s]
+            for k in range(L_b):
+                t = np.float16(z + (k + 0.5) * s)
+                vals += [t, np.nextafter(t, np.float16(np.inf)), np.nextafter(t, np.float16(-np.inf))]
+            while len(vals) < n:
+                vals.append(z + s * np.float32(rng.integers(0, 4 * L_b + 1)) / 4)
+            v = np.array(vals[:n], np.float32)
+            v = np.clip(v, z, z + L_b * s)                          # keep min / max as set
+            out[gi] = rng.permutation(v)
+        return out.astype(np.float16)
+    # keys: each channel over each block of G tokens is a group
+    K = groups((L // G) * D, G).reshape(L // G, D, G).transpose(0, 2, 1).reshape(1, 1, L, D)
+    # values: each token's G-channel groups
+    V = groups(L * (D // G), G).reshape(1, 1, L, D)
+    K = torch.from_numpy(np.ascontiguousarray(K)).cuda()
+    V = torch.from_numpy(np.ascontiguousarray(V)).cuda()
+    run = run_gpu(B, H, H, D, bits, G, R, L, 33, seed=11, decode_at={32}, prompt=(K, V))
+    check_slots(run, [(0, 0)], {32})
+
+
 def test_degenerate_groups():
     """Constant key channels / value groups (step 0) and signed zeros: codes 0, zero +0."""
     B, H, D, G, R, L = 1, 2, 128, 32, 32, 160
