@@ -47,8 +47,9 @@ __device__ __forceinline__ uint32_t nearest_code_r(float x, float s, float r, fl
     const float q0 = __fmul_rn(d, r);
     const float q = __fmaf_rn(__fmaf_rn(-s, q0, d), r, q0);
     if (q >= (float)L + 1.0f) return (uint32_t)L;
-    if (fabsf(__fsub_rn(q, floorf(q)) - 0.5f) <= 0x1p-17f) return nearest_code(x, s, z, L);
-    return (uint32_t)min(max(__float2int_rn(q), 0), L);
+    const int c = __float2int_rn(q);                      // q >= 0: x >= z, the group minimum
+    if (fabsf(__fsub_rn(q, __int2float_rn(c))) >= 0.5f - 0x1p-17f) return nearest_code(x, s, z, L);
+    return (uint32_t)min(c, L);
 }
 
 struct QuantArgs {
@@ -98,16 +99,25 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
     // ---------------- keys: per channel over the block's G tokens ----------------
     stage_rows(a.src_k);
     __syncthreads();
-    for (int c = tid; c < D; c += kQuantThreads) {
-        float mn = INFINITY, mx = -INFINITY;
-        for (int t = 0; t < G; ++t) {
-            const float v = __half2float(xs[t * DP + c]);
-            mn = fminf(mn, v);
-            mx = fmaxf(mx, v);
+    // min / max of channel pairs (2cp, 2cp+1) over the G tokens on fp16 pairs (exact);
+    // adjacent threads take alternate blocks of 4 tokens (rows 4 apart fall 16
+    // banks apart, so the pair's reads do not conflict) and combine
+    for (int idx = tid; idx < D; idx += kQuantThreads) {
+        const int cp = idx >> 1, half = idx & 1;
+        __half2 mn2 = __half2half2(__ushort_as_half(0x7C00)), mx2 = __half2half2(__ushort_as_half(0xFC00));
+        for (int jt = 0; jt < G / 2; ++jt) {
+            const int t = 8 * (jt >> 2) + 4 * half + (jt & 3);
+            const __half2 v = *reinterpret_cast<const __half2*>(xs + t * DP + 2 * cp);
+            mn2 = __hmin2(mn2, v);
+            mx2 = __hmax2(mx2, v);
         }
+        mn2 = __hmin2(mn2, __shfl_xor_sync(0xffffffffu, mn2, 1));
+        mx2 = __hmax2(mx2, __shfl_xor_sync(0xffffffffu, mx2, 1));
+        const float2 mn = __half22float2(mn2), mx = __half22float2(mx2);
+        const int c = 2 * cp + half;                    // each thread of the pair finishes one channel
         __half* ent = reinterpret_cast<__half*>(part_k + tiles_bytes);   // D steps, then D zeros
         float sc, zc;
-        group_step_zero(mn, mx, L, &sc, &zc, &ent[c], &ent[D + c]);
+        group_step_zero(half ? mn.y : mn.x, half ? mx.y : mx.x, L, &sc, &zc, &ent[c], &ent[D + c]);
         szr[c] = make_float4(sc, sc != 0.0f ? __frcp_rn(sc) : 0.0f, zc, 0.0f);
     }
     __syncthreads();
@@ -148,12 +158,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
     for (int e = tid; e < D; e += kQuantThreads) {
         const int t = e / ngrp, gr = e % ngrp;
         const __half* row = xs + t * DP + gr * G;
-        float mn = INFINITY, mx = -INFINITY;
-        for (int jj = 0; jj < G; ++jj) {
-            const float v = __half2float(row[(jj + tid) & (G - 1)]);   // rotated start: fewer bank conflicts
-            mn = fminf(mn, v);
-            mx = fmaxf(mx, v);
+        __half2 mn2 = __half2half2(__ushort_as_half(0x7C00)), mx2 = __half2half2(__ushort_as_half(0xFC00));
+        for (int jj = 0; jj < G / 2; ++jj) {           // channel pairs; the rotated start spreads banks
+            const __half2 v = *reinterpret_cast<const __half2*>(row + 2 * ((jj + tid + 4 * t) & (G / 2 - 1)));
+            mn2 = __hmin2(mn2, v);
+            mx2 = __hmax2(mx2, v);
         }
+        const float2 mnf = __half22float2(mn2), mxf = __half22float2(mx2);
+        const float mn = fminf(mnf.x, mnf.y), mx = fmaxf(mxf.x, mxf.y);
         // entry tile of the token's code tile: ngrp rows of 16 steps, then the zeros
         __half* ent = reinterpret_cast<__half*>(part_v + tiles_bytes + (long long)(t / 16) * 64 * ngrp);
         const int at = gr * 16 + entry_pos(t % 16);
