@@ -48,6 +48,8 @@ WORKLOADS = {
                                layers=40, outliers="range", sink=True, seed=1002),
     "llama3-8b-gqa": dict(B=64, Hq=32, Hkv=8, D=128, bits=4, G=128, R=128, prompt=8192, decode=20,
                           layers=2, outliers="range", sink=True, seed=1003),
+    "llama2-7b-layer-8bit": dict(B=8, Hq=32, Hkv=32, D=128, bits=8, G=32, R=128, prompt=4096, decode=64,
+                                 layers=4, outliers="range", sink=True, seed=1005),
     "long-context": dict(B=2, Hq=32, Hkv=32, D=128, bits=2, G=32, R=128, prompt=131072, decode=512,
                          layers=1, outliers="range", sink=True, seed=1004),
 }

@@ -61,7 +61,7 @@ kivi_status derive_geometry(const kivi_config* c, Geometry* g, const char** why)
         *why = "batch, heads, head_dim, group, residual and max_tokens must be positive";
         return KIVI_ERR_INVALID_ARG;
     }
-    if (c->bits != 2 && c->bits != 4) { *why = "bits must be 2 or 4"; return KIVI_ERR_UNSUPPORTED; }
+    if (c->bits != 2 && c->bits != 4 && c->bits != 8) { *why = "bits must be 2, 4 or 8"; return KIVI_ERR_UNSUPPORTED; }
     if (c->head_dim != 64 && c->head_dim != 128) { *why = "head_dim must be 64 or 128"; return KIVI_ERR_UNSUPPORTED; }
     if (c->group != 32 && c->group != 64 && c->group != 128) { *why = "group must be 32, 64 or 128"; return KIVI_ERR_UNSUPPORTED; }
     if (c->head_dim % c->group) { *why = "head_dim must be a multiple of group (value groups)"; return KIVI_ERR_INVALID_ARG; }

@@ -395,6 +395,8 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
     KIVI_DISPATCH(128, 4, 1) KIVI_DISPATCH(128, 4, 2) KIVI_DISPATCH(128, 4, 4)
     KIVI_DISPATCH(64, 2, 1) KIVI_DISPATCH(64, 2, 2) KIVI_DISPATCH(64, 2, 4)
     KIVI_DISPATCH(64, 4, 1) KIVI_DISPATCH(64, 4, 2) KIVI_DISPATCH(64, 4, 4)
+    KIVI_DISPATCH(128, 8, 1) KIVI_DISPATCH(128, 8, 2) KIVI_DISPATCH(128, 8, 4)
+    KIVI_DISPATCH(64, 8, 1) KIVI_DISPATCH(64, 8, 2) KIVI_DISPATCH(64, 8, 4)
 #undef KIVI_DISPATCH
     *launches = 0;
     return cudaErrorInvalidValue;

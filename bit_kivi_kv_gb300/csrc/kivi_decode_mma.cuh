@@ -214,6 +214,19 @@ __device__ __forceinline__ void a_frag(const uint32_t (&w)[W], const uint32_t (&
     }
 }
 
+// The same fragment with the 8-bit shifts done in place (no shifted copy of
+// the words kept): 8-bit codes give a lane 4x the words of 2-bit ones.
+template <int BITS, bool VALUES, int W>
+__device__ __forceinline__ void a_frag_inline(const uint32_t (&w)[W], int t, uint32_t (&a)[4]) {
+    using PP = PairPlace<BITS, VALUES>;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const uint32_t word = w[PP::word(t, r)];
+        const uint32_t field = ((1u << BITS) - 1u) * 0x00010001u << (BITS * (PP::cls(t, r) % PP::P));
+        a[r] = (PP::order(r) ? word >> 8 : word) & field;
+    }
+}
+
 template <int W>
 __device__ __forceinline__ void load_tile_words(const uint8_t* p, uint32_t (&w)[W]) {
     if constexpr (W % 4 == 0) {
@@ -567,7 +580,35 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
                                         beta);
             // keys: logits of tokens g, g+8 of both tiles for head i
             float sc[4];
-            {
+            if constexpr (BITS == 8) {
+                // one tile at a time: a lane's 16 words per tile, shifted in place
+                float ca[4] = {beta, 0.f, beta, 0.f};
+                float cb[4] = {beta, 0.f, beta, 0.f};
+                {
+                    uint32_t w[W];
+                    lds_words(stage_u32, w);
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        uint32_t fa[4];
+                        a_frag_inline<BITS, false, W>(w, kk, fa);
+                        mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
+                    }
+                }
+                {
+                    uint32_t w[W];
+                    lds_words(stage_u32 + C::TILE, w);
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        uint32_t fb[4];
+                        a_frag_inline<BITS, false, W>(w, kk, fb);
+                        mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
+                    }
+                }
+                sc[0] = ca[0] + ca[1];
+                sc[1] = ca[2] + ca[3];
+                sc[2] = cb[0] + cb[1];
+                sc[3] = cb[2] + cb[3];
+            } else {
                 uint32_t wa[W], wbw[W], wa8[W], wb8[W];
                 lds_words(stage_u32, wa);
                 lds_words(stage_u32 + C::TILE, wbw);
@@ -604,16 +645,27 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
                     const uint2 sv = lds64(ve + 32u * GB * f), zv = lds64(ve + 32u * (NGRP + GB * f));
                     p_frag(prb, ph01, ph89, pl01, pl89, sv, zv, pb[f][0], pb[f][1], zeta[f]);
                 }
-                uint32_t wv[W], wv8[W];
+                uint32_t wv[W];
                 lds_words(stage_u32 + (2 + t) * C::TILE, wv);
+                if constexpr (BITS == 8) {
 #pragma unroll
-                for (int x = 0; x < W; ++x) wv8[x] = wv[x] >> 8;
+                    for (int mt = 0; mt < KS; ++mt) {
+                        uint32_t af[4];
+                        a_frag_inline<BITS, true, W>(wv, mt, af);
+                        const int f = (16 * mt / G) / GB;
+                        mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                    }
+                } else {
+                    uint32_t wv8[W];
 #pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    uint32_t af[4];
-                    a_frag<BITS, true, W>(wv, wv8, mt, af);
-                    const int f = (16 * mt / G) / GB;
-                    mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                    for (int x = 0; x < W; ++x) wv8[x] = wv[x] >> 8;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        uint32_t af[4];
+                        a_frag<BITS, true, W>(wv, wv8, mt, af);
+                        const int f = (16 * mt / G) / GB;
+                        mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                    }
                 }
             }
             __syncwarp();                              // every lane is done with this stage

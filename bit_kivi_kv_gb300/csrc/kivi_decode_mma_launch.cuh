@@ -54,6 +54,7 @@ cudaError_t dispatch(mma_detail::Args& a, int bits, int nq, int G, int num_sms, 
 #define KIVI_MMA_G(BB, NN) KIVI_MMA(BB, NN, 32) KIVI_MMA(BB, NN, 64) if constexpr (D >= 128) { KIVI_MMA(BB, NN, 128) }
     KIVI_MMA_G(2, 1) KIVI_MMA_G(2, 2) KIVI_MMA_G(2, 4)
     KIVI_MMA_G(4, 1) KIVI_MMA_G(4, 2) KIVI_MMA_G(4, 4)
+    KIVI_MMA_G(8, 1) KIVI_MMA_G(8, 2) KIVI_MMA_G(8, 4)
 #undef KIVI_MMA_G
 #undef KIVI_MMA
     return cudaErrorInvalidValue;

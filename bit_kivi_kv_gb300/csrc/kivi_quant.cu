@@ -39,16 +39,17 @@ __device__ __forceinline__ uint32_t nearest_code(float x, float s, float z, int 
 // r = rn(1/s) plus one FMA correction, which lands within 1.5 ulp of the IEEE
 // quotient rn((x - z) / s).  Rounding to the nearest level can then differ
 // only when the quotient is within 2^-17 of a half-integer (ulp <= 2^-19 below
-// 16); those elements, and no others, take the IEEE division.  Quotients
-// >= L + 1 round to L either way.
+// 16; 2^-15 with 8-bit codes, ulp <= 2^-16 below 256); those elements, and no
+// others, take the IEEE division.  Quotients >= L + 1 round to L either way.
 __device__ __forceinline__ uint32_t nearest_code_r(float x, float s, float r, float z, int L) {
+    const float near = L > 15 ? 0x1p-15f : 0x1p-17f;
     if (s == 0.0f) return 0u;
     const float d = __fsub_rn(x, z);
     const float q0 = __fmul_rn(d, r);
     const float q = __fmaf_rn(__fmaf_rn(-s, q0, d), r, q0);
     if (q >= (float)L + 1.0f) return (uint32_t)L;
     const int c = __float2int_rn(q);                      // q >= 0: x >= z, the group minimum
-    if (fabsf(__fsub_rn(q, __int2float_rn(c))) >= 0.5f - 0x1p-17f) return nearest_code(x, s, z, L);
+    if (fabsf(__fsub_rn(q, __int2float_rn(c))) >= 0.5f - near) return nearest_code(x, s, z, L);
     return (uint32_t)min(c, L);
 }
 
@@ -238,6 +239,8 @@ cudaError_t launch_quantize_blocks(const Geometry& g, uint8_t* cache, const __ha
     else if (g.D == 128 && g.bits == 4) quantize_blocks_kernel<128, 4><<<grid, kQuantThreads, smem, st>>>(a);
     else if (g.D == 64 && g.bits == 2) quantize_blocks_kernel<64, 2><<<grid, kQuantThreads, smem, st>>>(a);
     else if (g.D == 64 && g.bits == 4) quantize_blocks_kernel<64, 4><<<grid, kQuantThreads, smem, st>>>(a);
+    else if (g.D == 128 && g.bits == 8) quantize_blocks_kernel<128, 8><<<grid, kQuantThreads, smem, st>>>(a);
+    else if (g.D == 64 && g.bits == 8) quantize_blocks_kernel<64, 8><<<grid, kQuantThreads, smem, st>>>(a);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

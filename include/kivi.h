@@ -75,7 +75,7 @@ typedef enum {
 } kivi_status;
 
 /*
- * Cache shape.  Supported: bits in {2, 4}; head_dim in {64, 128};
+ * Cache shape.  Supported: bits in {2, 4, 8}; head_dim in {64, 128};
  * group in {32, 64, 128} with head_dim % group == 0 (value groups) and
  * residual % group == 0, residual >= group; n_q_heads / n_kv_heads in
  * {1, 2, 4}; max_tokens >= 1 is the most tokens (quantized + residual) one

@@ -39,6 +39,8 @@ SMALL = [
     (2, 2, 2, 128, 2, 64, 128, 100, 5),       # prompt shorter than R: nothing quantized
     (1, 4, 1, 128, 2, 32, 32, 515, 40),       # 4 q heads per kv head, R = G
     (2, 2, 2, 128, 4, 32, 64, 161, 3),        # 4-bit with small groups
+    (2, 4, 2, 128, 8, 32, 64, 333, 40),       # 8-bit, grouped queries, a flush
+    (1, 2, 2, 64, 8, 64, 64, 200, 70),        # 8-bit D64 G64, flushes
 ]
 
 
@@ -65,7 +67,7 @@ def test_fused_append_decode(case, kernel):
     check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_quantizer_near_ties(bits):
     """Groups whose elements sit exactly on half-steps (power-of-two steps make
     (x - z) / s = k + 1/2 exact, so rint breaks ties to even) or one fp16 ulp
@@ -77,10 +79,12 @@ def test_quantizer_near_ties(bits):
         """n values per group: min 0, max L_b * s, then half-steps and their neighbours."""
         out = np.zeros((n_groups, n), np.float32)
         for gi in range(n_groups):
-            s = np.float32(2.0 ** int(rng.integers(-6, 3)))           # exact fp16 power of two
+            # an fp16 power of two small enough that z + k*s stays exact in fp16
+            s = np.float32(2.0 ** int(rng.integers(-6, 3) if bits < 8 else rng.integers(-9, -3)))
             z = np.float32(rng.choice([0.0, -1.0, 0.5, -3.25]))
             vals = [z, z + L_b * s]
-            for k in range(L_b):
+            levels = range(L_b) if L_b < 16 else sorted(rng.choice(L_b, 10, replace=False))
+            for k in levels:
                 t = np.float16(z + (k + 0.5) * s)
                 vals += [t, np.nextafter(t, np.float16(np.inf)), np.nextafter(t, np.float16(-np.inf))]
             while len(vals) < n:
@@ -175,7 +179,7 @@ def test_long_context_streaming_full_size():
     check_slots(run, [(0, 0), (1, 31)], steps)
 
 
-COMBOS = [(D, bits, nq, G) for D in (64, 128) for bits in (2, 4) for nq in (1, 2, 4)
+COMBOS = [(D, bits, nq, G) for D in (64, 128) for bits in (2, 4, 8) for nq in (1, 2, 4)
           for G in (32, 64, 128) if G <= D]
 
 

@@ -5,7 +5,7 @@ import pytest
 from oracle import accounting, layout
 
 
-@pytest.mark.parametrize("D,b", [(64, 2), (64, 4), (128, 2), (128, 4)])
+@pytest.mark.parametrize("D,b", [(64, 2), (64, 4), (64, 8), (128, 2), (128, 4), (128, 8)])
 @pytest.mark.parametrize("kind", ["key", "value"])
 def test_round_trip_and_full_coverage(D, b, kind):
     rng = np.random.default_rng(D + b)

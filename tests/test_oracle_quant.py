@@ -45,13 +45,14 @@ def _exact_nearest(x, s, z, L):
     return [abs(xs - (k * ss + zs)) for k in range(L + 1)]
 
 
-@pytest.mark.parametrize("B", [2, 4])
+@pytest.mark.parametrize("B", [2, 4, 8])
 def test_brute_force_nearest_level(B):
     """Each chosen code is a nearest level of the stored grid (exact arithmetic).
 
-    fp32 rounding of (x - z)/s may pick the farther neighbour only when the
-    exact ratio is within 2^-19 of a half-integer, so the allowed excess
-    distance is 2^-18 * s.
+    fp32 rounding of (x - z) and of its quotient by s moves the ratio by at
+    most 2^-23 of its size (< L + 1), so the farther neighbour can be picked
+    only that close to a half-integer: the allowed excess distance is
+    s * max(2^-18, (L + 1) * 2^-22).
     """
     rng = np.random.default_rng(7)
     L = quant.levels(B)
@@ -62,7 +63,7 @@ def test_brute_force_nearest_level(B):
             for j in range(G):
                 d = _exact_nearest(X[g, j], s[g, 0], z[g, 0], L)
                 assert 0 <= codes[g, j] <= L
-                slack = Fraction(float(s[g, 0])) / 2**18
+                slack = Fraction(float(s[g, 0])) * max(Fraction(1, 2**18), Fraction(L + 1, 2**22))
                 assert d[codes[g, j]] <= min(d) + slack
 
 
@@ -83,7 +84,7 @@ def test_joint_brute_force_small_groups(B):
         assert err(codes[g]) <= best + G * (ss / 2**17) ** 2 + 2 * G * ss * ss / 2**18
 
 
-@pytest.mark.parametrize("B", [2, 4])
+@pytest.mark.parametrize("B", [2, 4, 8])
 def test_half_step_bound_and_level_coverage(B):
     """|x - x_hat| <= s/2 (+ fp32 slack); the minimum gets code 0 and the maximum code L."""
     rng = np.random.default_rng(3)
@@ -93,7 +94,7 @@ def test_half_step_bound_and_level_coverage(B):
     xhat = quant.dequantize(codes, s, z)
     sd = s.astype(np.float64)
     err = np.abs(X.astype(np.float64) - xhat)
-    assert np.all(err <= sd / 2 * (1 + 2.0**-17))
+    assert np.all(err <= sd / 2 * (1 + max(2.0**-17, (L + 1) * 2.0**-21)))
     assert np.all(s > 0)
     assert np.all(codes[np.arange(2000), X.argmin(axis=1)] == 0)
     assert np.all(codes[np.arange(2000), X.argmax(axis=1)] == L)
