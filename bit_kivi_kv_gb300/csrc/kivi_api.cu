@@ -337,6 +337,8 @@ namespace kivi {
 
 kivi_status report_error(kivi_status st, const char* msg) { return fail(st, "%s", msg); }
 
+void count_launches(int n) { g_launches += (unsigned long long)n; }
+
 size_t decode_workspace_need(const kivi_cache* c) {
     const Geometry& g = c->geo;
     return (size_t)g.B * g.Hq * kPartialSlots * partial_stride(g.D) * sizeof(float);

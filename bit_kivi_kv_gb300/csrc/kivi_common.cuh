@@ -68,14 +68,21 @@ __host__ __device__ constexpr int entry_pos(int t) { return 4 * ((t & 7) >> 1) +
 struct WorkMap {
     long long P, PR, wq, wr, Ws, Wt, n;
 };
-__host__ __device__ inline long long unit_start(const WorkMap& m, long long u) {
-    return u < m.P ? u * m.wq : m.P * m.wq + (u - m.P) * m.wr;
+// the same for a slot of P quantized pairs (slots of ragged sequences differ)
+__host__ __device__ inline long long unit_start_p(long long P, long long wq, long long wr, long long u) {
+    return u < P ? u * wq : P * wq + (u - P) * wr;
 }
 // first unit of a slot starting at or after weight offset y (0 <= y <= Ws); P + PR if none
-__host__ __device__ inline long long first_unit_at(const WorkMap& m, long long y) {
+__host__ __device__ inline long long first_unit_at_p(long long P, long long wq, long long wr, long long y) {
     if (y <= 0) return 0;
-    if (y <= m.P * m.wq) return (y + m.wq - 1) / m.wq;
-    return m.P + (y - m.P * m.wq + m.wr - 1) / m.wr;
+    if (y <= P * wq) return (y + wq - 1) / wq;
+    return P + (y - P * wq + wr - 1) / wr;
+}
+__host__ __device__ inline long long unit_start(const WorkMap& m, long long u) {
+    return unit_start_p(m.P, m.wq, m.wr, u);
+}
+__host__ __device__ inline long long first_unit_at(const WorkMap& m, long long y) {
+    return first_unit_at_p(m.P, m.wq, m.wr, y);
 }
 __host__ __device__ inline long long map_begin(const WorkMap& m, long long c) { return c * m.Wt / m.n; }
 // the CTA whose range holds weight position x
@@ -130,9 +137,59 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
                           float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
                           int* launches, const FusedAppend& fa = FusedAppend{});
 
+// ---- paged cache (kivi.h, "Paged cache with ragged sequences") ----
+
+constexpr int kMaxCallSeqs = KIVI_PAGED_MAX_CALL_SEQS;
+
+// Geometry of a paged cache: g.B = max_seqs, g.NB = max_blocks_per_seq; the
+// residual offsets and resid_slot_bytes keep their meaning per (sequence, kv
+// head) slot; slot_bytes is unused.
+struct PagedGeometry {
+    Geometry g;
+    long long n_pages, page_bytes, table_off;
+};
+
+// One sequence of a paged decode call.  Its Hkv slots take weight positions
+// [start, start + Hkv * Ws), Ws = P * wq + ceil(n_resid / 32) * wr.
+struct PagedSeq {
+    long long start;
+    int seq;       // sequence slot: residual rows and block-table row
+    int P;         // quantized tile pairs (Lq / 32)
+    int n_resid;   // residual rows, the fused append's included
+    int new_row;   // the fused append's residual row, -1: none
+};
+
+// One block quantized into a page: head h's G rows start at
+// src + src_off + h * src_head_elems; table entry tbl_idx is set to page.
+struct QJob {
+    long long src_off;
+    int page;
+    int tbl_idx;
+};
+constexpr int kMaxQJobs = 1024;   // per launch
+
+// Quantize njobs blocks (any number; launched in chunks of kMaxQJobs).
+cudaError_t launch_quantize_pages(const PagedGeometry& pg, uint8_t* buf, const __half* src_k,
+                                  const __half* src_v, long long src_head_elems, const QJob* jobs,
+                                  int njobs, cudaStream_t st, int* launches);
+
+// Copy nrows rows per slot into residual rows [row0, row0 + nrows) of slots
+// [first_slot, first_slot + nslots); slot j's rows come from src + j * src_slot_elems.
+cudaError_t launch_copy_rows_slots(const Geometry& g, uint8_t* cache, const __half* src_k,
+                                   const __half* src_v, long long src_slot_elems, long long first_slot,
+                                   int nslots, int row0, int nrows, cudaStream_t st);
+
+// Tensor-core decode over the n sequences of a paged call (+ its merge).
+// new_k / new_v: the fused append's tokens [n][Hkv][D], or null.
+cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, const PagedSeq* seqs, int n,
+                                const __half* q, __half* out, float scale_log2, float* workspace,
+                                const __half* new_k, const __half* new_v, int early_ok, int num_sms,
+                                cudaStream_t st, int* launches);
+
 // Host-side helpers of the C ABI (kivi_api.cu): set the calling thread's
 // error string and return st; the decode workspace bytes a handle needs.
 kivi_status report_error(kivi_status st, const char* msg);
+void count_launches(int n);   // adds to kivi_launch_count()
 size_t decode_workspace_need(const struct ::kivi_cache* c);
 
 }  // namespace kivi

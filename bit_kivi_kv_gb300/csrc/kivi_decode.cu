@@ -339,6 +339,79 @@ cudaError_t launch_decode_mma_d128(mma_detail::Args& a, int bits, int nq, int G,
 cudaError_t launch_decode_mma_d64(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_mma_d128f(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_mma_d64f(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_mma_d128p(mma_detail::PagedArgs& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_mma_d64p(mma_detail::PagedArgs& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+
+namespace {
+
+// Launch the merge kernel as a programmatic dependent of the decode kernel.
+template <typename K, typename A>
+cudaError_t launch_finish(K kernel, const A& f, long long ctas, int D, cudaStream_t st) {
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3((unsigned)ctas);
+    lc.blockDim = dim3((unsigned)D);
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, f);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, const PagedSeq* seqs, int n,
+                                const __half* q, __half* out, float scale_log2, float* workspace,
+                                const __half* new_k, const __half* new_v, int early_ok, int num_sms,
+                                cudaStream_t st, int* launches) {
+    const Geometry& g = pg.g;
+    *launches = 0;
+    if (n < 1 || n > kMaxCallSeqs) return cudaErrorInvalidValue;
+    const int nq = g.Hq / g.Hkv;
+    WorkMap wm{};
+    wm.wq = (long long)g.D * g.bits / 4 + 8LL * g.D / g.G;
+    wm.wr = 4LL * g.D;
+    mma_detail::PagedArgs m;   // ~12 KB of kernel parameters
+    long long start = 0, ws_max = 0;
+    for (int i = 0; i < n; ++i) {
+        PagedSeq s = seqs[i];
+        const long long Ws = s.P * wm.wq + (long long)((s.n_resid + 31) / 32) * wm.wr;
+        if (Ws <= 0) return cudaErrorInvalidValue;   // a sequence without tokens
+        s.start = start;
+        start += g.Hkv * Ws;
+        if (Ws > ws_max) ws_max = Ws;
+        m.seqs[i] = s;
+    }
+    wm.Ws = ws_max;
+    wm.Wt = start;
+    static_cast<mma_detail::Args&>(m) =
+        mma_detail::Args{buf, q, workspace, g.NB, g.part_bytes, 0, g.tile_bytes, g.k_resid_off, g.v_resid_off,
+                         g.R, g.Hq, g.Hkv, 0, wm, scale_log2, new_k, new_v, -1, early_ok};
+    m.table = reinterpret_cast<const int*>(buf + pg.table_off);
+    m.max_blocks = (int)g.NB;
+    m.n_pages = (int)pg.n_pages;
+    m.n_seqs = n;
+    cudaError_t e = (g.D == 128 ? launch_decode_mma_d128p : launch_decode_mma_d64p)(m, g.bits, nq, g.G, num_sms, st);
+    if (e != cudaSuccess) return e;
+    *launches = 1;
+    mma_detail::PagedFinishArgs f;
+    f.ws = workspace;
+    f.out = out;
+    f.Hq = g.Hq;
+    f.Hkv = g.Hkv;
+    f.nq = nq;
+    f.wm = m.wm;   // with the grid size the launch chose
+    f.n_seqs = n;
+    for (int i = 0; i < n; ++i) f.seqs[i] = m.seqs[i];
+    e = g.D == 128 ? launch_finish(mma_detail::finish_paged_kernel<128>, f, (long long)n * g.Hq, g.D, st)
+                   : launch_finish(mma_detail::finish_paged_kernel<64>, f, (long long)n * g.Hq, g.D, st);
+    if (e != cudaSuccess) return e;
+    *launches = 2;
+    return cudaSuccess;
+}
 
 
 

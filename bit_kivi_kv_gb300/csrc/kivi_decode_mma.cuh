@@ -68,6 +68,36 @@ struct FinishArgs {
     WorkMap wm;
 };
 
+// Kernel modes: plain decode; decode with a fused append; paged cache with
+// ragged sequences (fused append optional per sequence).
+constexpr int kModePlain = 0, kModeFused = 1, kModePaged = 2;
+
+// Paged call: cache = the page pool (and the buffer holding residual rows and
+// the block table); q / out / ws / new_k / new_v are indexed by the call's
+// sequence i in place of the batch row; wm.Ws is the largest slot weight.
+// NB, slot_bytes, n_resid and new_row of Args are unused.
+struct PagedArgs : Args {
+    const int* table;
+    int max_blocks;
+    int n_pages;
+    int n_seqs;
+    PagedSeq seqs[kMaxCallSeqs];
+};
+
+struct PagedFinishArgs {
+    const float* ws;
+    __half* out;
+    int Hq, Hkv, nq;
+    WorkMap wm;
+    int n_seqs;
+    PagedSeq seqs[kMaxCallSeqs];
+};
+
+template <int MODE>
+struct ArgsOf { using type = Args; };
+template <>
+struct ArgsOf<kModePaged> { using type = PagedArgs; };
+
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -343,11 +373,14 @@ struct MinCtas {
     static constexpr int value = (D == 128 && NQ == 4) ? 3 : 4;
 };
 
-// FUSED: the call appends a token (Args::new_row) the kernel reads from its
-// inputs and stores in the cache; a separate instance so that plain decode
-// calls carry none of that code.
-template <int D, int BITS, int NQ, int G, bool FUSED>
-__global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_kernel(Args a) {
+// MODE kModeFused: the call appends a token (Args::new_row) the kernel reads
+// from its inputs and stores in the cache; kModePaged: blocks are addressed
+// through the block table and every sequence has its own length and appended
+// row.  Separate instances, so that plain decode calls carry none of that code.
+template <int D, int BITS, int NQ, int G, int MODE>
+__global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
+    decode_mma_kernel(const __grid_constant__ typename ArgsOf<MODE>::type a) {
+    constexpr bool FUSED = MODE != kModePlain, PAGED = MODE == kModePaged;
     using C = Cfg<D, BITS, NQ, G>;
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
     __shared__ __align__(16) float qf[NQ][D];
@@ -382,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
         qoff[j] = ((cc & 7) >> 1) * C::QSTRIDE + 2 * (cp >> 3) + (cc >> 3);
     }
     const uint32_t ring_u32 = smem_u32(ring), bars_u32 = smem_u32(bars);
-    const long long vdelta = a.NB * a.part_bytes;    // key part -> value part of a block
+    const long long vdelta = PAGED ? a.part_bytes : a.NB * a.part_bytes;   // key part -> value part of a block
     // this lane's B column for the values: head hP, group slot jP, hi/lo
     const int colP = g >> 1, hP = colP / GB, jP = colP % GB;
     const bool lo_col = (g & 1) != 0;
@@ -473,43 +506,109 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
     // This CTA's share of the call's work: the units starting in its weight range
     // [pos, pe); one partial result per slot it touches.
     const WorkMap& wm = a.wm;
-    const long long cta = blockIdx.x, NU = wm.P + wm.PR;
+    const long long cta = blockIdx.x;
     long long pos = map_begin(wm, cta);
     const long long pe = map_begin(wm, cta + 1);
     bool first_seg = true;
+    bool bad_page = false;   // lane 0: a block-table entry was out of range (sticky)
     while (pos < pe) {
-        const long long slot = pos / wm.Ws;
-        const long long u0 = first_unit_at(wm, pos - slot * wm.Ws);
-        if (u0 >= NU) { pos = (slot + 1) * wm.Ws; continue; }
-        if (slot * wm.Ws + unit_start(wm, u0) >= pe) break;
-        const long long u1 = first_unit_at(wm, min(pe - slot * wm.Ws, wm.Ws));
-        const int p0 = (int)min(u0, wm.P), p1 = (int)min(u1, wm.P);              // quantized pairs
-        const int r0 = (int)(max(u0, wm.P) - wm.P), r1 = (int)(max(u1, wm.P) - wm.P);  // residual pairs
-        const int part = (int)(cta - slot_first_cta(wm, slot));
-        const int b = (int)(slot / a.Hkv), hk = (int)(slot % a.Hkv);
-        const uint8_t* slot_base = a.cache + slot * a.slot_bytes;
+        // the slot holding weight position pos: weights [w0, w0 + Ws), P quantized
+        // pairs then PR residual pairs
+        long long w0, Ws, P, PR;
+        int b, hk;               // query / output row (batch row or call sequence), kv head
+        long long rslot, islot;  // residual slot; row of the fused append's inputs
+        int n_res, nrow;         // residual rows; the fused append's row (-1: none)
+        long long trow = 0;      // paged: offset of the sequence's block-table row
+        if constexpr (PAGED) {
+            int lo = 0, hi = a.n_seqs - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (a.seqs[mid].start <= pos) lo = mid; else hi = mid - 1;
+            }
+            const PagedSeq& sq = a.seqs[lo];
+            P = sq.P;
+            PR = (sq.n_resid + 31) / 32;
+            Ws = P * wm.wq + PR * wm.wr;
+            hk = (int)((pos - sq.start) / Ws);
+            w0 = sq.start + hk * Ws;
+            b = lo;
+            rslot = (long long)sq.seq * a.Hkv + hk;
+            islot = (long long)lo * a.Hkv + hk;
+            n_res = sq.n_resid;
+            nrow = sq.new_row;
+            trow = (long long)sq.seq * a.max_blocks;
+        } else {
+            const long long slot = pos / wm.Ws;
+            w0 = slot * wm.Ws;
+            Ws = wm.Ws;
+            P = wm.P;
+            PR = wm.PR;
+            b = (int)(slot / a.Hkv);
+            hk = (int)(slot % a.Hkv);
+            rslot = islot = slot;
+            n_res = a.n_resid;
+            nrow = a.new_row;
+        }
+        const long long NU = P + PR;
+        const long long u0 = first_unit_at_p(P, wm.wq, wm.wr, pos - w0);
+        if (u0 >= NU) { pos = w0 + Ws; continue; }
+        if (w0 + unit_start_p(P, wm.wq, wm.wr, u0) >= pe) break;
+        const long long u1 = first_unit_at_p(P, wm.wq, wm.wr, min(pe - w0, Ws));
+        const int p0 = (int)min(u0, P), p1 = (int)min(u1, P);                  // quantized pairs
+        const int r0 = (int)(max(u0, P) - P), r1 = (int)(max(u1, P) - P);      // residual pairs
+        const int part = (int)(cta - map_owner(wm, w0));
         // ---- this warp's contiguous run of pairs, two tiles per ring stage ----
         const int pw = (p1 - p0 + kWarps - 1) / kWarps;
         const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
         const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
         auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
         // lane 0's copy cursor: key part of the block of the next pair to fetch, tile in block
-        const uint8_t* kcur = slot_base + (long long)((2 * wb) / C::TPB) * a.part_bytes;
+        // (paged: the block's page pg and the next block's page pgn, loaded one block ahead)
+        const uint8_t* kcur;
+        int pg = 0, pgn = 0, blk = 0;
+        if constexpr (PAGED) {
+            kcur = a.cache;
+            if (lane == 0 && npairs > 0) {
+                blk = (2 * wb) / C::TPB;
+                pg = __ldg(a.table + trow + blk);
+                pgn = __ldg(a.table + trow + min(blk + 1, a.max_blocks - 1));
+            }
+        } else {
+            kcur = a.cache + rslot * a.slot_bytes + (long long)((2 * wb) / C::TPB) * a.part_bytes;
+        }
         int tcur = (2 * wb) % C::TPB;
         bool first = true;
         auto issue_next = [&](uint32_t it) {          // lane 0: next pair -> ring stage of item it
             const uint32_t st = it % C::STAGES;
             const uint32_t dst = ring_u32 + st * C::STAGE_BYTES, bar = bars_u32 + 8 * st;
             const bool kz = first || tcur == 0;
-            const uint8_t* vcur = kcur + vdelta;
+            const uint8_t* kp;
+            if constexpr (PAGED) {
+                // an entry outside the pool is flagged and read from page 0 instead
+                const bool okp = (unsigned)pg < (unsigned)a.n_pages;
+                bad_page |= !okp;
+                kp = a.cache + ((long long)(okp ? pg : 0) * a.Hkv + hk) * 2 * a.part_bytes;
+            } else {
+                kp = kcur;
+            }
+            const uint8_t* vcur = kp + vdelta;
             mbar_expect_tx_u32(bar, 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
-            tma_1d_u32(dst, kcur + tcur * C::TILE, 2 * C::TILE, bar);
+            tma_1d_u32(dst, kp + tcur * C::TILE, 2 * C::TILE, bar);
             tma_1d_u32(dst + 2 * C::TILE, vcur + tcur * C::TILE, 2 * C::TILE, bar);
             tma_1d_u32(dst + 4 * C::TILE, vcur + tiles_bytes + tcur * C::ENT, 2 * C::ENT, bar);
-            if (kz) tma_1d_u32(dst + 4 * C::TILE + 2 * C::ENT, kcur + tiles_bytes, C::KSZ, bar);
+            if (kz) tma_1d_u32(dst + 4 * C::TILE + 2 * C::ENT, kp + tiles_bytes, C::KSZ, bar);
             first = false;
             tcur += 2;
-            if (tcur == C::TPB) { tcur = 0; kcur += a.part_bytes; }
+            if (tcur == C::TPB) {
+                tcur = 0;
+                if constexpr (PAGED) {
+                    ++blk;
+                    pg = pgn;
+                    pgn = __ldg(a.table + trow + min(blk + 1, a.max_blocks - 1));
+                } else {
+                    kcur += a.part_bytes;
+                }
+            }
         };
         if (first_seg && !a.early_ok) griddepcontrol_wait();   // the preceding kernel wrote blocks
         if (lane == 0) {
@@ -524,7 +623,25 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
             griddepcontrol_wait();
             griddepcontrol_launch_dependents();       // the merge kernel may start launching
             first_seg = false;
-            if (FUSED && a.new_row >= 0) {
+            if constexpr (PAGED) {
+                // the fused append of a paged call: each sequence's own new row
+                constexpr int CPR = D * 2 / 16;
+                if (a.new_k != nullptr) {
+                    const long long nsl = (long long)a.n_seqs * a.Hkv;
+                    for (long long idx = cta * kThreads + tid; idx < nsl * 2 * CPR;
+                         idx += (long long)gridDim.x * kThreads) {
+                        const long long sl = idx / (2 * CPR);
+                        const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
+                        const int si = (int)(sl / a.Hkv), h2 = (int)(sl % a.Hkv);
+                        const int nr = a.seqs[si].new_row;
+                        if (nr < 0) continue;
+                        const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
+                        uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
+                        const long long drow = ((long long)a.seqs[si].seq * a.Hkv + h2) * a.R + nr;
+                        reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + drow * D)[c16] = *src;
+                    }
+                }
+            } else if (FUSED && a.new_row >= 0) {
                 // the fused append: store every slot's new row in the cache, 16
                 // bytes a thread over the grid (this call reads that row from the
                 // inputs, never from the cache)
@@ -695,15 +812,15 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
         const int rw = (r1 - r0 + kWarps - 1) / kWarps;
         const int rb = min(r0 + warp * rw, r1), re = min(rb + rw, r1);
         if (rb < re) {
-            const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + slot * a.R * D;
-            const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + slot * a.R * D;
-            const int n = a.n_resid;
+            const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + rslot * a.R * D;
+            const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + rslot * a.R * D;
+            const int n = n_res;
             // row rr of the residual: the fused append's token comes from its input
             auto krow = [&](int rr) {
-                return FUSED && rr == a.new_row ? a.new_k + slot * D : kr + (long long)rr * D;
+                return FUSED && rr == nrow ? a.new_k + islot * D : kr + (long long)rr * D;
             };
             auto vrow = [&](int rr) {
-                return FUSED && rr == a.new_row ? a.new_v + slot * D : vr + (long long)rr * D;
+                return FUSED && rr == nrow ? a.new_v + islot * D : vr + (long long)rr * D;
             };
             build_q_frags<C, D, NQ>(nullptr, qf, qh_s, ql_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
             for (int rp = rb; rp < re; ++rp) {
@@ -788,6 +905,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
         lt += __shfl_xor_sync(kFull, lt, 16);
         if (g == 0 && i < NQ) { red_m[warp][i] = m; red_l[warp][i] = lt; }
         if (status && lane == 0) atomicOr(&red_status, status);
+        if (PAGED && bad_page) atomicOr(&red_status, 2u);
         if (i == 0 && !lo_col && col_ok) {
 #pragma unroll
             for (int f = 0; f < NBF; ++f) red_z[warp][hP][f * GB + jP] = zeta[f];
@@ -822,24 +940,15 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value) decode_mma_ke
             pw[4 + c] = acc;
         }
         __syncthreads();                               // qf and red_* are reused by the next segment
-        pos = u1 >= NU ? (slot + 1) * wm.Ws : slot * wm.Ws + unit_start(wm, u1);
+        pos = u1 >= NU ? w0 + Ws : w0 + unit_start_p(P, wm.wq, wm.wr, u1);
     }
 }
 
-// One CTA (D threads) per (batch, query head): log-sum-exp merge of the
-// partials of the head's kv slot -> fp16 output.  A partial whose status is
-// set (a cache copy timed out) makes the output NaN.
+// Log-sum-exp merge of nparts partials at base into out[c] (thread c).  A
+// partial whose status is set (a cache copy timed out, a bad table entry)
+// makes the output NaN.
 template <int D>
-__global__ void __launch_bounds__(D) finish_kernel(FinishArgs a) {
-    // launched as a programmatic dependent of the main kernel: wait until its
-    // partial results are complete and visible
-    griddepcontrol_wait();
-    griddepcontrol_launch_dependents();   // the next decode call may start its prologue
-    const int c = threadIdx.x;
-    const long long bh = blockIdx.x;
-    const long long slot = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.nq;
-    const int nparts = slot_parts(a.wm, slot);
-    const float* base = a.ws + bh * kPartialSlots * partial_stride(D);
+__device__ __forceinline__ void merge_partials(const float* base, int nparts, __half* out, int c) {
     float M = -INFINITY;
     bool failed = false;
     for (int j = 0; j < nparts; ++j) {
@@ -854,7 +963,36 @@ __global__ void __launch_bounds__(D) finish_kernel(FinishArgs a) {
         lsum = fmaf(ps[1], e, lsum);
         acc = fmaf(ps[4 + c], e, acc);
     }
-    a.out[bh * D + c] = failed ? __float2half_rn(NAN) : __float2half_rn(acc / lsum);
+    out[c] = failed ? __float2half_rn(NAN) : __float2half_rn(acc / lsum);
+}
+
+// One CTA (D threads) per (batch, query head): merge of the partials of the
+// head's kv slot -> fp16 output.
+template <int D>
+__global__ void __launch_bounds__(D) finish_kernel(FinishArgs a) {
+    // launched as a programmatic dependent of the main kernel: wait until its
+    // partial results are complete and visible
+    griddepcontrol_wait();
+    griddepcontrol_launch_dependents();   // the next decode call may start its prologue
+    const long long bh = blockIdx.x;
+    const long long slot = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.nq;
+    merge_partials<D>(a.ws + bh * kPartialSlots * partial_stride(D), slot_parts(a.wm, slot), a.out + bh * D,
+                      threadIdx.x);
+}
+
+// The same for a paged call: one CTA per (call sequence, query head).
+template <int D>
+__global__ void __launch_bounds__(D) finish_paged_kernel(const __grid_constant__ PagedFinishArgs a) {
+    griddepcontrol_wait();
+    griddepcontrol_launch_dependents();
+    const long long bh = blockIdx.x;
+    const int i = (int)(bh / a.Hq), hk = (int)((bh % a.Hq) / a.nq);
+    const PagedSeq& sq = a.seqs[i];
+    const long long P = sq.P, PR = (sq.n_resid + 31) / 32;
+    const long long w0 = sq.start + hk * (P * a.wm.wq + PR * a.wm.wr);
+    const long long last = w0 + unit_start_p(P, a.wm.wq, a.wm.wr, P + PR - 1);
+    const int nparts = (int)(map_owner(a.wm, last) - map_owner(a.wm, w0) + 1);
+    merge_partials<D>(a.ws + bh * kPartialSlots * partial_stride(D), nparts, a.out + bh * D, threadIdx.x);
 }
 
 }  // namespace mma_detail

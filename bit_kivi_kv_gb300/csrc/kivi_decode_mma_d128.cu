@@ -4,7 +4,7 @@
 namespace kivi {
 
 cudaError_t launch_decode_mma_d128(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st) {
-    return mma_launch::dispatch<128, false>(a, bits, nq, G, num_sms, st);
+    return mma_launch::dispatch<128, mma_detail::kModePlain>(a, bits, nq, G, num_sms, st);
 }
 
 }  // namespace kivi

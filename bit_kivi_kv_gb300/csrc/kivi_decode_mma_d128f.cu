@@ -4,7 +4,7 @@
 namespace kivi {
 
 cudaError_t launch_decode_mma_d128f(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st) {
-    return mma_launch::dispatch<128, true>(a, bits, nq, G, num_sms, st);
+    return mma_launch::dispatch<128, mma_detail::kModeFused>(a, bits, nq, G, num_sms, st);
 }
 
 }  // namespace kivi

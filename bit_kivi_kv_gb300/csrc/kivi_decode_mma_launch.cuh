@@ -8,22 +8,23 @@
 namespace kivi {
 namespace mma_launch {
 
-template <int D, int BB, int NN, int GG, bool FUSED>
-cudaError_t launch_one(mma_detail::Args& a, int num_sms, cudaStream_t st) {
+template <int D, int BB, int NN, int GG, int MODE>
+cudaError_t launch_one(typename mma_detail::ArgsOf<MODE>::type& a, int num_sms, cudaStream_t st) {
     using namespace mma_detail;
     using C = Cfg<D, BB, NN, GG>;
     // opt in to the dynamic shared memory of the copy ring and size the
     // persistent grid from the occupancy, once per instance
     static int per_sm = -1;
     static cudaError_t init = [] {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BB, NN, GG, FUSED>,
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BB, NN, GG, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BB, NN, GG, FUSED>,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BB, NN, GG, MODE>,
                                                               kThreads, C::DYN_SMEM);
         return e;
     }();
     if (init != cudaSuccess) return init;
+    // slots of the largest weight (paged calls: wm.Ws is the largest slot's)
     const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;
     long long n = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
     const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
@@ -43,14 +44,15 @@ cudaError_t launch_one(mma_detail::Args& a, int num_sms, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, decode_mma_kernel<D, BB, NN, GG, FUSED>, a);
+    return cudaLaunchKernelEx(&lc, decode_mma_kernel<D, BB, NN, GG, MODE>, a);
 }
 
 // every (bits, q heads per kv head, G) instance of head_dim D
-template <int D, bool FUSED>
-cudaError_t dispatch(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st) {
+template <int D, int MODE>
+cudaError_t dispatch(typename mma_detail::ArgsOf<MODE>::type& a, int bits, int nq, int G, int num_sms,
+                     cudaStream_t st) {
 #define KIVI_MMA(BB, NN, GG) \
-    if (bits == BB && nq == NN && G == GG) return launch_one<D, BB, NN, GG, FUSED>(a, num_sms, st);
+    if (bits == BB && nq == NN && G == GG) return launch_one<D, BB, NN, GG, MODE>(a, num_sms, st);
 #define KIVI_MMA_G(BB, NN) KIVI_MMA(BB, NN, 32) KIVI_MMA(BB, NN, 64) if constexpr (D >= 128) { KIVI_MMA(BB, NN, 128) }
     KIVI_MMA_G(2, 1) KIVI_MMA_G(2, 2) KIVI_MMA_G(2, 4)
     KIVI_MMA_G(4, 1) KIVI_MMA_G(4, 2) KIVI_MMA_G(4, 4)

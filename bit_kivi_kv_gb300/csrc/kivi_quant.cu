@@ -63,14 +63,32 @@ struct QuantArgs {
     int G;
 };
 
+// Paged form: CTA (j, h) quantizes job j's block of kv head h into its page.
+struct PagedQuantArgs {
+    uint8_t* pool;
+    int* table;
+    const __half* src_k;
+    const __half* src_v;
+    long long src_head_elems;
+    long long part_bytes, tile_bytes;
+    int Hkv, G;
+    QJob jobs[kMaxQJobs];
+};
+
+template <bool PAGED>
+struct QuantArgsOf { using type = QuantArgs; };
+template <>
+struct QuantArgsOf<true> { using type = PagedQuantArgs; };
+
 // One CTA quantizes one block (G tokens x D channels) of keys and of values.
 // The block's rows are staged in shared memory with a stride of D + 8 halves,
 // so lanes reading one channel of different tokens hit different banks.  A
 // thread packs the same word position of every 16-token tile, so the
 // coordinates of its codes (and, for keys, their steps and zeros) are fixed
 // once per block.
-template <int D, int BITS>
-__global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArgs a) {
+template <int D, int BITS, bool PAGED>
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_blocks_kernel(const __grid_constant__ typename QuantArgsOf<PAGED>::type a) {
     constexpr int L = (1 << BITS) - 1;
     constexpr int W = D * BITS / 64;        // words per lane per tile
     constexpr int PER = 16 / BITS;          // code pairs per word
@@ -84,13 +102,31 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
     float4* szr = reinterpret_cast<float4*>(xs + G * DP);
 
     const int tid = threadIdx.x;
-    const long long slot = blockIdx.y;
-    const long long j = blockIdx.x;
-    uint8_t* part_k = a.cache + slot * a.slot_bytes + (a.first_block + j) * a.part_bytes;
-    uint8_t* part_v = part_k + a.NB * a.part_bytes;
+    const __half* blk_k;   // the block's G rows of keys / values
+    const __half* blk_v;
+    uint8_t* part_k;
+    uint8_t* part_v;
+    if constexpr (PAGED) {
+        const QJob& jb = a.jobs[blockIdx.x];
+        const int h = blockIdx.y;
+        const long long off = jb.src_off + h * a.src_head_elems;
+        blk_k = a.src_k + off;
+        blk_v = a.src_v + off;
+        part_k = a.pool + ((long long)jb.page * a.Hkv + h) * 2 * a.part_bytes;
+        part_v = part_k + a.part_bytes;
+        if (h == 0 && tid == 0) a.table[jb.tbl_idx] = jb.page;
+    } else {
+        const long long slot = blockIdx.y;
+        const long long j = blockIdx.x;
+        const long long off = slot * a.src_slot_elems + j * G * D;
+        blk_k = a.src_k + off;
+        blk_v = a.src_v + off;
+        part_k = a.cache + slot * a.slot_bytes + (a.first_block + j) * a.part_bytes;
+        part_v = part_k + a.NB * a.part_bytes;
+    }
     const long long tiles_bytes = (long long)TPB * a.tile_bytes;
     auto stage_rows = [&](const __half* src) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + slot * a.src_slot_elems + j * G * D);
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
         for (int v = tid; v < G * D / 8; v += kQuantThreads) {
             const int row = v / (D / 8), c8 = v - row * (D / 8);
             *reinterpret_cast<uint4*>(xs + row * DP + 8 * c8) = s4[v];
@@ -98,7 +134,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
     };
 
     // ---------------- keys: per channel over the block's G tokens ----------------
-    stage_rows(a.src_k);
+    stage_rows(blk_k);
     __syncthreads();
     // min / max of channel pairs (2cp, 2cp+1) over the G tokens on fp16 pairs (exact);
     // adjacent threads take alternate blocks of 4 tokens (rows 4 apart fall 16
@@ -153,7 +189,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_blocks_kernel(QuantArg
     __syncthreads();
 
     // ---------------- values: per token over groups of G channels ----------------
-    stage_rows(a.src_v);
+    stage_rows(blk_v);
     __syncthreads();
     const int ngrp = D / G;                 // channel groups per token; G * ngrp == D entries
     for (int e = tid; e < D; e += kQuantThreads) {
@@ -226,6 +262,19 @@ __global__ void __launch_bounds__(128) copy_rows_kernel(uint8_t* cache, const __
     }
 }
 
+template <bool PAGED>
+cudaError_t launch_q(const typename QuantArgsOf<PAGED>::type& a, const Geometry& g, dim3 grid, cudaStream_t st) {
+    const size_t smem = (size_t)g.G * (g.D + 8) * 2 + 16 * (size_t)g.D;   // staged rows + (step, 1/step, zero) per group
+#define KIVI_Q(DD, BB)                                                                          \
+    if (g.D == DD && g.bits == BB) {                                                            \
+        quantize_blocks_kernel<DD, BB, PAGED><<<grid, kQuantThreads, smem, st>>>(a);            \
+        return cudaGetLastError();                                                              \
+    }
+    KIVI_Q(128, 2) KIVI_Q(128, 4) KIVI_Q(128, 8) KIVI_Q(64, 2) KIVI_Q(64, 4) KIVI_Q(64, 8)
+#undef KIVI_Q
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_blocks(const Geometry& g, uint8_t* cache, const __half* src_k,
@@ -234,14 +283,40 @@ cudaError_t launch_quantize_blocks(const Geometry& g, uint8_t* cache, const __ha
     QuantArgs a{cache, src_k, src_v, src_slot_elems, first_block, g.NB, g.part_bytes,
                 g.slot_bytes, g.tile_bytes, g.G};
     const dim3 grid((unsigned)nblk, (unsigned)(g.B * g.Hkv));
-    const size_t smem = (size_t)g.G * (g.D + 8) * 2 + 16 * (size_t)g.D;   // staged rows + (step, 1/step, zero) per group
-    if (g.D == 128 && g.bits == 2) quantize_blocks_kernel<128, 2><<<grid, kQuantThreads, smem, st>>>(a);
-    else if (g.D == 128 && g.bits == 4) quantize_blocks_kernel<128, 4><<<grid, kQuantThreads, smem, st>>>(a);
-    else if (g.D == 64 && g.bits == 2) quantize_blocks_kernel<64, 2><<<grid, kQuantThreads, smem, st>>>(a);
-    else if (g.D == 64 && g.bits == 4) quantize_blocks_kernel<64, 4><<<grid, kQuantThreads, smem, st>>>(a);
-    else if (g.D == 128 && g.bits == 8) quantize_blocks_kernel<128, 8><<<grid, kQuantThreads, smem, st>>>(a);
-    else if (g.D == 64 && g.bits == 8) quantize_blocks_kernel<64, 8><<<grid, kQuantThreads, smem, st>>>(a);
-    else return cudaErrorInvalidValue;
+    return launch_q<false>(a, g, grid, st);
+}
+
+cudaError_t launch_quantize_pages(const PagedGeometry& pg, uint8_t* buf, const __half* src_k,
+                                  const __half* src_v, long long src_head_elems, const QJob* jobs,
+                                  int njobs, cudaStream_t st, int* launches) {
+    const Geometry& g = pg.g;
+    PagedQuantArgs a;          // ~16 KB of kernel parameters
+    a.pool = buf;
+    a.table = reinterpret_cast<int*>(buf + pg.table_off);
+    a.src_k = src_k;
+    a.src_v = src_v;
+    a.src_head_elems = src_head_elems;
+    a.part_bytes = g.part_bytes;
+    a.tile_bytes = g.tile_bytes;
+    a.Hkv = g.Hkv;
+    a.G = g.G;
+    *launches = 0;
+    for (int j0 = 0; j0 < njobs; j0 += kMaxQJobs) {
+        const int nj = njobs - j0 < kMaxQJobs ? njobs - j0 : kMaxQJobs;
+        for (int j = 0; j < nj; ++j) a.jobs[j] = jobs[j0 + j];
+        const cudaError_t e = launch_q<true>(a, g, dim3((unsigned)nj, (unsigned)g.Hkv), st);
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_copy_rows_slots(const Geometry& g, uint8_t* cache, const __half* src_k,
+                                   const __half* src_v, long long src_slot_elems, long long first_slot,
+                                   int nslots, int row0, int nrows, cudaStream_t st) {
+    const long long skip = first_slot * g.resid_slot_bytes;
+    copy_rows_kernel<<<nslots, 128, 0, st>>>(cache, src_k, src_v, src_slot_elems, g.k_resid_off + skip,
+                                             g.v_resid_off + skip, g.resid_slot_bytes, g.D, row0, nrows);
     return cudaGetLastError();
 }
 

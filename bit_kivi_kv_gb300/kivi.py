@@ -31,6 +31,22 @@ class kivi_layout(ctypes.Structure):
                 ("v_resid_offset", ctypes.c_size_t), ("resid_slot_bytes", ctypes.c_size_t)]
 
 
+class kivi_paged_config(ctypes.Structure):
+    _fields_ = [("max_seqs", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("bits", ctypes.c_int), ("group", ctypes.c_int),
+                ("residual", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int), ("n_pages", ctypes.c_longlong)]
+
+
+class kivi_paged_layout(ctypes.Structure):
+    _fields_ = [("total_bytes", ctypes.c_size_t), ("tile_bytes", ctypes.c_size_t),
+                ("part_bytes", ctypes.c_size_t), ("page_bytes", ctypes.c_size_t),
+                ("k_resid_offset", ctypes.c_size_t), ("v_resid_offset", ctypes.c_size_t),
+                ("resid_seq_bytes", ctypes.c_size_t), ("table_offset", ctypes.c_size_t)]
+
+
+KIVI_PAGED_MAX_CALL_SEQS = 512
+
+
 class KiviError(RuntimeError):
     def __init__(self, status: int, message: str):
         self.status = status
@@ -43,6 +59,8 @@ def _load():
     lib = ctypes.CDLL(_LIB_PATH)
     P, SZ, LL, I, F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_longlong, ctypes.c_int, ctypes.c_float
     cfgp = ctypes.POINTER(kivi_config)
+    pcfgp = ctypes.POINTER(kivi_paged_config)
+    IP = ctypes.POINTER(ctypes.c_int)
     sigs = {
         "kivi_cache_bytes": (SZ, [cfgp]),
         "kivi_cache_layout": (I, [cfgp, ctypes.POINTER(kivi_layout)]),
@@ -59,6 +77,17 @@ def _load():
         "kivi_launch_count": (ctypes.c_ulonglong, []),
         "kivi_cache_set_decode_kernel": (I, [P, I]),
         "kivi_decode_attn_static_ws": (I, [P, P, P, F, P]),
+        "kivi_paged_bytes": (SZ, [pcfgp]),
+        "kivi_paged_cache_layout": (I, [pcfgp, ctypes.POINTER(kivi_paged_layout)]),
+        "kivi_paged_create": (I, [pcfgp, P, SZ, ctypes.POINTER(P)]),
+        "kivi_paged_destroy": (I, [P]),
+        "kivi_paged_add": (I, [P, P, P, LL, P, IP]),
+        "kivi_paged_release": (I, [P, I]),
+        "kivi_paged_seq_counts": (I, [P, I, ctypes.POINTER(LL), ctypes.POINTER(LL)]),
+        "kivi_paged_seq_pages": (I, [P, I, IP, I, IP]),
+        "kivi_paged_free": (I, [P, ctypes.POINTER(LL), IP]),
+        "kivi_paged_workspace_bytes": (SZ, [pcfgp, I]),
+        "kivi_paged_append_decode": (I, [P, IP, I, P, P, P, P, F, P, SZ, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -142,6 +171,74 @@ def kivi_cache_set_decode_kernel(h: int, kernel: int):
     _check(lib.kivi_cache_set_decode_kernel(h, kernel))
 
 
+# ---- paged cache ----------------------------------------------------------------
+def make_paged_config(max_seqs, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_blocks_per_seq,
+                      n_pages) -> kivi_paged_config:
+    return kivi_paged_config(max_seqs, n_q_heads, n_kv_heads, head_dim, bits, group, residual,
+                             max_blocks_per_seq, n_pages)
+
+
+def kivi_paged_bytes(cfg: kivi_paged_config) -> int:
+    return lib.kivi_paged_bytes(ctypes.byref(cfg))
+
+
+def kivi_paged_cache_layout(cfg: kivi_paged_config) -> kivi_paged_layout:
+    out = kivi_paged_layout()
+    _check(lib.kivi_paged_cache_layout(ctypes.byref(cfg), ctypes.byref(out)))
+    return out
+
+
+def kivi_paged_create(cfg: kivi_paged_config, dev_buf: int, nbytes: int) -> int:
+    h = ctypes.c_void_p()
+    _check(lib.kivi_paged_create(ctypes.byref(cfg), dev_buf, nbytes, ctypes.byref(h)))
+    return h.value
+
+
+def kivi_paged_destroy(h: int):
+    _check(lib.kivi_paged_destroy(h))
+
+
+def kivi_paged_add(h: int, K: int, V: int, L: int, stream: int) -> int:
+    s = ctypes.c_int()
+    _check(lib.kivi_paged_add(h, K, V, L, stream, ctypes.byref(s)))
+    return s.value
+
+
+def kivi_paged_release(h: int, seq: int):
+    _check(lib.kivi_paged_release(h, seq))
+
+
+def kivi_paged_seq_counts(h: int, seq: int):
+    a, b = ctypes.c_longlong(), ctypes.c_longlong()
+    _check(lib.kivi_paged_seq_counts(h, seq, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def kivi_paged_seq_pages(h: int, seq: int) -> list:
+    n = ctypes.c_int()
+    _check(lib.kivi_paged_seq_pages(h, seq, None, 0, ctypes.byref(n)))
+    buf = (ctypes.c_int * max(n.value, 1))()
+    _check(lib.kivi_paged_seq_pages(h, seq, buf, n.value, ctypes.byref(n)))
+    return list(buf[:n.value])
+
+
+def kivi_paged_free(h: int):
+    a, b = ctypes.c_longlong(), ctypes.c_int()
+    _check(lib.kivi_paged_free(h, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def kivi_paged_workspace_bytes(cfg: kivi_paged_config, n: int) -> int:
+    return lib.kivi_paged_workspace_bytes(ctypes.byref(cfg), n)
+
+
+def kivi_paged_append_decode(h: int, seqs, k: int, v: int, q: int, out: int, softmax_scale: float,
+                             workspace: int, ws_bytes: int, stream: int):
+    arr = (ctypes.c_int * max(len(seqs), 1))(*seqs)
+    _check(lib.kivi_paged_append_decode(h, arr, len(seqs), k, v, q, out, softmax_scale, workspace, ws_bytes,
+                                        stream))
+
+
 def kivi_last_error_string() -> str:
     return lib.kivi_last_error_string().decode()
 
@@ -213,4 +310,60 @@ class KiviCache:
             out = torch.empty_like(q)
         kivi_append_decode(self.handle, self._ptr(k), self._ptr(v), self._ptr(q), self._ptr(out), softmax_scale,
                            self.workspace.data_ptr(), self.workspace.numel(), self._stream(stream))
+        return out
+
+
+class KiviPagedCache:
+    """A paged cache for ragged sequences: a torch-owned device buffer (page pool,
+    residual rows, block table) plus the library handle."""
+
+    def __init__(self, max_seqs, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_blocks_per_seq,
+                 n_pages, device="cuda"):
+        import torch
+        self.cfg = make_paged_config(max_seqs, n_q_heads, n_kv_heads, head_dim, bits, group, residual,
+                                     max_blocks_per_seq, n_pages)
+        nbytes = kivi_paged_bytes(self.cfg)
+        if nbytes == 0:
+            raise KiviError(KIVI_ERR_INVALID_ARG, kivi_last_error_string())
+        self.layout = kivi_paged_cache_layout(self.cfg)
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.workspace = torch.empty(kivi_paged_workspace_bytes(self.cfg, min(max_seqs, KIVI_PAGED_MAX_CALL_SEQS)),
+                                     dtype=torch.uint8, device=device)
+        self.handle = kivi_paged_create(self.cfg, self.buffer.data_ptr(), nbytes)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            lib.kivi_paged_destroy(h)
+            self.handle = None
+
+    def add(self, K, V, stream=None) -> int:
+        """New sequence with prompt K, V [Hkv][L][D] fp16; returns its id."""
+        L = K.shape[1]
+        return kivi_paged_add(self.handle, KiviCache._ptr(K) if L else 0, KiviCache._ptr(V) if L else 0, L,
+                              KiviCache._stream(stream))
+
+    def release(self, seq: int):
+        kivi_paged_release(self.handle, seq)
+
+    def counts(self, seq: int):
+        return kivi_paged_seq_counts(self.handle, seq)
+
+    def pages(self, seq: int) -> list:
+        return kivi_paged_seq_pages(self.handle, seq)
+
+    def free(self):
+        return kivi_paged_free(self.handle)
+
+    def append_decode(self, seqs, k, v, q, out=None, softmax_scale=0.0, stream=None):
+        """For each listed sequence: append k[i], v[i] ([n][Hkv][D]; both None: no
+        append), then decode q[i] ([n][Hq][D]) into out[i]."""
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        kp = KiviCache._ptr(k) if k is not None else 0
+        vp = KiviCache._ptr(v) if v is not None else 0
+        kivi_paged_append_decode(self.handle, list(seqs), kp, vp, KiviCache._ptr(q), KiviCache._ptr(out),
+                                 softmax_scale, self.workspace.data_ptr(), self.workspace.numel(),
+                                 KiviCache._stream(stream))
         return out

@@ -260,6 +260,126 @@ kivi_status kivi_cache_set_decode_kernel(kivi_cache_t cache, int kernel);
 kivi_status kivi_decode_attn_static_ws(kivi_cache_t cache, const void* q, void* out,
                                        float softmax_scale, kivi_stream_t stream);
 
+/* ===================== Paged cache with ragged sequences =====================
+ *
+ * The same quantized cache for a changing set of sequences of different
+ * lengths, as a serving engine runs it: quantized blocks live in pages of a
+ * shared pool and each sequence has a block table (the explainer's pointer to
+ * PagedAttention, section 7; the method itself is unchanged).  Every sequence
+ * follows the streaming rule above on its own: Lq = G * ceil(max(L - R, 0) / G)
+ * after its prompt, a flush of its R residual tokens when an append finds
+ * r == R.
+ *
+ * A page holds one block (G tokens) of one sequence for every kv head:
+ *
+ *   pages   : [n_pages][Hkv][2][PART] at offset 0; index 2: 0 = keys, 1 = values
+ *             (each part exactly as in a block of the dense cache above)
+ *   k_resid : [max_seqs][Hkv][R][D] fp16 at k_resid_offset
+ *   v_resid : [max_seqs][Hkv][R][D] fp16 at v_resid_offset
+ *   table   : [max_seqs][max_blocks_per_seq] int32 at table_offset; entry n of
+ *             row s is the page of block n of sequence s (tokens [n*G, (n+1)*G)),
+ *             valid for n < Lq / G
+ *
+ * Pages and sequence slots are handed out by an allocator on the host handle
+ * (free lists; a released sequence's pages are reused in any order).  The
+ * library writes table entries from its kernels when it fills a page; the
+ * host keeps its own copy, so no call reads device memory back.
+ *
+ * Conventions as for the dense cache (caller-owned device memory, stream
+ * ordering, errors before launch, no CPU fallback).
+ */
+typedef struct {
+    int max_seqs;             /* sequence slots */
+    int n_q_heads;
+    int n_kv_heads;
+    int head_dim;
+    int bits;
+    int group;
+    int residual;
+    int max_blocks_per_seq;   /* a sequence holds at most max_blocks_per_seq * group + residual tokens */
+    long long n_pages;        /* pages in the pool */
+} kivi_paged_config;
+
+typedef struct {
+    size_t total_bytes;       /* == kivi_paged_bytes() */
+    size_t tile_bytes;        /* TILE */
+    size_t part_bytes;        /* PART */
+    size_t page_bytes;        /* Hkv * 2 * PART */
+    size_t k_resid_offset;    /* 256-byte aligned */
+    size_t v_resid_offset;    /* 256-byte aligned */
+    size_t resid_seq_bytes;   /* Hkv * R * D * 2: one sequence's residual rows (keys or values) */
+    size_t table_offset;      /* 256-byte aligned */
+} kivi_paged_layout;
+
+typedef struct kivi_paged* kivi_paged_t;
+
+/* Most sequences one kivi_paged_append_decode call may take. */
+#define KIVI_PAGED_MAX_CALL_SEQS 512
+
+/* Bytes of device memory a paged cache of this shape needs; 0 if cfg is
+ * invalid.  The shape limits are those of the dense cache, plus max_seqs,
+ * max_blocks_per_seq and n_pages >= 1, n_pages < 2^31 and
+ * max_seqs * max_blocks_per_seq < 2^31.  Host-only. */
+size_t kivi_paged_bytes(const kivi_paged_config* cfg);
+
+/* Fill *out with the layout above.  Host-only. */
+kivi_status kivi_paged_cache_layout(const kivi_paged_config* cfg, kivi_paged_layout* out);
+
+/* Create a handle over the caller's device buffer (256-byte aligned, at least
+ * kivi_paged_bytes(cfg) bytes, no initialization needed): no sequences, every
+ * page free.  Host-only. */
+kivi_status kivi_paged_create(const kivi_paged_config* cfg, void* dev_buf, size_t bytes,
+                              kivi_paged_t* out);
+
+/* Free the host handle (not the buffer). */
+kivi_status kivi_paged_destroy(kivi_paged_t cache);
+
+/*
+ * Add a sequence with a prompt of L >= 0 tokens: K, V fp16 [Hkv][L][D] device
+ * tensors (may be NULL when L == 0).  Takes a free sequence slot (its id is
+ * written to *seq) and ceil(Lq / G) pages, quantizes tokens [0, Lq) into
+ * them and copies [Lq, L) into the sequence's residual rows, as kivi_prefill
+ * does for one batch row.  KIVI_ERR_CAPACITY when no slot is free, the pool
+ * has too few free pages, or Lq / G > max_blocks_per_seq.
+ */
+kivi_status kivi_paged_add(kivi_paged_t cache, const void* K, const void* V, long long L,
+                           kivi_stream_t stream, int* seq);
+
+/* Release a sequence: its slot and pages return to the free lists (host only,
+ * no device work; work already enqueued that reads them must finish before the
+ * next call that reuses them is enqueued on another stream). */
+kivi_status kivi_paged_release(kivi_paged_t cache, int seq);
+
+/* Token counts of one live sequence. */
+kivi_status kivi_paged_seq_counts(kivi_paged_t cache, int seq, long long* n_quant, long long* n_resid);
+
+/* The pages of a live sequence's blocks, in block order: writes
+ * min(count, cap) entries to pages[] and the count to *n. */
+kivi_status kivi_paged_seq_pages(kivi_paged_t cache, int seq, int* pages, int cap, int* n);
+
+/* Free pages and free sequence slots. */
+kivi_status kivi_paged_free(kivi_paged_t cache, long long* free_pages, int* free_seqs);
+
+/* Workspace bytes of a call over n sequences (n <= KIVI_PAGED_MAX_CALL_SEQS);
+ * 0 if cfg or n is invalid.  Host-only. */
+size_t kivi_paged_workspace_bytes(const kivi_paged_config* cfg, int n);
+
+/*
+ * For each of the n distinct live sequences seqs[0..n-1] (host array): append
+ * token k[i], v[i] (fp16 [n][Hkv][D]) with the flush rule above, then decode
+ * attention of q[i] (fp16 [n][Hq][D]) over that sequence's cached tokens into
+ * out[i] (fp16 [n][Hq][D]).  k and v both NULL: decode only, no append (a
+ * sequence must then hold a token).  softmax_scale and workspace as for
+ * kivi_decode_attn (ws_bytes >= kivi_paged_workspace_bytes(cfg, n)).  Runs on
+ * the tensor-core kernel (one decode launch and one merge launch, plus one
+ * quantize launch when a sequence flushes).  KIVI_ERR_CAPACITY when a flush
+ * needs more free pages than the pool has or a sequence is full; every check
+ * runs before anything is launched or allocated.
+ */
+kivi_status kivi_paged_append_decode(kivi_paged_t cache, const int* seqs, int n, const void* k,
+                                     const void* v, const void* q, void* out, float softmax_scale,
+                                     void* workspace, size_t ws_bytes, kivi_stream_t stream);
+
 /* Description of the last failure on the calling thread ("" if none). */
 const char* kivi_last_error_string(void);
 

@@ -113,3 +113,94 @@ def test_oracle_is_not_imported_by_the_library():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in re.findall(r"^\s*(?:from|import)\s+(\w+)", text, flags=re.M), f
+
+
+def test_paged_config_and_layout(K):
+    cfg = K.make_paged_config(4, 32, 32, 128, 2, 32, 128, 16, 64)
+    lay = K.kivi_paged_cache_layout(cfg)
+    assert (lay.tile_bytes, lay.part_bytes) == (512, 1536)
+    assert lay.page_bytes == 32 * 2 * 1536
+    assert lay.k_resid_offset == 64 * lay.page_bytes                     # 256-aligned already
+    assert lay.resid_seq_bytes == 32 * 128 * 128 * 2
+    assert lay.v_resid_offset == lay.k_resid_offset + 4 * lay.resid_seq_bytes
+    assert lay.table_offset == lay.v_resid_offset + 4 * lay.resid_seq_bytes
+    assert lay.total_bytes == lay.table_offset + 4 * 16 * 4 == K.kivi_paged_bytes(cfg)
+    assert K.kivi_paged_workspace_bytes(cfg, 3) == 3 * 32 * 65 * 132 * 4
+    assert K.kivi_paged_workspace_bytes(cfg, 0) == 0
+    assert K.kivi_paged_workspace_bytes(cfg, K.KIVI_PAGED_MAX_CALL_SEQS + 1) == 0
+    bad = [K.make_paged_config(0, 32, 32, 128, 2, 32, 128, 16, 64),     # max_seqs
+           K.make_paged_config(4, 32, 32, 128, 2, 32, 128, 0, 64),      # max_blocks_per_seq
+           K.make_paged_config(4, 32, 32, 128, 2, 32, 128, 16, 0),      # n_pages
+           K.make_paged_config(4, 32, 32, 128, 2, 32, 128, 16, 1 << 31),
+           K.make_paged_config(4, 32, 32, 128, 3, 32, 128, 16, 64),     # bits
+           K.make_paged_config(4, 32, 32, 128, 2, 32, 100, 16, 64)]     # residual % group
+    for c in bad:
+        assert K.kivi_paged_bytes(c) == 0
+        assert K.kivi_last_error_string()
+
+
+def test_paged_allocator_and_checks_without_gpu(K):
+    """Sequence slots and pages come from host free lists; every check of
+    add / append_decode runs before any launch, so failures leave the state as
+    it was (fake device pointers are never dereferenced)."""
+    cfg = K.make_paged_config(3, 2, 2, 64, 2, 32, 32, 4, 6)
+    n = K.kivi_paged_bytes(cfg)
+    fake = 1 << 20
+    with pytest.raises(K.KiviError) as e:
+        K.kivi_paged_create(cfg, fake + 16, n)
+    assert e.value.status == K.KIVI_ERR_INVALID_ARG
+    with pytest.raises(K.KiviError) as e:
+        K.kivi_paged_create(cfg, fake, n - 1)
+    assert e.value.status == K.KIVI_ERR_CAPACITY
+    h = K.kivi_paged_create(cfg, fake, n)
+    try:
+        assert K.kivi_paged_free(h) == (6, 3)
+        # empty prompts: no launch; slots handed out 0, 1, 2
+        seqs = [K.kivi_paged_add(h, 0, 0, 0, 0) for _ in range(3)]
+        assert seqs == [0, 1, 2] and K.kivi_paged_free(h) == (6, 0)
+        assert K.kivi_paged_seq_counts(h, 1) == (0, 0) and K.kivi_paged_seq_pages(h, 1) == []
+        with pytest.raises(K.KiviError) as e:          # no free slot
+            K.kivi_paged_add(h, 0, 0, 0, 0)
+        assert e.value.status == K.KIVI_ERR_CAPACITY
+        K.kivi_paged_release(h, 1)
+        assert K.kivi_paged_free(h) == (6, 1)
+        with pytest.raises(K.KiviError) as e:          # released twice
+            K.kivi_paged_release(h, 1)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
+        for bad in (-1, 3, 1):                          # out of range, out of range, not live
+            with pytest.raises(K.KiviError) as e:
+                K.kivi_paged_seq_counts(h, bad)
+            assert e.value.status == K.KIVI_ERR_INVALID_ARG
+        # a prompt of 4*32 + 32 + 1 tokens needs 5 blocks > max_blocks_per_seq 4
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_paged_add(h, fake, fake, 161, 0)
+        assert e.value.status == K.KIVI_ERR_CAPACITY
+        with pytest.raises(K.KiviError) as e:          # misaligned prompt
+            K.kivi_paged_add(h, fake + 8, fake, 10, 0)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
+        with pytest.raises(K.KiviError) as e:          # null prompt with L > 0
+            K.kivi_paged_add(h, 0, 0, 10, 0)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
+        assert K.kivi_paged_free(h) == (6, 1)
+        ws = K.kivi_paged_workspace_bytes(cfg, 2)
+        ad = K.kivi_paged_append_decode
+        cases = [(([0, 0], fake, fake, fake, fake, 0.0, fake, ws), K.KIVI_ERR_INVALID_ARG),   # listed twice
+                 (([0, 1], fake, fake, fake, fake, 0.0, fake, ws), K.KIVI_ERR_INVALID_ARG),   # 1 is not live
+                 (([], fake, fake, fake, fake, 0.0, fake, ws), K.KIVI_ERR_INVALID_ARG),       # n = 0
+                 (([0, 2], fake, 0, fake, fake, 0.0, fake, ws), K.KIVI_ERR_INVALID_ARG),      # k without v
+                 (([0, 2], fake + 8, fake + 8, fake, fake, 0.0, fake, ws), K.KIVI_ERR_INVALID_ARG),
+                 (([0, 2], fake, fake, fake, fake, 0.0, fake + 64, ws), K.KIVI_ERR_INVALID_ARG),
+                 (([0, 2], fake, fake, fake, fake, float("inf"), fake, ws), K.KIVI_ERR_INVALID_ARG),
+                 (([0, 2], fake, fake, fake, fake, 0.0, fake, ws - 1), K.KIVI_ERR_CAPACITY),
+                 (([0, 2], 0, 0, fake, fake, 0.0, fake, ws), K.KIVI_ERR_STATE)]           # decode only, empty
+        for args, status in cases:
+            with pytest.raises(K.KiviError) as e:
+                ad(h, *args, 0)
+            assert e.value.status == status, (args, e.value.status, K.kivi_last_error_string())
+        with pytest.raises(K.KiviError) as e:          # more than KIVI_PAGED_MAX_CALL_SEQS sequences
+            ad(h, [0] * (K.KIVI_PAGED_MAX_CALL_SEQS + 1), fake, fake, fake, fake, 0.0, fake, 1 << 40, 0)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
+        assert K.kivi_paged_free(h) == (6, 1)
+        assert K.kivi_paged_seq_counts(h, 0) == (0, 0)
+    finally:
+        K.kivi_paged_destroy(h)
