@@ -50,6 +50,10 @@ WORKLOADS = {
                           layers=2, outliers="range", sink=True, seed=1003),
     "llama2-7b-layer-8bit": dict(B=8, Hq=32, Hkv=32, D=128, bits=8, G=32, R=128, prompt=4096, decode=64,
                                  layers=4, outliers="range", sink=True, seed=1005),
+    # the 7B layer with ragged prompts (mean 4096) on the paged cache
+    "llama2-7b-ragged": dict(B=8, Hq=32, Hkv=32, D=128, bits=2, G=32, R=128, prompt=4096,
+                             lengths=[512, 1536, 2560, 3584, 4608, 5632, 6656, 7680], decode=64,
+                             layers=4, outliers="range", sink=True, seed=1006, paged=True),
     "long-context": dict(B=2, Hq=32, Hkv=32, D=128, bits=2, G=32, R=128, prompt=131072, decode=512,
                          layers=1, outliers="range", sink=True, seed=1004),
 }
@@ -70,9 +74,15 @@ def _prefill_split(L, G, R):
     return Lq, L - Lq
 
 
-def _call_counts(w):
-    """Per decode call: (n_quant, n_resid) after its append, for one layer."""
-    Lq, r = _prefill_split(w["prompt"], w["G"], w["R"])
+def _lengths(w):
+    """Prompt length of each batch row (sequence)."""
+    return list(w.get("lengths") or [w["prompt"]] * w["B"])
+
+
+def _call_counts(w, L=None):
+    """Per decode call: (n_quant, n_resid) after its append, for one sequence
+    of prompt L (default: the workload's prompt)."""
+    Lq, r = _prefill_split(w["prompt"] if L is None else L, w["G"], w["R"])
     out = []
     for _ in range(w["decode"]):
         if r == w["R"]:
@@ -82,13 +92,24 @@ def _call_counts(w):
     return out
 
 
-def _bytes_per_call(w, Lq, r):
+def _bytes_last_call(w):
+    """Algorithmic bytes of a decode call over the cache as the step leaves it:
+    codes + (step, zero) entries of every quantized token, fp16 residual rows,
+    the query and the output."""
     per_tok = 2 * (w["D"] * w["bits"] // 8) + 2 * (4 * w["D"] // w["G"])
-    return w["B"] * w["Hkv"] * (Lq * per_tok + r * 4 * w["D"]) + 2 * w["B"] * w["Hq"] * w["D"] * 2
+    kv = 0
+    for L in _lengths(w):
+        Lq, r = _call_counts(w, L)[-1]
+        kv += w["Hkv"] * (Lq * per_tok + r * 4 * w["D"])
+    return kv + 2 * w["B"] * w["Hq"] * w["D"] * 2
+
+
+def _tokens_last_call(w):
+    return sum(sum(_call_counts(w, L)[-1]) for L in _lengths(w))
 
 
 def _kv_tokens_per_step(w):
-    return w["layers"] * w["B"] * sum(Lq + r for Lq, r in _call_counts(w))
+    return w["layers"] * sum(Lq + r for L in _lengths(w) for Lq, r in _call_counts(w, L))
 
 
 # ---- N > 1: each rank runs its own replica of the workload (its own batch) ----
@@ -196,14 +217,16 @@ def oracle_sample(w, n_slots=None, budget_s=15.0, step_seed=0):
     outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
     syn = SynthKV(1, w["Hq"] // w["Hkv"], 1, w["D"], seed=w["seed"] + step_seed, outliers=outl,
                   sink=w["sink"], device="cpu")
-    K, V = syn.prompt(w["prompt"])
+    lengths = _lengths(w)
+    K, V = syn.prompt(max(lengths))
     Kn, Vn = K.numpy(), V.numpy()
     steps = [tuple(t.numpy() for t in syn.step(s)) for s in range(w["decode"])]
     t0 = time.perf_counter()
     done, tokens = 0, 0
     while True:
         oc = OracleCache(1, 1, w["D"], w["bits"], w["G"], w["R"])
-        oc.prefill(Kn, Vn)
+        L = lengths[(done + step_seed) % len(lengths)]     # ragged workloads: the rows' lengths in turn
+        oc.prefill(np.ascontiguousarray(Kn[:, :, :L]), np.ascontiguousarray(Vn[:, :, :L]))
         for (q, k, v) in steps:
             oc.append(k, v)
             decode_attention(q, oc.keys_hat(), oc.values_hat())
@@ -242,9 +265,14 @@ def run_reference(args, w):
 
 
 def _config(w, name):
-    return {"workload": name, "batch": w["B"], "q_heads": w["Hq"], "kv_heads": w["Hkv"],
-            "head_dim": w["D"], "bits": w["bits"], "group": w["G"], "residual": w["R"],
-            "prompt": w["prompt"], "decode_steps": w["decode"], "layers_rotated": w["layers"]}
+    c = {"workload": name, "batch": w["B"], "q_heads": w["Hq"], "kv_heads": w["Hkv"],
+         "head_dim": w["D"], "bits": w["bits"], "group": w["G"], "residual": w["R"],
+         "prompt": w["prompt"], "decode_steps": w["decode"], "layers_rotated": w["layers"]}
+    if w.get("lengths"):
+        c["prompt_lengths"] = list(w["lengths"])
+    if w.get("paged"):
+        c["cache"] = "paged (page pool + block tables)"
+    return c
 
 
 # --------------------------------------------------------------- GPU arm ----
@@ -266,34 +294,9 @@ def run_ours(args, w):
 
     outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
     NL, S = w["layers"], w["decode"]
-    max_tokens = w["prompt"] + S
-    caches, prompts, steps = [], [], []
-    for li in range(NL):
-        syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=replica_seed(w, li, rank),
-                      outliers=outl, sink=w["sink"], device=dev)
-        prompts.append(syn.prompt(w["prompt"]))
-        steps.append([syn.step(s) for s in range(S)])
-        caches.append(KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], max_tokens,
-                                device=dev))
-        caches[-1].set_decode_kernel(_KERNEL_IDS[args.decode_kernel])
-    outs = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
-
-    def step():
-        for li in range(NL):
-            caches[li].reset()
-            caches[li].prefill(*prompts[li])
-        for s in range(S):
-            for li in range(NL):
-                q, k, v = steps[li][s]
-                if args.separate_append:
-                    caches[li].append(k, v)
-                    caches[li].decode_attn(q, out=outs[li])
-                else:
-                    caches[li].append_decode(k, v, q, out=outs[li])
-
-    def decode_only():
-        for li in range(NL):
-            caches[li].decode_attn(steps[li][S - 1][0], out=outs[li])
+    paged = bool(w.get("paged") or args.paged)
+    eng = (_PagedEngine if paged else _DenseEngine)(args, w, dev, rank, outl, SynthKV, torch)
+    step, decode_only = eng.step, eng.decode_only
 
     # eager warm-up (also the first device query), then capture
     step()
@@ -351,14 +354,13 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     calls = reps * 8 * NL
     dec_ms = e0.elapsed_time(e1) / calls
-    Lq_last, r_last = _call_counts(w)[-1]
-    bytes_call = _bytes_per_call(w, Lq_last, r_last)
+    bytes_call = _bytes_last_call(w)
     achieved = bytes_call / (dec_ms / 1e3) / 1e9
     peak, peak_kind = _peaks()
-    traffic = _profile_traffic(args.workload)
+    traffic = _profile_traffic(args.workload + ("-paged" if paged and not w.get("paged") else ""))
 
     # ---- e2e through the Python API from pinned host memory ----
-    e2e = _e2e(args, w, caches, prompts, steps, torch, dev)
+    e2e = eng.e2e(max(3, min(args.steps, 10)))
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -366,16 +368,19 @@ def run_ours(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; key outlier channels, attention sink)",
         "config": dict(_config(w, args.workload), parallelism=f"replicas x{world}",
-                       step_calls="kivi_append + kivi_decode_attn" if args.separate_append else "kivi_append_decode",
+                       step_calls=("kivi_paged_add + kivi_paged_append_decode" if paged else
+                                   "kivi_append + kivi_decode_attn" if args.separate_append else
+                                   "kivi_append_decode"),
                        l2="inputs larger than L2: each step rotates layer caches "
                           f"({NL} x ~{bytes_call / 1e6:.0f} MB read per decode round)"),
         "decode_call": {"us": dec_ms * 1e3, "bytes": bytes_call, "gbs": achieved,
-                        "kv_tokens_per_s": w["B"] * (Lq_last + r_last) / (dec_ms / 1e3),
+                        "kv_tokens_per_s": _tokens_last_call(w) / (dec_ms / 1e3),
                         "steps_per_s": 1e3 / dec_ms},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "kernel": "decode attention call: " + (
-                         "decode_split_kernel + combine_kernel" if args.decode_kernel == "cuda-core"
+                         "decode_split_kernel + combine_kernel" if args.decode_kernel == "cuda-core" and not paged
+                         else "decode_mma_kernel (paged) + finish_paged_kernel (tensor cores)" if paged
                          else "decode_mma_kernel + finish_kernel (tensor cores)")},
         "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
     }
@@ -405,8 +410,9 @@ def _launches_in(step, K, stream, torch):
 def _decode_source_sha1():
     import hashlib
     h = hashlib.sha1()
-    for f in ("kivi_decode.cu", "kivi_common.cuh", "kivi_decode_mma.cuh", "kivi_decode_mma_d128.cu",
-              "kivi_decode_mma_d64.cu"):
+    for f in ("kivi_decode.cu", "kivi_common.cuh", "kivi_decode_mma.cuh", "kivi_decode_mma_launch.cuh",
+              "kivi_decode_mma_d128.cu", "kivi_decode_mma_d64.cu", "kivi_decode_mma_d128p.cu",
+              "kivi_decode_mma_d64p.cu"):
         with open(os.path.join(ROOT, "bit_kivi_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -425,67 +431,175 @@ def _profile_traffic(name):
 
 
 def run_profile(args, w):
-    """Small eager run for ncu: build the workload's caches, run one full step,
-    then a few more decode calls (no graphs, no e2e, no oracle)."""
+    """Small eager run for ncu: the bench's step on at most 2 layers (2 x decode
+    calls of decode kernels: appends + decodes), then profile_calls rounds of
+    decode-only calls at the state the step leaves (no graphs, e2e or oracle)."""
     import torch
     from bit_kivi_kv_gb300 import build as _b
     _b.build()
-    from bit_kivi_kv_gb300.kivi import KiviCache
     from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV
     dev = torch.device("cuda", 0)
     outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
-    NL, S = min(w["layers"], 2), w["decode"]
-    for li in range(NL):
-        syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=w["seed"] + 7919 * li, outliers=outl,
-                      sink=w["sink"], device=dev)
-        K_, V_ = syn.prompt(w["prompt"])
-        c = KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], w["prompt"] + S, device=dev)
-        c.set_decode_kernel(_KERNEL_IDS[args.decode_kernel])
-        c.prefill(K_, V_)
-        out = None
-        for s in range(S):
-            q, k, v = syn.step(s)
-            c.append(k, v)
-            out = c.decode_attn(q, out=out)
-        for _ in range(args.profile_calls):
-            c.decode_attn(q, out=out)
-        del K_, V_
+    w2 = dict(w, layers=min(w["layers"], 2))
+    paged = bool(w.get("paged") or args.paged)
+    eng = (_PagedEngine if paged else _DenseEngine)(args, w2, dev, 0, outl, SynthKV, torch)
+    eng.step()
+    for _ in range(args.profile_calls):
+        eng.decode_only()
     torch.cuda.synchronize()
-    print(json.dumps({"profile_run": args.workload, "decode_source_sha1": _decode_source_sha1()}))
+    print(json.dumps({"profile_run": args.workload, "paged": paged, "decode_source_sha1": _decode_source_sha1()}))
 
 
-def _e2e(args, w, caches, prompts, steps, torch, dev):
-    NL, S = w["layers"], w["decode"]
-    pin = lambda t: t.cpu().pin_memory()
-    h_prompts = [(pin(K_), pin(V_)) for K_, V_ in prompts]
-    h_steps = [[tuple(pin(t) for t in st) for st in layer] for layer in steps]
-    d_prompts = [(torch.empty_like(K_), torch.empty_like(V_)) for K_, V_ in prompts]
-    d_qkv = [tuple(torch.empty_like(t) for t in steps[0][0]) for _ in range(NL)]
-    h_out = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16).pin_memory() for _ in range(NL)]
-    d_out = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
-    h2d = sum(K_.numel() * 2 + V_.numel() * 2 for K_, V_ in h_prompts)
-    h2d += sum(t.numel() * 2 for layer in h_steps for st in layer for t in st)
-    d2h = NL * S * h_out[0].numel() * 2
+class _DenseEngine:
+    """The workload on dense caches (one KiviCache per layer, all rows of equal length)."""
 
-    def step():
+    def __init__(self, args, w, dev, rank, outl, SynthKV, torch):
+        from bit_kivi_kv_gb300.kivi import KiviCache
+        self.args, self.w, self.dev, self.torch = args, w, dev, torch
+        NL, S = w["layers"], w["decode"]
+        self.caches, self.prompts, self.steps = [], [], []
         for li in range(NL):
-            d_prompts[li][0].copy_(h_prompts[li][0], non_blocking=True)
-            d_prompts[li][1].copy_(h_prompts[li][1], non_blocking=True)
-            caches[li].reset()
-            caches[li].prefill(*d_prompts[li])
-        for s in range(S):
-            for li in range(NL):
-                q, k, v = d_qkv[li]
-                hq, hk, hv = h_steps[li][s]
-                q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
-                if args.separate_append:
-                    caches[li].append(k, v)
-                    caches[li].decode_attn(q, out=d_out[li])
-                else:
-                    caches[li].append_decode(k, v, q, out=d_out[li])
-                h_out[li].copy_(d_out[li], non_blocking=True)
+            syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=replica_seed(w, li, rank),
+                          outliers=outl, sink=w["sink"], device=dev)
+            self.prompts.append(syn.prompt(w["prompt"]))
+            self.steps.append([syn.step(s) for s in range(S)])
+            c = KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], w["prompt"] + S, device=dev)
+            c.set_decode_kernel(_KERNEL_IDS[args.decode_kernel])
+            self.caches.append(c)
+        self.outs = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
 
-    n = max(3, min(args.steps, 10))
+    def step(self):
+        w, sep = self.w, self.args.separate_append
+        for li, c in enumerate(self.caches):
+            c.reset()
+            c.prefill(*self.prompts[li])
+        for s in range(w["decode"]):
+            for li, c in enumerate(self.caches):
+                q, k, v = self.steps[li][s]
+                if sep:
+                    c.append(k, v)
+                    c.decode_attn(q, out=self.outs[li])
+                else:
+                    c.append_decode(k, v, q, out=self.outs[li])
+
+    def decode_only(self):
+        for li, c in enumerate(self.caches):
+            c.decode_attn(self.steps[li][-1][0], out=self.outs[li])
+
+    def e2e(self, n):
+        torch, w, dev = self.torch, self.w, self.dev
+        NL, S = w["layers"], w["decode"]
+        pin = lambda t: t.cpu().pin_memory()
+        h_prompts = [(pin(K_), pin(V_)) for K_, V_ in self.prompts]
+        h_steps = [[tuple(pin(t) for t in st) for st in layer] for layer in self.steps]
+        d_prompts = [(torch.empty_like(K_), torch.empty_like(V_)) for K_, V_ in self.prompts]
+        d_qkv = [tuple(torch.empty_like(t) for t in self.steps[0][0]) for _ in range(NL)]
+        h_out = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16).pin_memory() for _ in range(NL)]
+        d_out = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
+        h2d = sum(K_.numel() * 2 + V_.numel() * 2 for K_, V_ in h_prompts)
+        h2d += sum(t.numel() * 2 for layer in h_steps for st in layer for t in st)
+        d2h = NL * S * h_out[0].numel() * 2
+        sep = self.args.separate_append
+
+        def step():
+            for li, c in enumerate(self.caches):
+                d_prompts[li][0].copy_(h_prompts[li][0], non_blocking=True)
+                d_prompts[li][1].copy_(h_prompts[li][1], non_blocking=True)
+                c.reset()
+                c.prefill(*d_prompts[li])
+            for s in range(S):
+                for li, c in enumerate(self.caches):
+                    q, k, v = d_qkv[li]
+                    hq, hk, hv = h_steps[li][s]
+                    q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
+                    if sep:
+                        c.append(k, v)
+                        c.decode_attn(q, out=d_out[li])
+                    else:
+                        c.append_decode(k, v, q, out=d_out[li])
+                    h_out[li].copy_(d_out[li], non_blocking=True)
+
+        return _time_e2e(step, n, w, h2d, d2h, torch)
+
+
+class _PagedEngine:
+    """The workload on paged caches (one KiviPagedCache per layer): every step
+    releases the rows' sequences and adds them again with their prompts (the
+    allocator hands out the pages), then appends + decodes all of them."""
+
+    def __init__(self, args, w, dev, rank, outl, SynthKV, torch):
+        from bit_kivi_kv_gb300.kivi import KiviPagedCache
+        self.args, self.w, self.dev, self.torch = args, w, dev, torch
+        NL, S = w["layers"], w["decode"]
+        lengths = _lengths(w)
+        blocks = [_call_counts(w, L)[-1][0] // w["G"] for L in lengths]
+        self.caches, self.prompts, self.steps, self.seqs = [], [], [], []
+        for li in range(NL):
+            # the dense workload's generator: row b's prompt is the first L_b tokens
+            # of its row, its queries carry the row's attention-sink direction
+            syn = SynthKV(len(lengths), w["Hq"], w["Hkv"], w["D"], seed=replica_seed(w, li, rank),
+                          outliers=outl, sink=w["sink"], device=dev)
+            K_, V_ = syn.prompt(max(lengths))
+            self.prompts.append([(K_[b, :, :L].contiguous(), V_[b, :, :L].contiguous())
+                                 for b, L in enumerate(lengths)])
+            del K_, V_
+            self.steps.append([syn.step(s) for s in range(S)])
+            self.caches.append(KiviPagedCache(len(lengths), w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"],
+                                              max(blocks) + 1, sum(blocks) + len(lengths), device=dev))
+            self.seqs.append([])
+        self.outs = [torch.empty(len(lengths), w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
+
+    def _readd(self, li, prompts):
+        c = self.caches[li]
+        for s in self.seqs[li]:
+            c.release(s)
+        self.seqs[li] = [c.add(K_, V_) for K_, V_ in prompts]
+
+    def step(self):
+        for li in range(len(self.caches)):
+            self._readd(li, self.prompts[li])
+        for s in range(self.w["decode"]):
+            for li, c in enumerate(self.caches):
+                q, k, v = self.steps[li][s]
+                c.append_decode(self.seqs[li], k, v, q, out=self.outs[li])
+
+    def decode_only(self):
+        for li, c in enumerate(self.caches):
+            c.append_decode(self.seqs[li], None, None, self.steps[li][-1][0], out=self.outs[li])
+
+    def e2e(self, n):
+        torch, w, dev = self.torch, self.w, self.dev
+        NL, S = w["layers"], w["decode"]
+        pin = lambda t: t.cpu().pin_memory()
+        h_prompts = [[(pin(K_), pin(V_)) for K_, V_ in rows] for rows in self.prompts]
+        h_steps = [[tuple(pin(t) for t in st) for st in layer] for layer in self.steps]
+        d_prompts = [[(torch.empty_like(K_), torch.empty_like(V_)) for K_, V_ in rows] for rows in self.prompts]
+        d_qkv = [tuple(torch.empty_like(t) for t in self.steps[0][0]) for _ in range(NL)]
+        nb = len(self.seqs[0])
+        h_out = [torch.empty(nb, w["Hq"], w["D"], dtype=torch.float16).pin_memory() for _ in range(NL)]
+        d_out = [torch.empty(nb, w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
+        h2d = sum(K_.numel() * 2 + V_.numel() * 2 for rows in h_prompts for K_, V_ in rows)
+        h2d += sum(t.numel() * 2 for layer in h_steps for st in layer for t in st)
+        d2h = NL * S * h_out[0].numel() * 2
+
+        def step():
+            for li in range(NL):
+                for (dk, dv), (hk, hv) in zip(d_prompts[li], h_prompts[li]):
+                    dk.copy_(hk, non_blocking=True)
+                    dv.copy_(hv, non_blocking=True)
+                self._readd(li, d_prompts[li])
+            for s in range(S):
+                for li, c in enumerate(self.caches):
+                    q, k, v = d_qkv[li]
+                    hq, hk, hv = h_steps[li][s]
+                    q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
+                    c.append_decode(self.seqs[li], k, v, q, out=d_out[li])
+                    h_out[li].copy_(d_out[li], non_blocking=True)
+
+        return _time_e2e(step, n, w, h2d, d2h, torch)
+
+
+def _time_e2e(step, n, w, h2d, d2h, torch):
     step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -512,6 +626,8 @@ def main():
                     help="decode steps as kivi_append + kivi_decode_attn instead of kivi_append_decode")
     ap.add_argument("--decode-kernel", choices=["auto", "cuda-core", "tensor-core"], default="auto")
     ap.add_argument("--profile-calls", type=int, default=4)
+    ap.add_argument("--paged", action="store_true",
+                    help="run the workload on the paged cache (ragged workloads always are)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

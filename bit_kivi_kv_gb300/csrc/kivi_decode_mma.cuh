@@ -562,6 +562,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
         const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
         auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
+        // the preceding kernel wrote blocks (and, paged, block-table entries): wait
+        // before the first copy and before the first table read
+        if (first_seg && !a.early_ok) griddepcontrol_wait();
         // lane 0's copy cursor: key part of the block of the next pair to fetch, tile in block
         // (paged: the block's page pg and the next block's page pgn, loaded one block ahead)
         const uint8_t* kcur;
@@ -610,7 +613,6 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 }
             }
         };
-        if (first_seg && !a.early_ok) griddepcontrol_wait();   // the preceding kernel wrote blocks
         if (lane == 0) {
             for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
         }
