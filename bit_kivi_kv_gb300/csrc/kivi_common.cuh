@@ -62,35 +62,55 @@ __host__ __device__ constexpr int entry_pos(int t) { return 4 * ((t & 7) >> 1) +
 // Balanced partition of a decode call's work over the CTAs of the tensor-core
 // kernel.  Per (batch, kv-head) slot the work is a row of units: P quantized
 // tile pairs (32 tokens) of weight wq, then PR fp16 residual pairs (32 rows) of
-// weight wr (weights proportional to the bytes each reads).  Slots follow each
-// other; CTA c covers weight positions [c*Wt/n, (c+1)*Wt/n) and owns the units
-// that start there.  n <= Wt / max(wq, wr) guarantees every CTA owns a unit.
+// weight wr (weights proportional to the bytes each reads), after a lead-in of
+// weight S0 that stands for the fixed cost a CTA pays per slot it works on
+// (query setup, ring fill, warp merge): the CTA whose range takes in a slot's
+// start is given that much less of the units.  Slots follow each other; CTA c
+// covers weight positions [c*Wt/n, (c+1)*Wt/n) and owns the units that start
+// there.  n <= Wt / max(wq, wr) guarantees that every CTA between the first and
+// the last unit of a slot owns one of them.
 struct WorkMap {
-    long long P, PR, wq, wr, Ws, Wt, n;
+    long long P, PR, wq, wr, Ws, Wt, n, S0;
 };
-// the same for a slot of P quantized pairs (slots of ragged sequences differ)
-__host__ __device__ inline long long unit_start_p(long long P, long long wq, long long wr, long long u) {
-    return u < P ? u * wq : P * wq + (u - P) * wr;
+// The lead-in in quantized pairs, used when the call's shortest slot is shorter
+// than a CTA's share (with ~4 CTAs per SM), so that CTAs cover several slot
+// starts: measured on GB300, 10 pairs take ragged prompts of 512..7680 tokens
+// from 41.5 to 36.9 us per call and grouped-query slots of ~0.9 shares from
+// 119.9 to 117.6 us, while for slots of 2.4 shares (Llama-2-7B layer) any
+// lead-in is slower (33.9 -> 34.4 us at 5 pairs).
+constexpr long long kSegmentLeadPairs = 10;
+__host__ inline long long segment_lead(long long wq, long long ws_min, long long wt, int num_sms) {
+    const long long n_est = 4LL * (num_sms > 0 ? num_sms : 1);
+    return ws_min * n_est < wt ? kSegmentLeadPairs * wq : 0;
+}
+// unit u of a slot of P quantized pairs (slots of ragged sequences differ)
+__host__ __device__ inline long long unit_start_p(long long P, long long wq, long long wr, long long S0,
+                                                  long long u) {
+    return S0 + (u < P ? u * wq : P * wq + (u - P) * wr);
 }
 // first unit of a slot starting at or after weight offset y (0 <= y <= Ws); P + PR if none
-__host__ __device__ inline long long first_unit_at_p(long long P, long long wq, long long wr, long long y) {
+__host__ __device__ inline long long first_unit_at_p(long long P, long long wq, long long wr, long long S0,
+                                                     long long y) {
+    y -= S0;
     if (y <= 0) return 0;
     if (y <= P * wq) return (y + wq - 1) / wq;
     return P + (y - P * wq + wr - 1) / wr;
 }
 __host__ __device__ inline long long unit_start(const WorkMap& m, long long u) {
-    return unit_start_p(m.P, m.wq, m.wr, u);
+    return unit_start_p(m.P, m.wq, m.wr, m.S0, u);
 }
 __host__ __device__ inline long long first_unit_at(const WorkMap& m, long long y) {
-    return first_unit_at_p(m.P, m.wq, m.wr, y);
+    return first_unit_at_p(m.P, m.wq, m.wr, m.S0, y);
 }
 __host__ __device__ inline long long map_begin(const WorkMap& m, long long c) { return c * m.Wt / m.n; }
 // the CTA whose range holds weight position x
 __host__ __device__ inline long long map_owner(const WorkMap& m, long long x) {
     return ((x + 1) * m.n + m.Wt - 1) / m.Wt - 1;
 }
-// partials of slot s: CTAs [map_owner(s*Ws), map_owner(s*Ws + start of its last unit)]
-__host__ __device__ inline long long slot_first_cta(const WorkMap& m, long long s) { return map_owner(m, s * m.Ws); }
+// partials of slot s: CTAs [owner of its first unit's start, owner of its last unit's start]
+__host__ __device__ inline long long slot_first_cta(const WorkMap& m, long long s) {
+    return map_owner(m, s * m.Ws + m.S0);
+}
 __host__ __device__ inline int slot_parts(const WorkMap& m, long long s) {
     if (m.P + m.PR == 0) return 0;
     return (int)(map_owner(m, s * m.Ws + unit_start(m, m.P + m.PR - 1)) - slot_first_cta(m, s) + 1);

@@ -374,12 +374,19 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
     WorkMap wm{};
     wm.wq = (long long)g.D * g.bits / 4 + 8LL * g.D / g.G;
     wm.wr = 4LL * g.D;
+    long long wt0 = 0, ws_min = -1;
+    for (int i = 0; i < n; ++i) {
+        if (seqs[i].P + seqs[i].n_resid <= 0) return cudaErrorInvalidValue;   // a sequence without tokens
+        const long long w = seqs[i].P * wm.wq + (long long)((seqs[i].n_resid + 31) / 32) * wm.wr;
+        wt0 += g.Hkv * w;
+        if (ws_min < 0 || w < ws_min) ws_min = w;
+    }
+    wm.S0 = segment_lead(wm.wq, ws_min, wt0, num_sms);
     mma_detail::PagedArgs m;   // ~12 KB of kernel parameters
     long long start = 0, ws_max = 0;
     for (int i = 0; i < n; ++i) {
         PagedSeq s = seqs[i];
-        const long long Ws = s.P * wm.wq + (long long)((s.n_resid + 31) / 32) * wm.wr;
-        if (Ws <= 0) return cudaErrorInvalidValue;   // a sequence without tokens
+        const long long Ws = wm.S0 + s.P * wm.wq + (long long)((s.n_resid + 31) / 32) * wm.wr;
         s.start = start;
         start += g.Hkv * Ws;
         if (Ws > ws_max) ws_max = Ws;
@@ -428,7 +435,9 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         wm.PR = (n_resid + 31) / 32;
         wm.wq = (long long)g.D * g.bits / 4 + 8LL * g.D / g.G;   // bytes of a quantized pair / 32
         wm.wr = 4LL * g.D;                                        // bytes of a residual pair / 32
-        wm.Ws = wm.P * wm.wq + wm.PR * wm.wr;
+        const long long ws0 = wm.P * wm.wq + wm.PR * wm.wr;
+        wm.S0 = segment_lead(wm.wq, ws0, slots * ws0, plan.num_sms);
+        wm.Ws = wm.S0 + ws0;
         wm.Wt = slots * wm.Ws;
         mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                            g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2,

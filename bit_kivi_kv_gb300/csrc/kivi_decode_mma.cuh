@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             const PagedSeq& sq = a.seqs[lo];
             P = sq.P;
             PR = (sq.n_resid + 31) / 32;
-            Ws = P * wm.wq + PR * wm.wr;
+            Ws = wm.S0 + P * wm.wq + PR * wm.wr;
             hk = (int)((pos - sq.start) / Ws);
             w0 = sq.start + hk * Ws;
             b = lo;
@@ -550,13 +550,13 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             nrow = a.new_row;
         }
         const long long NU = P + PR;
-        const long long u0 = first_unit_at_p(P, wm.wq, wm.wr, pos - w0);
+        const long long u0 = first_unit_at_p(P, wm.wq, wm.wr, wm.S0, pos - w0);
         if (u0 >= NU) { pos = w0 + Ws; continue; }
-        if (w0 + unit_start_p(P, wm.wq, wm.wr, u0) >= pe) break;
-        const long long u1 = first_unit_at_p(P, wm.wq, wm.wr, min(pe - w0, Ws));
+        if (w0 + unit_start_p(P, wm.wq, wm.wr, wm.S0, u0) >= pe) break;
+        const long long u1 = first_unit_at_p(P, wm.wq, wm.wr, wm.S0, min(pe - w0, Ws));
         const int p0 = (int)min(u0, P), p1 = (int)min(u1, P);                  // quantized pairs
         const int r0 = (int)(max(u0, P) - P), r1 = (int)(max(u1, P) - P);      // residual pairs
-        const int part = (int)(cta - map_owner(wm, w0));
+        const int part = (int)(cta - map_owner(wm, w0 + wm.S0));
         // ---- this warp's contiguous run of pairs, two tiles per ring stage ----
         const int pw = (p1 - p0 + kWarps - 1) / kWarps;
         const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
@@ -942,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             pw[4 + c] = acc;
         }
         __syncthreads();                               // qf and red_* are reused by the next segment
-        pos = u1 >= NU ? w0 + Ws : w0 + unit_start_p(P, wm.wq, wm.wr, u1);
+        pos = u1 >= NU ? w0 + Ws : w0 + unit_start_p(P, wm.wq, wm.wr, wm.S0, u1);
     }
 }
 
@@ -991,9 +991,9 @@ __global__ void __launch_bounds__(D) finish_paged_kernel(const __grid_constant__
     const int i = (int)(bh / a.Hq), hk = (int)((bh % a.Hq) / a.nq);
     const PagedSeq& sq = a.seqs[i];
     const long long P = sq.P, PR = (sq.n_resid + 31) / 32;
-    const long long w0 = sq.start + hk * (P * a.wm.wq + PR * a.wm.wr);
-    const long long last = w0 + unit_start_p(P, a.wm.wq, a.wm.wr, P + PR - 1);
-    const int nparts = (int)(map_owner(a.wm, last) - map_owner(a.wm, w0) + 1);
+    const long long w0 = sq.start + hk * (a.wm.S0 + P * a.wm.wq + PR * a.wm.wr);
+    const long long last = w0 + unit_start_p(P, a.wm.wq, a.wm.wr, a.wm.S0, P + PR - 1);
+    const int nparts = (int)(map_owner(a.wm, last) - map_owner(a.wm, w0 + a.wm.S0) + 1);
     merge_partials<D>(a.ws + bh * kPartialSlots * partial_stride(D), nparts, a.out + bh * D, threadIdx.x);
 }
 

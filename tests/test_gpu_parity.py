@@ -193,3 +193,14 @@ def test_every_tensor_core_instantiation(combo):
     run = run_gpu(2, 2 * nq, 2, D, bits, G, R, L, R - 20, seed=sum(combo), decode_at={0, R - 21},
                   decode_kernel=KIVI_DECODE_TENSOR_CORE)
     check_slots(run, [(0, 0), (1, 1)], {0, R - 21})
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_many_short_slots(fused):
+    """256 (batch, kv-head) slots of 200 + 40 tokens: each slot is shorter than a
+    CTA's share, so the partition gives every slot a lead-in weight and CTAs
+    cover several slot starts; sampled slots against the oracle at three steps."""
+    steps = {0, 20, 39}
+    run = run_gpu(16, 32, 16, 64, 2, 32, 64, 200, 40, seed=91, decode_at=steps,
+                  decode_kernel=KIVI_DECODE_TENSOR_CORE, fused=fused)
+    check_slots(run, [(0, 0), (3, 7), (7, 15), (8, 1), (12, 9), (15, 15)], steps)
