@@ -23,7 +23,7 @@ Readings (where the pages are silent or disagree):
   * group boundaries therefore always fall on multiples of G counted from
     token 0;
   * keys and values share one residual count and flush together (the
-    one-token-at-a-time value queue of [explainer] 3.2 is not this cache).
+    one-token-at-a-time value queue of [explainer] 3.2 is OracleCacheFifo).
 
 Parity status: pinned (streaming equals one-shot quantization of the same
 token prefix; accounting invariants; residual holds the exact fp16 inputs).
@@ -113,3 +113,63 @@ class OracleCache:
         """All cached values in fp64 [B][H][Lq + r][d]: dequantized prefix, then residual."""
         vq = quant.dequantize_values(self.v_codes, self.v_s, self.v_z, self.G)
         return np.concatenate([vq, self.v_res.astype(np.float64)], axis=2)
+
+
+class OracleCacheFifo(OracleCache):
+    """The same cache with the value residual kept as a queue ([explainer] 3.2).
+
+    Keys behave exactly as in OracleCache (whole groups, flush of the R
+    residual tokens when full).  Values follow [explainer] 3.2: new value
+    tokens enter an fp16 queue; once it holds R tokens, the oldest token
+    leaves the queue, is quantized on its own (per token, groups of G
+    channels) and joins the quantized values; the newest R values stay fp16.
+
+    Readings: after every call the queue holds the newest min(l, R) value
+    tokens and the first max(l - R, 0) are quantized (an append pushes the
+    new token and pops the oldest once the queue would exceed R; a prompt
+    quantizes all but its last R values).  Because value groups lie within one
+    token, the quantized values equal a one-shot per-token quantization of
+    the same prefix.
+
+    Extra state: v_codes / v_s / v_z cover the first max(l - R, 0) tokens
+    (n_quant_v of them); v_res holds the queue in token order.
+
+    Parity status: pinned (one-shot equality, the queue's contents, keys
+    identical to OracleCache, hand-worked positions).
+    """
+
+    @property
+    def n_quant_v(self) -> int:
+        return self.v_codes.shape[2]
+
+    def prefill(self, X_K: np.ndarray, X_V: np.ndarray):
+        if self.n_quant or self.n_resid or self.n_quant_v or self.v_res.shape[2]:
+            raise RuntimeError("prefill on a non-empty cache")
+        l = X_K.shape[2]
+        Lq, _ = prefill_split(l, self.G, self.R)
+        if Lq:
+            kc, ks, kz = quant.quantize_keys(X_K[:, :, :Lq], self.bits, self.G)
+            self.k_codes, self.k_s, self.k_z = kc, ks, kz
+        self.k_res = X_K[:, :, Lq:].copy()
+        Lv = max(l - self.R, 0)
+        if Lv:
+            self.v_codes, self.v_s, self.v_z = quant.quantize_values(X_V[:, :, :Lv], self.bits, self.G)
+        self.v_res = X_V[:, :, Lv:].copy()
+
+    def append(self, k: np.ndarray, v: np.ndarray):
+        # keys: as in OracleCache
+        if self.n_resid == self.R:
+            kc, ks, kz = quant.quantize_keys(self.k_res, self.bits, self.G)
+            cat = lambda a, b: np.concatenate([a, b], axis=2)
+            self.k_codes, self.k_s, self.k_z = cat(self.k_codes, kc), cat(self.k_s, ks), cat(self.k_z, kz)
+            self.k_res = self.k_res[:, :, :0]
+            self.flushes += 1
+        self.k_res = np.concatenate([self.k_res, k[:, :, None, :]], axis=2)
+        # values: push, then pop the oldest once the queue would exceed R
+        self.v_res = np.concatenate([self.v_res, v[:, :, None, :]], axis=2)
+        if self.v_res.shape[2] > self.R:
+            vc, vs, vz = quant.quantize_values(self.v_res[:, :, :1], self.bits, self.G)
+            cat = lambda a, b: np.concatenate([a, b], axis=2)
+            self.v_codes, self.v_s, self.v_z = cat(self.v_codes, vc), cat(self.v_s, vs), cat(self.v_z, vz)
+            self.v_res = self.v_res[:, :, 1:]
+
