@@ -50,6 +50,9 @@ WORKLOADS = {
                           layers=2, outliers="range", sink=True, seed=1003),
     "llama2-7b-layer-8bit": dict(B=8, Hq=32, Hkv=32, D=128, bits=8, G=32, R=128, prompt=4096, decode=64,
                                  layers=4, outliers="range", sink=True, seed=1005),
+    # the 7B layer with the value residual kept as a queue (one value quantized per append)
+    "llama2-7b-layer-vqueue": dict(B=8, Hq=32, Hkv=32, D=128, bits=2, G=32, R=128, prompt=4096, decode=64,
+                                   layers=4, outliers="range", sink=True, seed=1001, vqueue=True),
     # the 7B layer with ragged prompts (mean 4096) on the paged cache
     "llama2-7b-ragged": dict(B=8, Hq=32, Hkv=32, D=128, bits=2, G=32, R=128, prompt=4096,
                              lengths=[512, 1536, 2560, 3584, 4608, 5632, 6656, 7680], decode=64,
@@ -96,11 +99,13 @@ def _bytes_last_call(w):
     """Algorithmic bytes of a decode call over the cache as the step leaves it:
     codes + (step, zero) entries of every quantized token, fp16 residual rows,
     the query and the output."""
-    per_tok = 2 * (w["D"] * w["bits"] // 8) + 2 * (4 * w["D"] // w["G"])
+    half_tok = w["D"] * w["bits"] // 8 + 4 * w["D"] // w["G"]   # codes + (step, zero) of K or of V
     kv = 0
     for L in _lengths(w):
         Lq, r = _call_counts(w, L)[-1]
-        kv += w["Hkv"] * (Lq * per_tok + r * 4 * w["D"])
+        # values quantized: with the value queue all but the newest R, else those of the keys
+        Lv = max(Lq + r - w["R"], 0) if w.get("vqueue") else Lq
+        kv += w["Hkv"] * (Lq * half_tok + Lv * half_tok + r * 2 * w["D"] + (Lq + r - Lv) * 2 * w["D"])
     return kv + 2 * w["B"] * w["Hq"] * w["D"] * 2
 
 
@@ -212,7 +217,7 @@ def oracle_sample(w, n_slots=None, budget_s=15.0, step_seed=0):
     import torch
     from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV
     from oracle.attention import decode_attention
-    from oracle.cache import OracleCache
+    from oracle.cache import OracleCache, OracleCacheFifo
 
     outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
     syn = SynthKV(1, w["Hq"] // w["Hkv"], 1, w["D"], seed=w["seed"] + step_seed, outliers=outl,
@@ -224,7 +229,7 @@ def oracle_sample(w, n_slots=None, budget_s=15.0, step_seed=0):
     t0 = time.perf_counter()
     done, tokens = 0, 0
     while True:
-        oc = OracleCache(1, 1, w["D"], w["bits"], w["G"], w["R"])
+        oc = (OracleCacheFifo if w.get("vqueue") else OracleCache)(1, 1, w["D"], w["bits"], w["G"], w["R"])
         L = lengths[(done + step_seed) % len(lengths)]     # ragged workloads: the rows' lengths in turn
         oc.prefill(np.ascontiguousarray(Kn[:, :, :L]), np.ascontiguousarray(Vn[:, :, :L]))
         for (q, k, v) in steps:
@@ -272,6 +277,8 @@ def _config(w, name):
         c["prompt_lengths"] = list(w["lengths"])
     if w.get("paged"):
         c["cache"] = "paged (page pool + block tables)"
+    if w.get("vqueue"):
+        c["value_residual"] = "queue (one value token quantized per append)"
     return c
 
 
@@ -465,6 +472,8 @@ class _DenseEngine:
             self.steps.append([syn.step(s) for s in range(S)])
             c = KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], w["prompt"] + S, device=dev)
             c.set_decode_kernel(_KERNEL_IDS[args.decode_kernel])
+            if w.get("vqueue"):
+                c.set_value_residual(1)
             self.caches.append(c)
         self.outs = [torch.empty(w["B"], w["Hq"], w["D"], dtype=torch.float16, device=dev) for _ in range(NL)]
 

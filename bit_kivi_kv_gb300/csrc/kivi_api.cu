@@ -22,6 +22,7 @@ struct kivi_cache {
     int device;      // -1 until the first decode queries it
     int num_sms;
     int decode_kernel;   // kivi_decode_kernel
+    int value_queue;     // 1: the value residual is a queue ([explainer] 3.2)
 };
 
 namespace {
@@ -51,6 +52,12 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
 
 }  // namespace
+
+// Value queue, before an append stores its token: flush the key residual when
+// full (its blocks get their values as not quantized yet: they are all still
+// queued), then quantize the oldest queued value, whose ring row the new token
+// takes.  *wrote: a kernel that writes quantized blocks was launched.
+static kivi_status queue_before_append(kivi_cache* c, cudaStream_t st, bool* wrote);
 
 namespace kivi {
 
@@ -126,7 +133,7 @@ kivi_status kivi_cache_create(const kivi_config* cfg, void* dev_buf, size_t byte
     if (!aligned(dev_buf, 256)) return fail(KIVI_ERR_INVALID_ARG, "cache buffer must be 256-byte aligned");
     if (bytes < (size_t)g.total_bytes)
         return fail(KIVI_ERR_CAPACITY, "cache buffer has %zu bytes, needs %lld", bytes, g.total_bytes);
-    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0, KIVI_DECODE_AUTO};
+    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0, KIVI_DECODE_AUTO, 0};
     if (!c) return fail(KIVI_ERR_INVALID_ARG, "out of host memory");
     *out = c;
     return ok();
@@ -167,6 +174,23 @@ kivi_status kivi_prefill(kivi_cache_t c, const void* K, const void* V, long long
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const __half* k = static_cast<const __half*>(K);
     const __half* v = static_cast<const __half*>(V);
+    if (c->value_queue) {
+        // values: all but the newest R are quantized (per token); the newest sit
+        // in the ring at row position % R; keys as below
+        const long long Lv = L > g.R ? L - g.R : 0;
+        if (Lq) {
+            const cudaError_t e = kivi::launch_quantize_blocks(g, c->buf, k, v, L * g.D, 0, Lq / g.G, st, Lv);
+            if (e != cudaSuccess) return cuda_fail(e, "prefill quantize launch");
+            g_launches++;
+        }
+        const cudaError_t e = kivi::launch_copy_rows_ring(g, c->buf, k, v, L * g.D, 0, Lq, (int)r, Lv, Lv,
+                                                          (int)(L - Lv), st);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill residual copy launch");
+        g_launches++;
+        c->n_quant = Lq;
+        c->n_resid = r;
+        return ok();
+    }
     if (Lq) {
         const cudaError_t e = kivi::launch_quantize_blocks(g, c->buf, k, v, L * g.D, 0, Lq / g.G, st);
         if (e != cudaSuccess) return cuda_fail(e, "prefill quantize launch");
@@ -190,6 +214,19 @@ kivi_status kivi_append(kivi_cache_t c, const void* k, const void* v, kivi_strea
     if (c->n_quant + c->n_resid + 1 > g.max_tokens)
         return fail(KIVI_ERR_CAPACITY, "cache already holds max_tokens (%lld) tokens", g.max_tokens);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (c->value_queue) {
+        bool unused;
+        const kivi_status sq = queue_before_append(c, st, &unused);
+        if (sq != KIVI_OK) return sq;
+        const long long L = c->n_quant + c->n_resid;
+        const cudaError_t e = kivi::launch_copy_rows_ring(g, c->buf, static_cast<const __half*>(k),
+                                                          static_cast<const __half*>(v), g.D, (int)c->n_resid, 0, 1,
+                                                          L, 0, 1, st);
+        if (e != cudaSuccess) return cuda_fail(e, "append copy launch");
+        g_launches++;
+        c->n_resid += 1;
+        return ok();
+    }
     if (c->n_resid == g.R) {
         const __half* rk = reinterpret_cast<const __half*>(c->buf + g.k_resid_off);
         const __half* rv = reinterpret_cast<const __half*>(c->buf + g.v_resid_off);
@@ -271,10 +308,17 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void* q, void* out, float sof
     const kivi_status st = decode_checks(c, q, out, softmax_scale, workspace, ws_bytes);
     if (st != KIVI_OK) return st;
     if (c->n_quant + c->n_resid == 0) return fail(KIVI_ERR_STATE, "decode on an empty cache");
+    const int variant = c->decode_kernel == KIVI_DECODE_AUTO ? KIVI_DECODE_TENSOR_CORE : c->decode_kernel;
+    if (c->value_queue && variant != KIVI_DECODE_TENSOR_CORE)
+        return fail(KIVI_ERR_UNSUPPORTED, "the value queue is decoded by the tensor-core kernel only");
     const kivi_status sdev = ensure_device(c);
     if (sdev != KIVI_OK) return sdev;
-    const int variant = c->decode_kernel == KIVI_DECODE_AUTO ? KIVI_DECODE_TENSOR_CORE : c->decode_kernel;
-    return decode_launch(c, q, out, softmax_scale, workspace, c->n_resid, variant, stream, kivi::FusedAppend{});
+    kivi::FusedAppend fa;
+    if (c->value_queue) {
+        const long long L = c->n_quant + c->n_resid;
+        fa.lqv = L > c->geo.R ? L - c->geo.R : 0;
+    }
+    return decode_launch(c, q, out, softmax_scale, workspace, c->n_resid, variant, stream, fa);
 }
 
 kivi_status kivi_append_decode(kivi_cache_t c, const void* k, const void* v, const void* q, void* out,
@@ -287,6 +331,8 @@ kivi_status kivi_append_decode(kivi_cache_t c, const void* k, const void* v, con
     if (c->n_quant + c->n_resid + 1 > g.max_tokens)
         return fail(KIVI_ERR_CAPACITY, "cache already holds max_tokens (%lld) tokens", g.max_tokens);
     const int variant = c->decode_kernel == KIVI_DECODE_AUTO ? KIVI_DECODE_TENSOR_CORE : c->decode_kernel;
+    if (c->value_queue && variant != KIVI_DECODE_TENSOR_CORE)
+        return fail(KIVI_ERR_UNSUPPORTED, "the value queue is decoded by the tensor-core kernel only");
     if (variant != KIVI_DECODE_TENSOR_CORE) {
         // the CUDA-core kernel has no fused form: append, then decode
         const kivi_status sa = kivi_append(c, k, v, stream);
@@ -297,6 +343,21 @@ kivi_status kivi_append_decode(kivi_cache_t c, const void* k, const void* v, con
     if (sdev != KIVI_OK) return sdev;
     cudaStream_t sp = reinterpret_cast<cudaStream_t>(stream);
     bool flushed = false;
+    if (c->value_queue) {
+        const kivi_status sq = queue_before_append(c, sp, &flushed);
+        if (sq != KIVI_OK) return sq;
+        const long long L = c->n_quant + c->n_resid + 1;   // with the new token
+        kivi::FusedAppend fa;
+        fa.k = static_cast<const __half*>(k);
+        fa.v = static_cast<const __half*>(v);
+        fa.row = (int)c->n_resid;
+        fa.early_ok = flushed ? 0 : 1;
+        fa.lqv = L > g.R ? L - g.R : 0;
+        const kivi_status sd = decode_launch(c, q, out, softmax_scale, workspace, c->n_resid + 1, variant, stream, fa);
+        if (sd != KIVI_OK) return sd;
+        c->n_resid += 1;
+        return ok();
+    }
     if (c->n_resid == g.R) {
         const __half* rk = reinterpret_cast<const __half*>(c->buf + g.k_resid_off);
         const __half* rv = reinterpret_cast<const __half*>(c->buf + g.v_resid_off);
@@ -316,6 +377,16 @@ kivi_status kivi_append_decode(kivi_cache_t c, const void* k, const void* v, con
     const kivi_status sd = decode_launch(c, q, out, softmax_scale, workspace, c->n_resid + 1, variant, stream, fa);
     if (sd != KIVI_OK) return sd;
     c->n_resid += 1;
+    return ok();
+}
+
+kivi_status kivi_cache_set_value_residual(kivi_cache_t c, int mode) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    if (mode != KIVI_VALUE_FLUSH && mode != KIVI_VALUE_QUEUE) return fail(KIVI_ERR_INVALID_ARG, "unknown value residual mode %d", mode);
+    if (c->n_quant || c->n_resid) return fail(KIVI_ERR_STATE, "the value residual mode is set on an empty cache");
+    if (mode == KIVI_VALUE_QUEUE && c->geo.R > 128)
+        return fail(KIVI_ERR_UNSUPPORTED, "the value queue needs residual <= 128 (residual is %d)", c->geo.R);
+    c->value_queue = mode == KIVI_VALUE_QUEUE;
     return ok();
 }
 
@@ -345,3 +416,30 @@ size_t decode_workspace_need(const kivi_cache* c) {
 }
 
 }  // namespace kivi
+
+static kivi_status queue_before_append(kivi_cache* c, cudaStream_t st, bool* wrote) {
+    const kivi::Geometry& g = c->geo;
+    *wrote = false;
+    const long long L = c->n_quant + c->n_resid;
+    const long long Lv = L > g.R ? L - g.R : 0;   // values quantized so far
+    if (c->n_resid == g.R) {
+        // keys [Lq, Lq + R) into blocks; their values are all >= Lv, so written as
+        // not quantized yet (the value source is not read for them)
+        const __half* rk = reinterpret_cast<const __half*>(c->buf + g.k_resid_off);
+        const cudaError_t e = kivi::launch_quantize_blocks(g, c->buf, rk, rk, (long long)g.R * g.D,
+                                                           c->n_quant / g.G, g.R / g.G, st, Lv);
+        if (e != cudaSuccess) return cuda_fail(e, "residual flush launch");
+        g_launches++;
+        c->n_quant += g.R;
+        c->n_resid = 0;
+        *wrote = true;
+    }
+    if (L >= g.R) {
+        const cudaError_t e = kivi::launch_pop_values(g, c->buf, L - g.R, st);
+        if (e != cudaSuccess) return cuda_fail(e, "value queue launch");
+        g_launches++;
+        *wrote = true;
+    }
+    return ok();
+}
+

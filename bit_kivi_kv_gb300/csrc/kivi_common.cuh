@@ -120,10 +120,25 @@ __host__ __device__ inline int slot_parts(const WorkMap& m, long long s) {
 
 // Quantize nblk whole blocks per slot.  Block j of slot s is read from
 // src_k/src_v + s*src_slot_elems + j*G*D (rows of D fp16, consecutive tokens)
-// and written to block first_block + j of that slot.
+// and written to block first_block + j of that slot.  Value tokens at slot
+// positions >= vlimit are written as not yet quantized (zero codes, step and
+// zero point); the value queue fills them in later.
+constexpr long long kNoValueLimit = 1LL << 62;
 cudaError_t launch_quantize_blocks(const Geometry& g, uint8_t* cache, const __half* src_k,
                                    const __half* src_v, long long src_slot_elems,
-                                   long long first_block, long long nblk, cudaStream_t st);
+                                   long long first_block, long long nblk, cudaStream_t st,
+                                   long long vlimit = kNoValueLimit);
+
+// Value queue: quantize value token t of every slot from residual row t % R
+// into its block (whose value part holds zeros for it).
+cudaError_t launch_pop_values(const Geometry& g, uint8_t* cache, long long t, cudaStream_t st);
+
+// Residual copies with the values kept as a ring of R rows: per slot, nk key
+// rows (source rows k_src0.. into residual rows k_row0..) and nv value rows
+// (source rows v_src0.., tokens v_tok0.. into rows token % R).
+cudaError_t launch_copy_rows_ring(const Geometry& g, uint8_t* cache, const __half* src_k, const __half* src_v,
+                                  long long src_slot_elems, int k_row0, long long k_src0, int nk,
+                                  long long v_tok0, long long v_src0, int nv, cudaStream_t st);
 
 // Copy nrows token rows per slot (K and V) into residual rows [row0, row0+nrows).
 cudaError_t launch_copy_rows(const Geometry& g, uint8_t* cache, const __half* src_k,
@@ -148,6 +163,9 @@ struct FusedAppend {
     const __half* v = nullptr;
     int row = -1;
     int early_ok = 1;
+    // value queue (tensor-core kernel only): >= 0 selects it; values of slot
+    // positions below lqv are quantized, the rest sit in the residual ring
+    long long lqv = -1;
 };
 
 // variant: KIVI_DECODE_CUDA_CORE or KIVI_DECODE_TENSOR_CORE (resolved, never AUTO).

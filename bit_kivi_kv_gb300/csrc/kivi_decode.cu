@@ -340,6 +340,8 @@ cudaError_t launch_decode_mma_d64(mma_detail::Args& a, int bits, int nq, int G, 
 cudaError_t launch_decode_mma_d128f(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_mma_d64f(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_mma_d128p(mma_detail::PagedArgs& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_mma_d128q(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_mma_d64q(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_mma_d64p(mma_detail::PagedArgs& a, int bits, int nq, int G, int num_sms, cudaStream_t st);
 
 namespace {
@@ -426,7 +428,8 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
                           long long n_resid, const __half* q, __half* out, float scale_log2,
                           float* workspace, const DecodePlan& plan, int variant, cudaStream_t st,
                           int* launches, const FusedAppend& fa) {
-    if (fa.row >= 0 && variant != KIVI_DECODE_TENSOR_CORE) return cudaErrorInvalidValue;   // fused: tensor cores only
+    if ((fa.row >= 0 || fa.lqv >= 0) && variant != KIVI_DECODE_TENSOR_CORE)
+        return cudaErrorInvalidValue;   // fused append and value queue: tensor cores only
     if (variant == KIVI_DECODE_TENSOR_CORE) {
         const int nq = g.Hq / g.Hkv;
         const long long slots = (long long)g.B * g.Hkv;
@@ -441,12 +444,14 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         wm.Wt = slots * wm.Ws;
         mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                            g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2,
-                           fa.k, fa.v, fa.row, fa.early_ok};
-        const bool fused = fa.row >= 0;
-        cudaError_t e = g.D == 128 ? (fused ? launch_decode_mma_d128f : launch_decode_mma_d128)(m, g.bits, nq, g.G,
-                                                                                             plan.num_sms, st)
-                                   : (fused ? launch_decode_mma_d64f : launch_decode_mma_d64)(m, g.bits, nq, g.G,
-                                                                                           plan.num_sms, st);
+                           fa.k, fa.v, fa.row, fa.early_ok, fa.lqv};
+        const bool fused = fa.row >= 0, fifo = fa.lqv >= 0;
+        using L = cudaError_t (*)(mma_detail::Args&, int, int, int, int, cudaStream_t);
+        const L launch = g.D == 128 ? (fifo ? launch_decode_mma_d128q : fused ? launch_decode_mma_d128f
+                                                                              : launch_decode_mma_d128)
+                                    : (fifo ? launch_decode_mma_d64q : fused ? launch_decode_mma_d64f
+                                                                             : launch_decode_mma_d64);
+        cudaError_t e = launch(m, g.bits, nq, g.G, plan.num_sms, st);
         if (e != cudaSuccess) return e;
         mma_detail::FinishArgs f{workspace, out, g.Hq, g.Hkv, nq, m.wm};
         // the merge may start while the main kernel drains; it waits for it on the GPU

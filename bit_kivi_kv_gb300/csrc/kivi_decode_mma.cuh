@@ -59,6 +59,9 @@ struct Args {
     // 1: the preceding kernel writes no quantized block, so the first bulk
     // copies may go out before waiting for it
     int early_ok;
+    // value queue (kModeFifo): values of slot positions >= lqv are in the
+    // residual ring (row = position % R), those below are quantized
+    long long lqv = -1;
 };
 
 struct FinishArgs {
@@ -70,7 +73,12 @@ struct FinishArgs {
 
 // Kernel modes: plain decode; decode with a fused append; paged cache with
 // ragged sequences (fused append optional per sequence).
-constexpr int kModePlain = 0, kModeFused = 1, kModePaged = 2;
+// kModeFifo: dense cache whose values are a queue of R fp16 rows (a ring).
+constexpr int kModePlain = 0, kModeFused = 1, kModePaged = 2, kModeFifo = 3;
+// value queue: tile pairs with quantized keys but queued values, per warp at
+// most R / 32 (R <= 128); their logits wait in shared memory for the second pass
+constexpr int kMaxMixPairs = 4;
+constexpr int kMixBytes = kWarps * kMaxMixPairs * 32 * 16;
 
 // Paged call: cache = the page pool (and the buffer holding residual rows and
 // the block table); q / out / ws / new_k / new_v are indexed by the call's
@@ -380,7 +388,7 @@ struct MinCtas {
 template <int D, int BITS, int NQ, int G, int MODE>
 __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     decode_mma_kernel(const __grid_constant__ typename ArgsOf<MODE>::type a) {
-    constexpr bool FUSED = MODE != kModePlain, PAGED = MODE == kModePaged;
+    constexpr bool FUSED = MODE != kModePlain, PAGED = MODE == kModePaged, FIFO = MODE == kModeFifo;
     using C = Cfg<D, BITS, NQ, G>;
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
     __shared__ __align__(16) float qf[NQ][D];
@@ -398,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     const int g = lane >> 2, i = lane & 3;
     uint32_t* qfrag = qfrag_all[warp];
     uint8_t* ring = dyn_smem + warp * C::STAGES * C::STAGE_BYTES;
+    float4* mixbuf = reinterpret_cast<float4*>(dyn_smem + C::DYN_SMEM) + warp * kMaxMixPairs * 32;   // FIFO only
     uint64_t* bars = full_bar[warp];
     for (int idx = lane; idx < 32 * C::QSTRIDE; idx += 32) qfrag[idx] = 0u;   // unused columns stay 0
     if (lane == 0) {
@@ -561,6 +570,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         const int pw = (p1 - p0 + kWarps - 1) / kWarps;
         const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
         const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
+        // value queue: this warp's pairs from mix0 on have quantized keys and queued values
+        const int mix0 = FIFO ? max(wb, (int)(a.lqv / 32)) : 0;
         auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
         // the preceding kernel wrote blocks (and, paged, block-table entries): wait
         // before the first copy and before the first table read
@@ -655,7 +666,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
                     const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
                     uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
-                    reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + (sl * a.R + a.new_row) * D)[c16] = *src;
+                    // value queue: the new value goes to ring row (its slot position) % R
+                    const long long vr_row = FIFO && is_v ? (32 * wm.P + a.new_row) % a.R : a.new_row;
+                    reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + (sl * a.R + vr_row) * D)[c16] = *src;
                 }
             }
         }
@@ -748,42 +761,58 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 sc[2] = cb[0] + cb[1];
                 sc[3] = cb[2] + cb[3];
             }
-            float p[4];
-            softmax(sc, p, 0x1p24f);                   // scores are in units of 2^-24
-            // values, tile by tile
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                float prb[4];
-                gather(p[2 * t], p[2 * t + 1], prb);
-                uint32_t ph01, ph89, pl01, pl89;
-                split_p(prb, ph01, ph89, pl01, pl89);
-                const uint32_t ve = stage_u32 + 4 * C::TILE + t * C::ENT + eoff;
-                uint32_t pb[NBF][2];
-#pragma unroll
-                for (int f = 0; f < NBF; ++f) {
-                    const uint2 sv = lds64(ve + 32u * GB * f), zv = lds64(ve + 32u * (NGRP + GB * f));
-                    p_frag(prb, ph01, ph89, pl01, pl89, sv, zv, pb[f][0], pb[f][1], zeta[f]);
+            bool live = true;                          // the pair has a token to count in this pass
+            if constexpr (FIFO) {
+                const long long t0 = 32LL * pr;
+                if (t0 + 32 > a.lqv) {
+                    // keys quantized, some values still in the queue: keep the logits
+                    // for the second pass; here only the value-quantized tokens count
+                    mixbuf[(pr - mix0) * 32 + lane] = make_float4(sc[0], sc[1], sc[2], sc[3]);
+                    if (t0 + g >= a.lqv) sc[0] = -INFINITY;
+                    if (t0 + g + 8 >= a.lqv) sc[1] = -INFINITY;
+                    if (t0 + 16 + g >= a.lqv) sc[2] = -INFINITY;
+                    if (t0 + 24 + g >= a.lqv) sc[3] = -INFINITY;
+                    live = t0 < a.lqv;
                 }
-                uint32_t wv[W];
-                lds_words(stage_u32 + (2 + t) * C::TILE, wv);
-                if constexpr (BITS == 8) {
+            }
+            if (live) {
+                float p[4];
+                softmax(sc, p, 0x1p24f);                   // scores are in units of 2^-24
+                // values, tile by tile
 #pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        uint32_t af[4];
-                        a_frag_inline<BITS, true, W>(wv, mt, af);
-                        const int f = (16 * mt / G) / GB;
-                        mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                for (int t = 0; t < 2; ++t) {
+                    float prb[4];
+                    gather(p[2 * t], p[2 * t + 1], prb);
+                    uint32_t ph01, ph89, pl01, pl89;
+                    split_p(prb, ph01, ph89, pl01, pl89);
+                    const uint32_t ve = stage_u32 + 4 * C::TILE + t * C::ENT + eoff;
+                    uint32_t pb[NBF][2];
+#pragma unroll
+                    for (int f = 0; f < NBF; ++f) {
+                        const uint2 sv = lds64(ve + 32u * GB * f), zv = lds64(ve + 32u * (NGRP + GB * f));
+                        p_frag(prb, ph01, ph89, pl01, pl89, sv, zv, pb[f][0], pb[f][1], zeta[f]);
                     }
-                } else {
-                    uint32_t wv8[W];
+                    uint32_t wv[W];
+                    lds_words(stage_u32 + (2 + t) * C::TILE, wv);
+                    if constexpr (BITS == 8) {
 #pragma unroll
-                    for (int x = 0; x < W; ++x) wv8[x] = wv[x] >> 8;
+                        for (int mt = 0; mt < KS; ++mt) {
+                            uint32_t af[4];
+                            a_frag_inline<BITS, true, W>(wv, mt, af);
+                            const int f = (16 * mt / G) / GB;
+                            mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                        }
+                    } else {
+                        uint32_t wv8[W];
 #pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        uint32_t af[4];
-                        a_frag<BITS, true, W>(wv, wv8, mt, af);
-                        const int f = (16 * mt / G) / GB;
-                        mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                        for (int x = 0; x < W; ++x) wv8[x] = wv[x] >> 8;
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            uint32_t af[4];
+                            a_frag<BITS, true, W>(wv, wv8, mt, af);
+                            const int f = (16 * mt / G) / GB;
+                            mma16816(o[mt], af, pb[f][0], pb[f][1]);
+                        }
                     }
                 }
             }
@@ -810,6 +839,51 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             const float u1 = pow2i(24 - BITS * ((2 * mt + 1) % (8 / BITS)));
             o[mt][0] *= u0; o[mt][1] *= u0; o[mt][2] *= u1; o[mt][3] *= u1;
         }
+        if constexpr (FIFO) {
+            // ---- value queue: the queued tokens of this warp's mixed pairs, with the
+            // logits kept in the first pass and the values from the ring's fp16 rows ----
+            const int me = wb + k;                    // pairs this warp processed
+            const __half* ring_v = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + rslot * a.R * D;
+            for (int pr = mix0; pr < me; ++pr) {
+                const float4 s4 = mixbuf[(pr - mix0) * 32 + lane];
+                float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+                const long long t0 = 32LL * pr;       // the first pass counted the tokens below lqv
+                if (t0 + g < a.lqv) sc[0] = -INFINITY;
+                if (t0 + g + 8 < a.lqv) sc[1] = -INFINITY;
+                if (t0 + 16 + g < a.lqv) sc[2] = -INFINITY;
+                if (t0 + 24 + g < a.lqv) sc[3] = -INFINITY;
+                float p[4];
+                softmax(sc, p, 0x1p24f);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    float prb[4];
+                    gather(p[2 * t], p[2 * t + 1], prb);
+                    uint32_t ph01, ph89, pl01, pl89;
+                    split_p(prb, ph01, ph89, pl01, pl89);
+                    const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
+                    const long long tA = t0 + 16 * t + 2 * i, tB = tA + 8;
+                    auto row = [&](long long tok) { return ring_v + (tok % a.R) * D; };
+                    const __half* vA0 = row(tA);
+                    const __half* vA1 = row(tA + 1);
+                    const __half* vB0 = row(tB);
+                    const __half* vB1 = row(tB + 1);
+                    const bool okA0 = tA >= a.lqv, okA1 = tA + 1 >= a.lqv, okB0 = tB >= a.lqv, okB1 = tB + 1 >= a.lqv;
+                    auto ld = [&](bool ok, const __half* r, int ch) -> uint32_t {
+                        return ok ? (uint32_t)__half_as_ushort(r[ch]) : 0u;
+                    };
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        const int c0 = 16 * mt + g;
+                        uint32_t af[4];
+                        af[0] = ld(okA0, vA0, c0) | (ld(okA1, vA1, c0) << 16);
+                        af[1] = ld(okA0, vA0, c0 + 8) | (ld(okA1, vA1, c0 + 8) << 16);
+                        af[2] = ld(okB0, vB0, c0) | (ld(okB1, vB1, c0) << 16);
+                        af[3] = ld(okB0, vB0, c0 + 8) | (ld(okB1, vB1, c0 + 8) << 16);
+                        mma16816(o[mt], af, pb0, pb1);
+                    }
+                }
+            }
+        }
         // ---- this warp's residual pairs: 32 fp16 rows each, A operands straight from memory ----
         const int rw = (r1 - r0 + kWarps - 1) / kWarps;
         const int rb = min(r0 + warp * rw, r1), re = min(rb + rw, r1);
@@ -822,6 +896,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 return FUSED && rr == nrow ? a.new_k + islot * D : kr + (long long)rr * D;
             };
             auto vrow = [&](int rr) {
+                if constexpr (FIFO)   // residual row rr is slot position 32P + rr: ring row (32P + rr) % R
+                    return rr == nrow ? a.new_v + islot * D : vr + ((32 * P + rr) % a.R) * D;
                 return FUSED && rr == nrow ? a.new_v + islot * D : vr + (long long)rr * D;
             };
             build_q_frags<C, D, NQ>(nullptr, qf, qh_s, ql_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0

@@ -1,0 +1,10 @@
+// Instantiations of the tensor-core decode kernel: head_dim 128, caches whose value residual is a queue.
+#include "kivi_decode_mma_launch.cuh"
+
+namespace kivi {
+
+cudaError_t launch_decode_mma_d128q(mma_detail::Args& a, int bits, int nq, int G, int num_sms, cudaStream_t st) {
+    return mma_launch::dispatch<128, mma_detail::kModeFifo>(a, bits, nq, G, num_sms, st);
+}
+
+}  // namespace kivi

@@ -12,15 +12,16 @@ template <int D, int BB, int NN, int GG, int MODE>
 cudaError_t launch_one(typename mma_detail::ArgsOf<MODE>::type& a, int num_sms, cudaStream_t st) {
     using namespace mma_detail;
     using C = Cfg<D, BB, NN, GG>;
+    constexpr int kDyn = C::DYN_SMEM + (MODE == kModeFifo ? kMixBytes : 0);
     // opt in to the dynamic shared memory of the copy ring and size the
     // persistent grid from the occupancy, once per instance
     static int per_sm = -1;
     static cudaError_t init = [] {
         cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BB, NN, GG, MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
         if (e == cudaSuccess)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BB, NN, GG, MODE>,
-                                                              kThreads, C::DYN_SMEM);
+                                                              kThreads, kDyn);
         return e;
     }();
     if (init != cudaSuccess) return init;
@@ -37,7 +38,7 @@ cudaError_t launch_one(typename mma_detail::ArgsOf<MODE>::type& a, int num_sms, 
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3((unsigned)n);
     lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = C::DYN_SMEM;
+    lc.dynamicSmemBytes = kDyn;
     lc.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

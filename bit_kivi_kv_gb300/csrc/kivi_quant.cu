@@ -60,6 +60,7 @@ struct QuantArgs {
     long long src_slot_elems;
     long long first_block;
     long long NB, part_bytes, slot_bytes, tile_bytes;
+    long long vlimit;   // value tokens at or after this slot position stay unquantized (zero codes, step, zero)
     int G;
 };
 
@@ -192,6 +193,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     stage_rows(blk_v);
     __syncthreads();
     const int ngrp = D / G;                 // channel groups per token; G * ngrp == D entries
+    long long vfirst = 0;                   // slot position of the block's first token (value limit)
+    if constexpr (!PAGED) vfirst = (a.first_block + (long long)blockIdx.x) * G;
     for (int e = tid; e < D; e += kQuantThreads) {
         const int t = e / ngrp, gr = e % ngrp;
         const __half* row = xs + t * DP + gr * G;
@@ -202,7 +205,11 @@ __global__ void __launch_bounds__(kQuantThreads)
             mx2 = __hmax2(mx2, v);
         }
         const float2 mnf = __half22float2(mn2), mxf = __half22float2(mx2);
-        const float mn = fminf(mnf.x, mnf.y), mx = fmaxf(mxf.x, mxf.y);
+        float mn = fminf(mnf.x, mnf.y), mx = fmaxf(mxf.x, mxf.y);
+        if constexpr (!PAGED) {
+            // a value token not quantized yet: step 0 and zero point 0, so codes 0
+            if (vfirst + t >= a.vlimit) mn = mx = 0.0f;
+        }
         // entry tile of the token's code tile: ngrp rows of 16 steps, then the zeros
         __half* ent = reinterpret_cast<__half*>(part_v + tiles_bytes + (long long)(t / 16) * 64 * ngrp);
         const int at = gr * 16 + entry_pos(t % 16);
@@ -238,6 +245,75 @@ __global__ void __launch_bounds__(kQuantThreads)
             }
             reinterpret_cast<uint32_t*>(part_v)[tt * TILE_WORDS + wt] = word;
         }
+    }
+}
+
+// One value token per slot leaves the queue: token t (slot position) is read
+// from residual row t % R, quantized per group of G channels with the fixed
+// formula, and its codes and (step, zero) entries are written into block t / G,
+// whose value part holds zeros for it until now (the codes are OR-ed in).
+struct PopArgs {
+    uint8_t* cache;
+    long long t;
+    long long NB, part_bytes, slot_bytes, tile_bytes, v_resid_off;
+    int R, G;
+};
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(D) pop_value_kernel(PopArgs a) {
+    constexpr int L = (1 << BITS) - 1;
+    constexpr int W = D * BITS / 64;
+    using PP = PairPlace<BITS, true>;
+    __shared__ float x[D];
+    __shared__ float s_g[D], z_g[D];       // per group (at most D / 32 used)
+    const int c = threadIdx.x;
+    const long long slot = blockIdx.x;
+    const __half* row = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + (slot * a.R + a.t % a.R) * D;
+    x[c] = __half2float(row[c]);
+    __syncthreads();
+    const int G = a.G, ngrp = D / G, gr = c / G;
+    const long long blk = a.t / G;
+    const int tt = (int)(a.t % G), tile = tt / 16, tok = tt % 16;
+    uint8_t* part_v = a.cache + slot * a.slot_bytes + (a.NB + blk) * a.part_bytes;
+    if (c % G == 0) {
+        float mn = x[c], mx = x[c];
+        for (int j = 1; j < G; ++j) { mn = fminf(mn, x[c + j]); mx = fmaxf(mx, x[c + j]); }
+        __half* ent = reinterpret_cast<__half*>(part_v + (long long)(G / 16) * a.tile_bytes + (long long)tile * 64 * ngrp);
+        const int at = gr * 16 + entry_pos(tok);
+        float s, z;
+        group_step_zero(mn, mx, L, &s, &z, &ent[at], &ent[16 * ngrp + at]);
+        s_g[gr] = s;
+        z_g[gr] = z;
+    }
+    __syncthreads();
+    const uint32_t code = nearest_code(x[c], s_g[gr], z_g[gr], L);
+    // value tile placement: channel c = 16k + g + 8(r%2), token tok = 2i + 8(r/2) + half
+    const int k = c / 16, cc = c % 16, g = cc % 8;
+    const int r = (cc / 8) + 2 * (tok / 8), i = (tok % 8) / 2, half = tok % 2;
+    const int lane = 4 * g + i;
+    uint32_t* words = reinterpret_cast<uint32_t*>(part_v + (long long)tile * a.tile_bytes);
+    atomicOr(&words[lane * W + PP::word(k, r)], code << (PP::bit(k, r) + 16 * half));
+}
+
+// Copy nk key rows (source rows k_src0.., residual rows k_row0..) and nv value
+// rows (source rows v_src0.., tokens v_tok0.. at residual rows token % R) per slot.
+__global__ void __launch_bounds__(128) copy_rows_ring_kernel(uint8_t* cache, const __half* src_k,
+                                                             const __half* src_v, long long src_slot_elems,
+                                                             long long k_off, long long v_off,
+                                                             long long resid_slot_bytes, int D, int R,
+                                                             int k_row0, long long k_src0, int nk,
+                                                             long long v_tok0, long long v_src0, int nv) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const long long slot = blockIdx.x;
+    const int cpr = D / 8;      // 16-byte chunks per row
+    const uint4* sk = reinterpret_cast<const uint4*>(src_k + slot * src_slot_elems + k_src0 * D);
+    const uint4* sv = reinterpret_cast<const uint4*>(src_v + slot * src_slot_elems + v_src0 * D);
+    uint4* dk = reinterpret_cast<uint4*>(cache + k_off + slot * resid_slot_bytes);
+    uint4* dv = reinterpret_cast<uint4*>(cache + v_off + slot * resid_slot_bytes);
+    for (int v = threadIdx.x; v < nk * cpr; v += blockDim.x) dk[(long long)k_row0 * cpr + v] = sk[v];
+    for (int v = threadIdx.x; v < nv * cpr; v += blockDim.x) {
+        const int j = v / cpr, c = v % cpr;
+        dv[((v_tok0 + j) % R) * cpr + c] = sv[v];
     }
 }
 
@@ -279,9 +355,9 @@ cudaError_t launch_q(const typename QuantArgsOf<PAGED>::type& a, const Geometry&
 
 cudaError_t launch_quantize_blocks(const Geometry& g, uint8_t* cache, const __half* src_k,
                                    const __half* src_v, long long src_slot_elems,
-                                   long long first_block, long long nblk, cudaStream_t st) {
+                                   long long first_block, long long nblk, cudaStream_t st, long long vlimit) {
     QuantArgs a{cache, src_k, src_v, src_slot_elems, first_block, g.NB, g.part_bytes,
-                g.slot_bytes, g.tile_bytes, g.G};
+                g.slot_bytes, g.tile_bytes, vlimit, g.G};
     const dim3 grid((unsigned)nblk, (unsigned)(g.B * g.Hkv));
     return launch_q<false>(a, g, grid, st);
 }
@@ -317,6 +393,25 @@ cudaError_t launch_copy_rows_slots(const Geometry& g, uint8_t* cache, const __ha
     const long long skip = first_slot * g.resid_slot_bytes;
     copy_rows_kernel<<<nslots, 128, 0, st>>>(cache, src_k, src_v, src_slot_elems, g.k_resid_off + skip,
                                              g.v_resid_off + skip, g.resid_slot_bytes, g.D, row0, nrows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pop_values(const Geometry& g, uint8_t* cache, long long t, cudaStream_t st) {
+    PopArgs a{cache, t, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes, g.v_resid_off, g.R, g.G};
+    const unsigned slots = (unsigned)((long long)g.B * g.Hkv);
+#define KIVI_POP(DD, BB) \
+    if (g.D == DD && g.bits == BB) { pop_value_kernel<DD, BB><<<slots, DD, 0, st>>>(a); return cudaGetLastError(); }
+    KIVI_POP(128, 2) KIVI_POP(128, 4) KIVI_POP(128, 8) KIVI_POP(64, 2) KIVI_POP(64, 4) KIVI_POP(64, 8)
+#undef KIVI_POP
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_copy_rows_ring(const Geometry& g, uint8_t* cache, const __half* src_k, const __half* src_v,
+                                  long long src_slot_elems, int k_row0, long long k_src0, int nk,
+                                  long long v_tok0, long long v_src0, int nv, cudaStream_t st) {
+    copy_rows_ring_kernel<<<g.B * g.Hkv, 128, 0, st>>>(cache, src_k, src_v, src_slot_elems, g.k_resid_off,
+                                                       g.v_resid_off, g.resid_slot_bytes, g.D, g.R, k_row0,
+                                                       k_src0, nk, v_tok0, v_src0, nv);
     return cudaGetLastError();
 }
 

@@ -76,6 +76,7 @@ def _load():
         "kivi_last_error_string": (ctypes.c_char_p, []),
         "kivi_launch_count": (ctypes.c_ulonglong, []),
         "kivi_cache_set_decode_kernel": (I, [P, I]),
+        "kivi_cache_set_value_residual": (I, [P, I]),
         "kivi_decode_attn_static_ws": (I, [P, P, P, F, P]),
         "kivi_paged_bytes": (SZ, [pcfgp]),
         "kivi_paged_cache_layout": (I, [pcfgp, ctypes.POINTER(kivi_paged_layout)]),
@@ -169,6 +170,13 @@ KIVI_DECODE_AUTO, KIVI_DECODE_CUDA_CORE, KIVI_DECODE_TENSOR_CORE = 0, 1, 2
 
 def kivi_cache_set_decode_kernel(h: int, kernel: int):
     _check(lib.kivi_cache_set_decode_kernel(h, kernel))
+
+
+KIVI_VALUE_FLUSH, KIVI_VALUE_QUEUE = 0, 1
+
+
+def kivi_cache_set_value_residual(h: int, mode: int):
+    _check(lib.kivi_cache_set_value_residual(h, mode))
 
 
 # ---- paged cache ----------------------------------------------------------------
@@ -285,6 +293,10 @@ class KiviCache:
 
     def set_decode_kernel(self, kernel: int):
         kivi_cache_set_decode_kernel(self.handle, kernel)
+
+    def set_value_residual(self, mode: int):
+        """KIVI_VALUE_FLUSH (default) or KIVI_VALUE_QUEUE; on an empty cache."""
+        kivi_cache_set_value_residual(self.handle, mode)
 
     def reset(self):
         kivi_cache_reset(self.handle)

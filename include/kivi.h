@@ -239,6 +239,32 @@ typedef enum {
 kivi_status kivi_cache_set_decode_kernel(kivi_cache_t cache, int kernel);
 
 /*
+ * Value residual as a queue ([explainer] 3.2): new value tokens enter an fp16
+ * queue of R rows; once it holds R tokens, each append quantizes the oldest
+ * value on its own (per token, groups of G channels, the formula above) and
+ * drops it, so after every call the newest min(L, R) values are fp16 and the
+ * first Lv = max(L - R, 0) are quantized.  Keys keep the flush-all rule, so
+ * Lv <= Lq and tokens [Lv, Lq) have quantized keys with fp16 values.
+ *
+ *   KIVI_VALUE_FLUSH (default): values flush with the keys (the rule above).
+ *   KIVI_VALUE_QUEUE          : the queue.  Layout changes: v_resid row j of a
+ *       slot holds the value of token p with p % R == j, for p in [Lv, L);
+ *       in the value part of a block, tokens not quantized yet have all-zero
+ *       codes and step = zero = +0.  Decode runs on the tensor-core kernel only
+ *       (KIVI_ERR_UNSUPPORTED with the CUDA-core kernel selected); residual
+ *       must be <= 128.  kivi_cache_counts still reports (Lq, r) of the keys.
+ *
+ * Set on an empty cache (after create or reset; KIVI_ERR_STATE otherwise); a
+ * reset keeps the mode.  Host-only.
+ */
+typedef enum {
+    KIVI_VALUE_FLUSH = 0,
+    KIVI_VALUE_QUEUE = 1
+} kivi_value_residual;
+
+kivi_status kivi_cache_set_value_residual(kivi_cache_t cache, int mode);
+
+/*
  * Decode attention with a workspace owned by the library (the method's
  * description has no counterpart; this is an integration aid).
  *

@@ -9,16 +9,17 @@ from bit_kivi_kv_gb300.kivi import KiviCache
 from bit_kivi_kv_gb300.synth import RANGE_2_6_X10_50, SynthKV
 from oracle import layout
 from oracle.attention import decode_attention
-from oracle.cache import OracleCache
+from oracle.cache import OracleCache, OracleCacheFifo
 
 ATOL = 4e-3      # max |out - oracle|
 RTOL_L2 = 1e-3   # ||out - oracle||_2 / ||oracle||_2
 
 
 def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RANGE_2_6_X10_50,
-            sink=True, max_tokens=None, prompt=None, decode_kernel=0, fused=False):
+            sink=True, max_tokens=None, prompt=None, decode_kernel=0, fused=False, vqueue=False):
     """Prefill L tokens, then n_app x append (decoding at the steps in decode_at;
-    with fused, those steps append and decode in one kivi_append_decode call).
+    with fused, those steps append and decode in one kivi_append_decode call;
+    with vqueue, the cache keeps its value residual as a queue).
 
     Returns dict(cache, K, V, steps=[(q,k,v)], outs={step: out fp16 cpu}).
     """
@@ -26,6 +27,8 @@ def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RA
     K, V = prompt if prompt is not None else syn.prompt(L)
     cache = KiviCache(B, Hq, Hkv, D, bits, G, R, max_tokens or max(L + n_app, 1))
     cache.set_decode_kernel(decode_kernel)
+    if vqueue:
+        cache.set_value_residual(1)
     cache.prefill(K, V)
     steps, outs = [], {}
     for s in range(n_app):
@@ -39,7 +42,7 @@ def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RA
             outs[s] = cache.decode_attn(q).cpu()
     torch.cuda.synchronize()
     return dict(cache=cache, K=K, V=V, steps=steps, outs=outs, B=B, Hq=Hq, Hkv=Hkv, D=D,
-                bits=bits, G=G, R=R, L=L)
+                bits=bits, G=G, R=R, L=L, vqueue=vqueue)
 
 
 def slot_bytes(run, b, h):
@@ -56,14 +59,22 @@ def slot_bytes(run, b, h):
     vb = base + lay.blocks_per_slot * lay.part_bytes
     vp = buf[vb: vb + nblk * lay.part_bytes].view(nblk, lay.part_bytes) if nblk else buf[:0].view(0, lay.part_bytes)
     rk = buf[lay.k_resid_offset + slot * lay.resid_slot_bytes:][: n_resid * D * 2]
-    rv = buf[lay.v_resid_offset + slot * lay.resid_slot_bytes:][: n_resid * D * 2]
+    if run.get("vqueue"):
+        # the value queue: tokens [Lv, L) at ring rows position % R, in token order
+        R = run["R"]
+        L = n_quant + n_resid
+        Lv = max(L - R, 0)
+        ring = buf[lay.v_resid_offset + slot * lay.resid_slot_bytes:][: R * D * 2].view(R, D * 2)
+        rv = ring[[t % R for t in range(Lv, L)]].reshape(-1) if L > Lv else ring[:0].reshape(-1)
+    else:
+        rv = buf[lay.v_resid_offset + slot * lay.resid_slot_bytes:][: n_resid * D * 2]
     return kp.cpu().numpy(), vp.cpu().numpy(), rk.cpu().numpy(), rv.cpu().numpy()
 
 
 def oracle_slot(run, b, h, upto=None, on_step=None):
     """Replay slot (b, h) through the oracle; on_step(s, oracle_cache) after each append."""
     D, bits, G, R = run["D"], run["bits"], run["G"], run["R"]
-    oc = OracleCache(1, 1, D, bits, G, R)
+    oc = (OracleCacheFifo if run.get("vqueue") else OracleCache)(1, 1, D, bits, G, R)
     oc.prefill(run["K"][b, h][None, None].cpu().numpy(), run["V"][b, h][None, None].cpu().numpy())
     n = len(run["steps"]) if upto is None else upto
     for s in range(n):
@@ -81,7 +92,14 @@ def check_slot_bytes(run, b, h, oc):
     assert oc.n_quant == kp.shape[0] * G, (oc.n_quant, kp.shape)
     if oc.n_quant:
         ek = layout.pack_key_parts(oc.k_codes[0, 0], oc.k_s[0, 0], oc.k_z[0, 0], bits, G)
-        ev = layout.pack_value_parts(oc.v_codes[0, 0], oc.v_s[0, 0], oc.v_z[0, 0], bits, G)
+        vc, vs, vz = oc.v_codes[0, 0], oc.v_s[0, 0], oc.v_z[0, 0]
+        if vc.shape[0] < oc.n_quant:
+            # the value queue: tokens whose values are still queued read as zeros
+            pad = oc.n_quant - vc.shape[0]
+            vc = np.concatenate([vc, np.zeros((pad,) + vc.shape[1:], vc.dtype)])
+            vs = np.concatenate([vs, np.zeros((pad,) + vs.shape[1:], vs.dtype)])
+            vz = np.concatenate([vz, np.zeros((pad,) + vz.shape[1:], vz.dtype)])
+        ev = layout.pack_value_parts(vc, vs, vz, bits, G)
         if not np.array_equal(kp, ek):
             bad = np.argwhere(kp != ek)[:5]
             raise AssertionError(f"key blocks differ at (block, byte) {bad.tolist()} in slot {(b, h)}")

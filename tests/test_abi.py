@@ -204,3 +204,25 @@ def test_paged_allocator_and_checks_without_gpu(K):
         assert K.kivi_paged_seq_counts(h, 0) == (0, 0)
     finally:
         K.kivi_paged_destroy(h)
+
+
+def test_value_residual_mode_checks_without_gpu(K):
+    cfg = K.make_config(1, 2, 2, 64, 2, 32, 64, 256)
+    fake = 1 << 20
+    h = K.kivi_cache_create(cfg, fake, K.kivi_cache_bytes(cfg))
+    try:
+        K.kivi_cache_set_value_residual(h, K.KIVI_VALUE_QUEUE)
+        K.kivi_cache_set_value_residual(h, K.KIVI_VALUE_FLUSH)
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_cache_set_value_residual(h, 7)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
+    finally:
+        K.kivi_cache_destroy(h)
+    big = K.make_config(1, 2, 2, 64, 2, 32, 256, 1024)     # residual > 128
+    h = K.kivi_cache_create(big, fake, K.kivi_cache_bytes(big))
+    try:
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_cache_set_value_residual(h, K.KIVI_VALUE_QUEUE)
+        assert e.value.status == K.KIVI_ERR_UNSUPPORTED
+    finally:
+        K.kivi_cache_destroy(h)

@@ -14,7 +14,8 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU hosts t
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
 from bit_kivi_kv_gb300.kivi import (KIVI_DECODE_CUDA_CORE, KIVI_DECODE_TENSOR_CORE,  # noqa: E402
-                                    KIVI_ERR_CAPACITY, KiviCache, KiviError)
+                                    KIVI_ERR_CAPACITY, KIVI_ERR_STATE, KIVI_ERR_UNSUPPORTED, KiviCache,
+                                    KiviError)
 
 KERNELS = {"cuda_core": KIVI_DECODE_CUDA_CORE, "tensor_core": KIVI_DECODE_TENSOR_CORE}
 from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50  # noqa: E402
@@ -204,3 +205,67 @@ def test_many_short_slots(fused):
     run = run_gpu(16, 32, 16, 64, 2, 32, 64, 200, 40, seed=91, decode_at=steps,
                   decode_kernel=KIVI_DECODE_TENSOR_CORE, fused=fused)
     check_slots(run, [(0, 0), (3, 7), (7, 15), (8, 1), (12, 9), (15, 15)], steps)
+
+
+# ---- value residual as a queue ([explainer] 3.2) ---------------------------------------------
+VQ = [
+    # B, Hq, Hkv, D, bits, G, R, L, n_app
+    (2, 4, 4, 128, 2, 32, 128, 700, 140),     # ragged prompt, pops every step, key flushes
+    (2, 8, 2, 128, 4, 128, 128, 1000, 10),    # grouped queries, 4-bit, G = R = 128
+    (1, 4, 2, 64, 4, 64, 64, 300, 70),        # D64, flushes
+    (3, 2, 2, 64, 2, 32, 64, 0, 100),         # empty prompt: the queue fills, then pops
+    (2, 2, 2, 128, 2, 64, 128, 100, 5),       # prompt shorter than R: nothing quantized
+    (1, 4, 1, 128, 2, 32, 32, 515, 40),       # R = G
+    (2, 4, 2, 128, 8, 32, 64, 333, 40),       # 8-bit
+]
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("case", VQ, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}D{c[3]}b{c[4]}G{c[5]}R{c[6]}L{c[7]}n{c[8]}" for c in VQ])
+def test_value_queue(case, fused):
+    """The value queue: outputs at every step (keys flushing, values popping one
+    token per append) and the cache bytes (blocks with queued values as zeros,
+    the ring's rows) against the oracle's queue cache."""
+    B, Hq, Hkv, D, bits, G, R, L, n = case
+    steps = set(range(n))
+    run = run_gpu(B, Hq, Hkv, D, bits, G, R, L, n, seed=53 + sum(case), decode_at=steps,
+                  decode_kernel=KIVI_DECODE_TENSOR_CORE, fused=fused, vqueue=True)
+    check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
+
+
+@pytest.mark.parametrize("combo", COMBOS, ids=[f"D{c[0]}b{c[1]}nq{c[2]}G{c[3]}" for c in COMBOS])
+def test_every_value_queue_instantiation(combo):
+    """Each value-queue kernel instance: ragged prompt, a key flush, pops."""
+    D, bits, nq, G = combo
+    R = max(G, 64)
+    L = 3 * G + R + 21
+    steps = {0, 1, R - 22, R - 21}
+    run = run_gpu(2, 2 * nq, 2, D, bits, G, R, L, R - 20, seed=sum(combo) + 5, decode_at=steps,
+                  decode_kernel=KIVI_DECODE_TENSOR_CORE, fused=True, vqueue=True)
+    check_slots(run, [(0, 0), (1, 1)], steps)
+
+
+def test_value_queue_llama2_7b_layer_full_size():
+    """B8 H32 D128 2-bit G32 R128, prompt 4096, 64 fused appends with the value queue."""
+    steps = {0, 1, 63}
+    run = run_gpu(8, 32, 32, 128, 2, 32, 128, 4096, 64, seed=1001, decode_at=steps, fused=True, vqueue=True)
+    check_slots(run, [(0, 0), (3, 17), (7, 31)], steps)
+
+
+def test_value_queue_rules():
+    c = KiviCache(1, 2, 2, 64, 2, 32, 64, 256)
+    c.set_decode_kernel(KIVI_DECODE_CUDA_CORE)
+    c.set_value_residual(1)
+    syn_K = torch.zeros(1, 2, 100, 64, dtype=torch.float16, device="cuda")
+    c.prefill(syn_K, syn_K)
+    q = torch.zeros(1, 2, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(KiviError) as e:        # the queue is decoded by the tensor-core kernel only
+        c.decode_attn(q)
+    assert e.value.status == KIVI_ERR_UNSUPPORTED
+    with pytest.raises(KiviError) as e:        # the mode is set on an empty cache
+        c.set_value_residual(0)
+    assert e.value.status == KIVI_ERR_STATE
+    c.set_decode_kernel(KIVI_DECODE_TENSOR_CORE)
+    out = c.decode_attn(q)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
