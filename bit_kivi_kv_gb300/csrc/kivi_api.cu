@@ -23,6 +23,7 @@ struct kivi_cache {
     int num_sms;
     int decode_kernel;   // kivi_decode_kernel
     int value_queue;     // 1: the value residual is a queue ([explainer] 3.2)
+    int fault;           // kivi_fault for the next tensor-core decode call (test hook)
 };
 
 namespace {
@@ -133,7 +134,7 @@ kivi_status kivi_cache_create(const kivi_config* cfg, void* dev_buf, size_t byte
     if (!aligned(dev_buf, 256)) return fail(KIVI_ERR_INVALID_ARG, "cache buffer must be 256-byte aligned");
     if (bytes < (size_t)g.total_bytes)
         return fail(KIVI_ERR_CAPACITY, "cache buffer has %zu bytes, needs %lld", bytes, g.total_bytes);
-    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0, KIVI_DECODE_AUTO, 0};
+    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0, KIVI_DECODE_AUTO, 0, KIVI_FAULT_NONE};
     if (!c) return fail(KIVI_ERR_INVALID_ARG, "out of host memory");
     *out = c;
     return ok();
@@ -291,9 +292,14 @@ kivi_status decode_launch(kivi_cache_t c, const void* q, void* out, float softma
     const float scale_log2 = scale * 1.4426950408889634f;
     const kivi::DecodePlan plan = kivi::plan_decode(g, c->n_quant, n_resid, c->num_sms);
     int launches = 0;
+    kivi::FusedAppend f2 = fa;
+    if (variant == KIVI_DECODE_TENSOR_CORE && c->fault == KIVI_FAULT_COPY_STALL) {
+        f2.stall_bytes = 16;
+        c->fault = KIVI_FAULT_NONE;   // one call
+    }
     const cudaError_t e = kivi::launch_decode(g, c->buf, c->n_quant, n_resid, static_cast<const __half*>(q),
                                               static_cast<__half*>(out), scale_log2, static_cast<float*>(workspace),
-                                              plan, variant, reinterpret_cast<cudaStream_t>(stream), &launches, fa);
+                                              plan, variant, reinterpret_cast<cudaStream_t>(stream), &launches, f2);
     g_launches += (unsigned long long)launches;
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ok();
@@ -387,6 +393,13 @@ kivi_status kivi_cache_set_value_residual(kivi_cache_t c, int mode) {
     if (mode == KIVI_VALUE_QUEUE && c->geo.R > 128)
         return fail(KIVI_ERR_UNSUPPORTED, "the value queue needs residual <= 128 (residual is %d)", c->geo.R);
     c->value_queue = mode == KIVI_VALUE_QUEUE;
+    return ok();
+}
+
+kivi_status kivi_cache_set_fault(kivi_cache_t c, int fault) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    if (fault != KIVI_FAULT_NONE && fault != KIVI_FAULT_COPY_STALL) return fail(KIVI_ERR_INVALID_ARG, "unknown fault %d", fault);
+    c->fault = fault;
     return ok();
 }
 

@@ -166,6 +166,9 @@ struct FusedAppend {
     // value queue (tensor-core kernel only): >= 0 selects it; values of slot
     // positions below lqv are quantized, the rest sit in the residual ring
     long long lqv = -1;
+    // failure-detection test hook (kivi_cache_set_fault): bytes the first ring
+    // stage of CTA 0, warp 0 waits for beyond its copies
+    int stall_bytes = 0;
 };
 
 // variant: KIVI_DECODE_CUDA_CORE or KIVI_DECODE_TENSOR_CORE (resolved, never AUTO).

@@ -444,7 +444,7 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         wm.Wt = slots * wm.Ws;
         mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                            g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2,
-                           fa.k, fa.v, fa.row, fa.early_ok, fa.lqv};
+                           fa.k, fa.v, fa.row, fa.early_ok, fa.lqv, fa.stall_bytes};
         const bool fused = fa.row >= 0, fifo = fa.lqv >= 0;
         using L = cudaError_t (*)(mma_detail::Args&, int, int, int, int, cudaStream_t);
         const L launch = g.D == 128 ? (fifo ? launch_decode_mma_d128q : fused ? launch_decode_mma_d128f

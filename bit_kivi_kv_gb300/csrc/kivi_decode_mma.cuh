@@ -62,6 +62,9 @@ struct Args {
     // value queue (kModeFifo): values of slot positions >= lqv are in the
     // residual ring (row = position % R), those below are quantized
     long long lqv = -1;
+    // failure-detection test hook: the first ring stage of CTA 0, warp 0 expects
+    // this many bytes more than its copies bring, so its bounded wait runs out
+    int stall_bytes = 0;
 };
 
 struct FinishArgs {
@@ -190,6 +193,10 @@ __device__ __forceinline__ void tma_1d(void* dst, const void* src, uint32_t byte
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+// raise the phase's expected byte count without arriving
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx_u32(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
@@ -412,6 +419,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     if (lane == 0) {
 #pragma unroll
         for (int st = 0; st < C::STAGES; ++st) mbar_init(&bars[st], 1);
+        // failure-detection test hook: warp 0 of CTA 0 expects bytes that never come
+        // on its first stage, so its first bounded wait runs out
+        if (a.stall_bytes && blockIdx.x == 0 && warp == 0) mbar_expect_tx_only(smem_u32(&bars[0]), (uint32_t)a.stall_bytes);
         fence_mbar_init();
     }
     if (tid == 0) red_status = 0u;

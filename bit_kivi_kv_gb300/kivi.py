@@ -77,6 +77,7 @@ def _load():
         "kivi_launch_count": (ctypes.c_ulonglong, []),
         "kivi_cache_set_decode_kernel": (I, [P, I]),
         "kivi_cache_set_value_residual": (I, [P, I]),
+        "kivi_cache_set_fault": (I, [P, I]),
         "kivi_decode_attn_static_ws": (I, [P, P, P, F, P]),
         "kivi_paged_bytes": (SZ, [pcfgp]),
         "kivi_paged_cache_layout": (I, [pcfgp, ctypes.POINTER(kivi_paged_layout)]),
@@ -173,6 +174,12 @@ def kivi_cache_set_decode_kernel(h: int, kernel: int):
 
 
 KIVI_VALUE_FLUSH, KIVI_VALUE_QUEUE = 0, 1
+KIVI_FAULT_NONE, KIVI_FAULT_COPY_STALL = 0, 1
+
+
+def kivi_cache_set_fault(h: int, fault: int):
+    """Failure-detection test hook (kivi.h): the next decode call's first copy stage in CTA 0 times out."""
+    _check(lib.kivi_cache_set_fault(h, fault))
 
 
 def kivi_cache_set_value_residual(h: int, mode: int):

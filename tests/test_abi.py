@@ -226,3 +226,16 @@ def test_value_residual_mode_checks_without_gpu(K):
         assert e.value.status == K.KIVI_ERR_UNSUPPORTED
     finally:
         K.kivi_cache_destroy(h)
+
+
+def test_fault_hook_argument_checks_without_gpu(K):
+    cfg = K.make_config(1, 1, 1, 64, 2, 32, 32, 64)
+    h = K.kivi_cache_create(cfg, 1 << 20, K.kivi_cache_bytes(cfg))
+    try:
+        K.kivi_cache_set_fault(h, K.KIVI_FAULT_COPY_STALL)
+        K.kivi_cache_set_fault(h, K.KIVI_FAULT_NONE)
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_cache_set_fault(h, 5)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
+    finally:
+        K.kivi_cache_destroy(h)

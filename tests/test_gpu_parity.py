@@ -18,7 +18,7 @@ from bit_kivi_kv_gb300.kivi import (KIVI_DECODE_CUDA_CORE, KIVI_DECODE_TENSOR_CO
                                     KiviError)
 
 KERNELS = {"cuda_core": KIVI_DECODE_CUDA_CORE, "tensor_core": KIVI_DECODE_TENSOR_CORE}
-from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50  # noqa: E402
+from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV  # noqa: E402
 from kivi_harness import check_slots, run_gpu  # noqa: E402
 
 
@@ -269,3 +269,28 @@ def test_value_queue_rules():
     out = c.decode_attn(q)
     torch.cuda.synchronize()
     assert torch.isfinite(out.float()).all()
+
+
+def test_copy_wait_runs_out_marks_heads_and_context_stays_usable():
+    """Failure detection without a fault: the test hook makes the first copy
+    stage of CTA 0 wait for bytes that never come; its bounded wait gives up
+    (about 2 s, twice), the heads of the slot CTA 0 covers come back NaN, every
+    other head equals a clean call bit for bit, and the next call is clean."""
+    from bit_kivi_kv_gb300.kivi import KIVI_FAULT_COPY_STALL, kivi_cache_set_fault
+    B, H, D = 4, 8, 128
+    syn = SynthKV(B, H, H, D, 99, device="cuda")
+    K, V = syn.prompt(2048)
+    c = KiviCache(B, H, H, D, 2, 32, 128, 2048)
+    c.prefill(K, V)
+    q = syn.step(0)[0]
+    clean = c.decode_attn(q).clone()
+    kivi_cache_set_fault(c.handle, KIVI_FAULT_COPY_STALL)
+    bad = c.decode_attn(q)
+    torch.cuda.synchronize()
+    assert torch.isnan(bad[0, 0].float()).all()                 # slot (0, 0): CTA 0's only slot
+    rest = torch.ones(B, H, dtype=torch.bool)
+    rest[0, 0] = False
+    assert torch.equal(bad[rest], clean[rest])
+    again = c.decode_attn(q)
+    torch.cuda.synchronize()
+    assert torch.equal(again, clean)
