@@ -24,6 +24,7 @@ struct kivi_cache {
     int decode_kernel;   // kivi_decode_kernel
     int value_queue;     // 1: the value residual is a queue ([explainer] 3.2)
     int fault;           // kivi_fault for the next tensor-core decode call (test hook)
+    int max_ctas;        // cap on the tensor-core decode kernel's grid (0: none)
 };
 
 namespace {
@@ -134,7 +135,7 @@ kivi_status kivi_cache_create(const kivi_config* cfg, void* dev_buf, size_t byte
     if (!aligned(dev_buf, 256)) return fail(KIVI_ERR_INVALID_ARG, "cache buffer must be 256-byte aligned");
     if (bytes < (size_t)g.total_bytes)
         return fail(KIVI_ERR_CAPACITY, "cache buffer has %zu bytes, needs %lld", bytes, g.total_bytes);
-    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0, KIVI_DECODE_AUTO, 0, KIVI_FAULT_NONE};
+    kivi_cache* c = new (std::nothrow) kivi_cache{g, static_cast<uint8_t*>(dev_buf), 0, 0, -1, 0, KIVI_DECODE_AUTO, 0, KIVI_FAULT_NONE, 0};
     if (!c) return fail(KIVI_ERR_INVALID_ARG, "out of host memory");
     *out = c;
     return ok();
@@ -290,7 +291,8 @@ kivi_status decode_launch(kivi_cache_t c, const void* q, void* out, float softma
     const kivi::Geometry& g = c->geo;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)g.D);
     const float scale_log2 = scale * 1.4426950408889634f;
-    const kivi::DecodePlan plan = kivi::plan_decode(g, c->n_quant, n_resid, c->num_sms);
+    kivi::DecodePlan plan = kivi::plan_decode(g, c->n_quant, n_resid, c->num_sms);
+    plan.max_ctas = c->max_ctas;
     int launches = 0;
     kivi::FusedAppend f2 = fa;
     if (variant == KIVI_DECODE_TENSOR_CORE && c->fault == KIVI_FAULT_COPY_STALL) {
@@ -393,6 +395,13 @@ kivi_status kivi_cache_set_value_residual(kivi_cache_t c, int mode) {
     if (mode == KIVI_VALUE_QUEUE && c->geo.R > 128)
         return fail(KIVI_ERR_UNSUPPORTED, "the value queue needs residual <= 128 (residual is %d)", c->geo.R);
     c->value_queue = mode == KIVI_VALUE_QUEUE;
+    return ok();
+}
+
+kivi_status kivi_cache_set_max_ctas(kivi_cache_t c, int max_ctas) {
+    if (!c) return fail(KIVI_ERR_INVALID_ARG, "null handle");
+    if (max_ctas < 0) return fail(KIVI_ERR_INVALID_ARG, "max_ctas must be >= 0");
+    c->max_ctas = max_ctas;
     return ok();
 }
 

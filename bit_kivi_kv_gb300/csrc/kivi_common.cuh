@@ -150,6 +150,7 @@ struct DecodePlan {
     int n_qsplits;         // CUDA-core kernel: splits over the quantized tokens
     int n_splits;          // CUDA-core kernel: n_qsplits + (residual split ? 1 : 0)
     int num_sms;           // tensor-core kernel: sizes its persistent grid
+    int max_ctas;          // tensor-core kernel: cap on that grid (0: none)
 };
 
 DecodePlan plan_decode(const Geometry& g, long long n_quant, long long n_resid, int num_sms);

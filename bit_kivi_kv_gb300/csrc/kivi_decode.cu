@@ -441,6 +441,7 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         const long long ws0 = wm.P * wm.wq + wm.PR * wm.wr;
         wm.S0 = segment_lead(wm.wq, ws0, slots * ws0, plan.num_sms);
         wm.Ws = wm.S0 + ws0;
+        wm.n = plan.max_ctas;   // 0: the launch sizes the grid
         wm.Wt = slots * wm.Ws;
         mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                            g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2,

@@ -28,6 +28,7 @@ cudaError_t launch_one(typename mma_detail::ArgsOf<MODE>::type& a, int num_sms, 
     // slots of the largest weight (paged calls: wm.Ws is the largest slot's)
     const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;
     long long n = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
+    if (a.wm.n > 0 && a.wm.n < n) n = a.wm.n;                         // the caller's cap on the grid
     const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
     if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every CTA owns a unit
     if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot

@@ -78,6 +78,7 @@ def _load():
         "kivi_cache_set_decode_kernel": (I, [P, I]),
         "kivi_cache_set_value_residual": (I, [P, I]),
         "kivi_cache_set_fault": (I, [P, I]),
+        "kivi_cache_set_max_ctas": (I, [P, I]),
         "kivi_decode_attn_static_ws": (I, [P, P, P, F, P]),
         "kivi_paged_bytes": (SZ, [pcfgp]),
         "kivi_paged_cache_layout": (I, [pcfgp, ctypes.POINTER(kivi_paged_layout)]),
@@ -175,6 +176,10 @@ def kivi_cache_set_decode_kernel(h: int, kernel: int):
 
 KIVI_VALUE_FLUSH, KIVI_VALUE_QUEUE = 0, 1
 KIVI_FAULT_NONE, KIVI_FAULT_COPY_STALL = 0, 1
+
+
+def kivi_cache_set_max_ctas(h: int, max_ctas: int):
+    _check(lib.kivi_cache_set_max_ctas(h, max_ctas))
 
 
 def kivi_cache_set_fault(h: int, fault: int):

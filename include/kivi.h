@@ -239,6 +239,15 @@ typedef enum {
 kivi_status kivi_cache_set_decode_kernel(kivi_cache_t cache, int kernel);
 
 /*
+ * Cap the tensor-core decode kernel's persistent grid at max_ctas CTAs (0, the
+ * default: SMs x resident CTAs per SM), e.g. to leave SMs to other work on the
+ * GPU.  The result does not depend on the grid beyond fp32 summation order
+ * (the split of a slot over CTAs changes, the arithmetic per token does not).
+ * Host-only; KIVI_ERR_INVALID_ARG for a negative cap.
+ */
+kivi_status kivi_cache_set_max_ctas(kivi_cache_t cache, int max_ctas);
+
+/*
  * Value residual as a queue ([explainer] 3.2): new value tokens enter an fp16
  * queue of R rows; once it holds R tokens, each append quantizes the oldest
  * value on its own (per token, groups of G channels, the formula above) and

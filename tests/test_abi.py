@@ -234,6 +234,11 @@ def test_fault_hook_argument_checks_without_gpu(K):
     try:
         K.kivi_cache_set_fault(h, K.KIVI_FAULT_COPY_STALL)
         K.kivi_cache_set_fault(h, K.KIVI_FAULT_NONE)
+        K.kivi_cache_set_max_ctas(h, 3)
+        K.kivi_cache_set_max_ctas(h, 0)
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_cache_set_max_ctas(h, -1)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
         with pytest.raises(K.KiviError) as e:
             K.kivi_cache_set_fault(h, 5)
         assert e.value.status == K.KIVI_ERR_INVALID_ARG

@@ -294,3 +294,29 @@ def test_copy_wait_runs_out_marks_heads_and_context_stays_usable():
     again = c.decode_attn(q)
     torch.cuda.synchronize()
     assert torch.equal(again, clean)
+
+
+def test_split_invariance():
+    """The same decode call on grids of 1, 7, 64 CTAs and the default: a slot's
+    split over CTAs changes, its arithmetic per token does not, so the outputs
+    agree to fp32 summation order (within 1e-4, or one fp16 ulp of the value
+    where that is larger)."""
+    from bit_kivi_kv_gb300.kivi import kivi_cache_set_max_ctas
+    B, H, D = 2, 8, 128
+    syn = SynthKV(B, H, H, D, 7, device="cuda")
+    K, V = syn.prompt(3000)
+    c = KiviCache(B, H, H, D, 2, 32, 128, 3010)
+    c.prefill(K, V)
+    for s in range(5):
+        _, k, v = syn.step(s)
+        c.append(k, v)
+    q = syn.step(5)[0]
+    ref = c.decode_attn(q).float()
+    for cap in (1, 7, 64):
+        kivi_cache_set_max_ctas(c.handle, cap)
+        out = c.decode_attn(q).float()
+        ulp16 = torch.exp2(torch.floor(torch.log2(ref.abs().clamp(min=2.0 ** -14))) - 10)   # fp16 spacing at |ref|
+        allowed = torch.clamp(ulp16, min=1e-4)
+        assert torch.all((out - ref).abs() <= allowed), (cap, (out - ref).abs().max().item())
+    kivi_cache_set_max_ctas(c.handle, 0)
+    assert torch.equal(c.decode_attn(q).float(), ref)
