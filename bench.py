@@ -243,6 +243,34 @@ def oracle_sample(w, n_slots=None, budget_s=15.0, step_seed=0):
     return tokens / w["Hkv"], time.perf_counter() - t0, done
 
 
+def sink_mass_sample(w, n_slots=8):
+    """Attention weight of the sink token (token 0) at the first decode step,
+    from the oracle, over n_slots (batch, kv-head) slots of the workload's
+    generator: (median, all).  None for workloads without a sink."""
+    if not w["sink"]:
+        return None
+    import math
+    import numpy as np
+    from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV
+    from oracle.attention import decode_attention
+    from oracle.cache import OracleCache
+    outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
+    L = min(_lengths(w))
+    masses = []
+    for j in range(n_slots):
+        syn = SynthKV(1, 1, 1, w["D"], seed=w["seed"] * 1000 + j, outliers=outl, sink=True, device="cpu")
+        K, V = syn.prompt(L)
+        oc = OracleCache(1, 1, w["D"], w["bits"], w["G"], w["R"])
+        oc.prefill(K.numpy(), V.numpy())
+        q, k, v = (t.numpy() for t in syn.step(0))
+        oc.append(k, v)
+        Kh = oc.keys_hat()
+        _, lse = decode_attention(q, Kh, oc.values_hat())
+        l0 = (Kh[0, 0, 0] * q[0, 0].astype(np.float64)).sum() / math.sqrt(w["D"])
+        masses.append(float(np.exp(l0 - lse[0, 0])))
+    return float(np.median(masses)), masses
+
+
 def run_reference(args, w):
     world, rank, _ = _dist_env()
     if rank != 0:
@@ -392,6 +420,11 @@ def run_ours(args, w):
         "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sm = sink_mass_sample(w)
+        if sm is not None:
+            result["sink_mass"] = {"median": sm[0], "slots": len(sm[1]),
+                                   "how": "oracle attention weight of token 0 at the first decode step, "
+                                          "one head per slot, prompt of the workload's shortest length"}
         tok, secs, done = oracle_sample(w, budget_s=args.cpu_budget)
         result["cpu_baseline"] = {
             "value": tok / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
