@@ -320,3 +320,14 @@ def test_split_invariance():
         assert torch.all((out - ref).abs() <= allowed), (cap, (out - ref).abs().max().item())
     kivi_cache_set_max_ctas(c.handle, 0)
     assert torch.equal(c.decode_attn(q).float(), ref)
+
+
+def test_maximum_slot_count():
+    """2047 x 32 = 65504 (batch, kv-head) slots, next to the 65535 limit the
+    quantize grid's y dimension sets: prompt 96 (one quantized block, a full
+    residual), 3 appends (the first flushes), decode; sampled slots against
+    the oracle."""
+    run = run_gpu(2047, 32, 32, 64, 2, 32, 64, 96, 3, seed=13, decode_at={2},
+                  outliers=FIXED_4_X20, sink=False)
+    assert run["cache"].counts() == (96, 3)
+    check_slots(run, [(0, 0), (1023, 17), (2046, 31)], {2})
