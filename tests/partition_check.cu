@@ -1,0 +1,125 @@
+// Host-only check of the decode partition (the work map in kivi_common.cuh),
+// built and run by tests/test_partition.py.  For random dense and ragged calls
+// it walks every CTA's weight range the way the decode kernel does and checks
+// that every unit (tile pair or residual pair) of every slot is owned by
+// exactly one CTA, that a slot's partial indices are 0 .. parts-1 with no gap,
+// and that no slot has more partials than the workspace holds.
+#include <cstdio>
+#include <random>
+#include <vector>
+
+#include "kivi_common.cuh"
+
+using namespace kivi;
+
+namespace {
+
+struct Slot {
+    long long P, PR, w0, Ws;
+};
+
+// the grid size rule of the launch (occupancy, then the two bounds, then a cap)
+long long grid_size(long long Wt, long long wmax, long long slots_of_max, long long resident, long long cap) {
+    long long n = resident;
+    if (cap > 0 && cap < n) n = cap;
+    if (n > Wt / wmax) n = Wt / wmax;
+    if (n > (kMaxSplits - 1) * slots_of_max) n = (kMaxSplits - 1) * slots_of_max;
+    return n < 1 ? 1 : n;
+}
+
+bool check(const std::vector<Slot>& slots, const WorkMap& wm, int trial) {
+    std::vector<std::vector<int>> owner(slots.size()), part(slots.size());
+    for (size_t s = 0; s < slots.size(); ++s) {
+        owner[s].assign((size_t)(slots[s].P + slots[s].PR), -1);
+        part[s].assign((size_t)(slots[s].P + slots[s].PR), -1);
+    }
+    size_t si = 0;
+    for (long long c = 0; c < wm.n; ++c) {
+        long long pos = map_begin(wm, c);
+        const long long pe = map_begin(wm, c + 1);
+        while (pos < pe) {
+            while (si + 1 < slots.size() && slots[si + 1].w0 <= pos) ++si;   // the slot holding pos
+            while (si > 0 && slots[si].w0 > pos) --si;
+            const Slot& sl = slots[si];
+            const long long NU = sl.P + sl.PR;
+            const long long u0 = first_unit_at_p(sl.P, wm.wq, wm.wr, wm.S0, pos - sl.w0);
+            if (u0 >= NU) { pos = sl.w0 + sl.Ws; continue; }
+            if (sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, u0) >= pe) break;
+            const long long u1 = first_unit_at_p(sl.P, wm.wq, wm.wr, wm.S0, pe - sl.w0 < sl.Ws ? pe - sl.w0 : sl.Ws);
+            const long long p = c - map_owner(wm, sl.w0 + wm.S0);
+            for (long long u = u0; u < u1; ++u) {
+                if (owner[si][(size_t)u] != -1) { std::printf("trial %d: unit owned twice\n", trial); return false; }
+                owner[si][(size_t)u] = (int)c;
+                part[si][(size_t)u] = (int)p;
+            }
+            pos = u1 >= NU ? sl.w0 + sl.Ws : sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, u1);
+        }
+    }
+    for (size_t s = 0; s < slots.size(); ++s) {
+        const Slot& sl = slots[s];
+        const long long last = sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, sl.P + sl.PR - 1);
+        const long long nparts = map_owner(wm, last) - map_owner(wm, sl.w0 + wm.S0) + 1;
+        if (nparts < 1 || nparts > kPartialSlots) { std::printf("trial %d: %lld parts\n", trial, nparts); return false; }
+        std::vector<int> seen((size_t)nparts, 0);
+        for (size_t u = 0; u < owner[s].size(); ++u) {
+            if (owner[s][u] < 0) { std::printf("trial %d: unit not owned\n", trial); return false; }
+            if (part[s][u] < 0 || part[s][u] >= nparts) { std::printf("trial %d: part out of range\n", trial); return false; }
+            seen[(size_t)part[s][u]] = 1;
+        }
+        for (long long p = 0; p < nparts; ++p)
+            if (!seen[(size_t)p]) { std::printf("trial %d: part %lld has no unit\n", trial, p); return false; }
+    }
+    return true;
+}
+
+}  // namespace
+
+int main() {
+    std::mt19937_64 rng(12345);
+    auto pick = [&](long long lo, long long hi) { return lo + (long long)(rng() % (unsigned long long)(hi - lo + 1)); };
+    const long long wqs[] = {40, 64, 96, 136, 288}, wrs[] = {256, 512};
+    for (int trial = 0; trial < 4000; ++trial) {
+        WorkMap wm{};
+        wm.wq = wqs[pick(0, 4)];
+        wm.wr = wrs[pick(0, 1)];
+        const bool ragged = trial % 2 == 1;
+        const long long nslots = pick(1, trial % 7 == 0 ? 2000 : 300);
+        std::vector<Slot> slots((size_t)nslots);
+        long long start = 0, ws_min = -1, ws_max = 0;
+        const long long P0 = pick(0, 400), PR0 = pick(P0 == 0 ? 1 : 0, 4);
+        for (auto& s : slots) {
+            s.P = ragged ? pick(0, 400) : P0;
+            s.PR = ragged ? pick(s.P == 0 ? 1 : 0, 4) : PR0;
+            const long long w = s.P * wm.wq + s.PR * wm.wr;
+            if (ws_min < 0 || w < ws_min) ws_min = w;
+        }
+        long long wt0 = 0;
+        for (auto& s : slots) wt0 += s.P * wm.wq + s.PR * wm.wr;
+        const int num_sms = (int)pick(1, 152);
+        wm.S0 = segment_lead(wm.wq, ws_min, wt0, num_sms);
+        for (auto& s : slots) {
+            s.w0 = start;
+            s.Ws = wm.S0 + s.P * wm.wq + s.PR * wm.wr;
+            start += s.Ws;
+            if (s.Ws > ws_max) ws_max = s.Ws;
+        }
+        wm.Wt = start;
+        wm.Ws = ws_max;
+        wm.P = slots[0].P;
+        wm.PR = slots[0].PR;
+        const long long resident = (long long)num_sms * pick(1, 4);
+        wm.n = grid_size(wm.Wt, wm.wq > wm.wr ? wm.wq : wm.wr, wm.Wt / ws_max, resident,
+                         trial % 5 == 0 ? pick(1, 64) : 0);
+        if (!check(slots, wm, trial)) return 1;
+        if (!ragged) {
+            // the dense helpers agree with the walk
+            for (long long s = 0; s < nslots; ++s) {
+                if (slot_first_cta(wm, s) != map_owner(wm, slots[(size_t)s].w0 + wm.S0)) { std::printf("first cta\n"); return 1; }
+                const long long last = slots[(size_t)s].w0 + unit_start(wm, wm.P + wm.PR - 1);
+                if (slot_parts(wm, s) != (int)(map_owner(wm, last) - slot_first_cta(wm, s) + 1)) { std::printf("parts\n"); return 1; }
+            }
+        }
+    }
+    std::printf("ok\n");
+    return 0;
+}
