@@ -78,8 +78,10 @@ typedef enum {
  * Cache shape.  Supported: bits in {2, 4, 8}; head_dim in {64, 128};
  * group in {32, 64, 128} with head_dim % group == 0 (value groups) and
  * residual % group == 0, residual >= group; n_q_heads / n_kv_heads in
- * {1, 2, 4}; max_tokens >= 1 is the most tokens (quantized + residual) one
- * sequence may hold.  All sequences of the batch have the same length.
+ * {1, 2, 4}; batch * n_kv_heads <= 65535; 1 <= max_tokens <= 2^30 is the
+ * most tokens (quantized + residual) one sequence may hold.  All sequences of
+ * the batch have the same length (sequences of different lengths: the paged
+ * cache below).
  * Typical group sizes 32-128 and residual lengths 64-128 follow
  * [explainer] 5.2.
  */
