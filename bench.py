@@ -243,6 +243,46 @@ def oracle_sample(w, n_slots=None, budget_s=15.0, step_seed=0):
     return tokens / w["Hkv"], time.perf_counter() - t0, done
 
 
+def _oracle_worker(job):
+    """One process of the all-cores oracle run: its own slots, its own budget."""
+    name, budget_s, idx = job
+    t0 = time.time()
+    tok, secs, done = oracle_sample(WORKLOADS[name], budget_s=budget_s, step_seed=idx)
+    return tok, done, t0 + 0.0, time.time()
+
+
+def host_cores():
+    """Cores of this host: os.cpu_count() and the ones this process may run on (nproc)."""
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        usable = os.cpu_count() or 1
+    return {"cpu_count": os.cpu_count(), "nproc": usable}
+
+
+def oracle_all_cores(name, workers, budget_s):
+    """The oracle on every usable core at once: one process per core (spawned,
+    single-threaded numpy), each on its own (batch, kv-head) slots for about
+    budget_s seconds of work.  KV tokens of all processes / the wall time from
+    the first start to the last finish."""
+    import multiprocessing as mp
+    env = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in env:
+        os.environ[k] = "1"
+    try:
+        with mp.get_context("spawn").Pool(workers) as pool:
+            res = pool.map(_oracle_worker, [(name, budget_s, 1 + i) for i in range(workers)])
+    finally:
+        for k, v in env.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    tok = sum(r[0] for r in res)
+    wall = max(r[3] for r in res) - min(r[2] for r in res)
+    return tok / wall, wall, sum(r[1] for r in res)
+
+
 def sink_mass_sample(w, n_slots=8):
     """Attention weight of the sink token (token 0) at the first decode step,
     from the oracle, over n_slots (batch, kv-head) slots of the workload's
@@ -288,7 +328,8 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config(w, args.workload),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "threads": 1, "host_cores": host_cores(),
+                         "kind": "oracle",
                          "sample": f"per step one (batch, kv-head) slot of {args.workload}: prefill "
                                    f"{w['prompt']} + {w['decode']} x (append + attention); "
                                    f"KV tokens counted per slot / {w['Hkv']} heads"},
@@ -394,6 +435,16 @@ def run_ours(args, w):
     peak, peak_kind = _peaks()
     traffic = _profile_traffic(args.workload + ("-paged" if paged and not w.get("paged") else ""))
 
+    # ---- the other workloads' decode calls, measured the same way (1 GPU only) ----
+    configs = None
+    if world == 1 and args.configs and args.workload in FIVE:
+        configs = {args.workload: {"us": dec_ms * 1e3, "bytes": bytes_call, "gbs": achieved,
+                                   "frac": achieved / peak, "context": "after the step's decode calls",
+                                   "note": "the headline: same numbers as decode_call / roofline"}}
+        for name in FIVE:
+            if name != args.workload:
+                configs[name] = decode_call_config(name, dev, torch, peak)
+
     # ---- e2e through the Python API from pinned host memory ----
     barrier()
     e2e = eng.e2e(max(3, min(args.steps, 10)))
@@ -425,6 +476,10 @@ def run_ours(args, w):
                          else "decode_mma_kernel + finish_kernel (tensor cores)")},
         "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
     }
+    if configs is not None:
+        result["configs"] = {"peak_gbs": peak, "how": "decode call: CUDA-graph replay over rotated caches, "
+                                                      "CUDA events; frac of the measured copy bandwidth",
+                             **configs}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sm = sink_mass_sample(w)
         if sm is not None:
@@ -432,16 +487,88 @@ def run_ours(args, w):
                                    "how": "oracle attention weight of token 0 at the first decode step, "
                                           "one head per slot, prompt of the workload's shortest length"}
         tok, secs, done = oracle_sample(w, budget_s=args.cpu_budget)
+        hc = host_cores()
         result["cpu_baseline"] = {
-            "value": tok / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "value": tok / secs, "unit": UNIT, "cores": 1, "threads": 1, "host_cores": hc, "kind": "oracle",
             "sample": f"{done} (batch, kv-head) slot(s) of {args.workload}: prefill {w['prompt']} + "
-                      f"{w['decode']} x (append + fp64 attention), {secs:.1f} s; KV tokens per slot "
+                      f"{w['decode']} x (append + fp64 attention), {secs:.1f} s on one core; KV tokens per slot "
                       f"counted / {w['Hkv']} heads"}
+        if args.cpu_all_cores and hc["nproc"] > 1:
+            v_all, wall, n_all = oracle_all_cores(args.workload, hc["nproc"], args.cpu_budget / 2)
+            result["cpu_baseline"]["all_cores"] = {
+                "value": v_all, "unit": UNIT, "cores": hc["nproc"], "slots": n_all,
+                "how": f"{hc['nproc']} spawned single-threaded oracle processes, one per usable core, each on "
+                       f"its own slots for ~{args.cpu_budget / 2:.0f} s; all their KV tokens / {wall:.1f} s wall"}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# the method's five workloads (the headline is measured by run_ours itself)
+FIVE = ("tiny-b1h1d64", "llama2-7b-layer", "llama2-13b-40layer", "llama3-8b-gqa", "long-context")
+
+
+def decode_call_config(name, dev, torch, peak):
+    """One workload's decode call, measured as the headline's is: caches built once
+    (prefill of the prompt, then one append, which flushes where the residual is
+    full), then decode calls replayed back to back from a CUDA graph over rotated
+    caches (each call of the large workloads reads more than L2 holds), timed with
+    CUDA events.  Returns {us, bytes, gbs, frac, kv_tokens_per_s, calls}."""
+    from bit_kivi_kv_gb300.kivi import KiviCache
+    from bit_kivi_kv_gb300.synth import FIXED_4_X20, RANGE_2_6_X10_50, SynthKV
+    w = dict(WORKLOADS[name], decode=1)
+    outl = FIXED_4_X20 if w["outliers"] == "fixed4x20" else RANGE_2_6_X10_50
+    nl = {"tiny-b1h1d64": 4, "long-context": 1}.get(name, 2)
+    caches, qs, outs = [], [], []
+    for li in range(nl):
+        syn = SynthKV(w["B"], w["Hq"], w["Hkv"], w["D"], seed=replica_seed(w, li, 0), outliers=outl,
+                      sink=w["sink"], device=dev)
+        Kp, Vp = syn.prompt(w["prompt"])
+        q, k, v = syn.step(0)
+        c = KiviCache(w["B"], w["Hq"], w["Hkv"], w["D"], w["bits"], w["G"], w["R"], w["prompt"] + 1, device=dev)
+        c.prefill(Kp, Vp)
+        c.append(k, v)
+        torch.cuda.synchronize()
+        del Kp, Vp
+        caches.append(c)
+        qs.append(q)
+        outs.append(torch.empty_like(q))
+    rounds = max(1, 16 // nl)
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for c, q, o in zip(caches, qs, outs):
+            c.decode_attn(q, out=o)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(rounds):
+                for c, q, o in zip(caches, qs, outs):
+                    c.decode_attn(q, out=o)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = 40 if name == "tiny-b1h1d64" else 8
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    calls = reps * rounds * nl
+    us = e0.elapsed_time(e1) * 1e3 / calls
+    nbytes = _bytes_last_call(w)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    out = {"us": us, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak,
+           "kv_tokens_per_s": _tokens_last_call(w) / (us * 1e-6), "calls": calls,
+           "caches_rotated": nl, "context": w["prompt"] + 1}
+    if name == "tiny-b1h1d64":
+        out["note"] = "latency-bound (12.8 KB per call): no roofline claim"
+    del caches, qs, outs, g
+    torch.cuda.empty_cache()
+    return out
 
 
 def _launches_in(step, K, stream, torch):
@@ -702,6 +829,10 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-all-cores", type=int, default=1,
+                    help="also time the oracle on every usable core (1, default) or not (0)")
+    ap.add_argument("--configs", type=int, default=1,
+                    help="also measure the decode call of the other workloads of the method's five (1, default)")
     ap.add_argument("--profile", action="store_true", help="small eager run for ncu captures")
     ap.add_argument("--separate-append", action="store_true",
                     help="decode steps as kivi_append + kivi_decode_attn instead of kivi_append_decode")

@@ -19,7 +19,7 @@ struct kivi_cache {
     uint8_t* buf;
     long long n_quant;
     long long n_resid;
-    int device;      // -1 until the first decode queries it
+    int device;      // -1 until the first launching call records the current device
     int num_sms;
     int decode_kernel;   // kivi_decode_kernel
     int value_queue;     // 1: the value residual is a queue ([explainer] 3.2)
@@ -52,6 +52,26 @@ kivi_status cuda_fail(cudaError_t e, const char* what) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+
+// The cache's device: the device current at the handle's first call that
+// launches work (its SM count is taken then too).  Every later launching call
+// must find that device current, since the kernels run on the current device
+// and the cache buffer lives on its own.
+kivi_status ensure_device(kivi_cache_t c) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    if (c->device < 0) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "device query");
+        c->device = dev;
+        c->num_sms = sms;
+    } else if (dev != c->device) {
+        return fail(KIVI_ERR_INVALID_ARG, "the cache is on device %d but device %d is current", c->device, dev);
+    }
+    return KIVI_OK;
+}
 
 }  // namespace
 
@@ -169,6 +189,8 @@ kivi_status kivi_prefill(kivi_cache_t c, const void* K, const void* V, long long
     if (L == 0) return ok();
     if (!K || !V) return fail(KIVI_ERR_INVALID_ARG, "null K or V");
     if (!aligned(K, 16) || !aligned(V, 16)) return fail(KIVI_ERR_INVALID_ARG, "K and V must be 16-byte aligned");
+    const kivi_status sdev = ensure_device(c);
+    if (sdev != KIVI_OK) return sdev;
     const kivi::Geometry& g = c->geo;
     const long long over = L > g.R ? L - g.R : 0;
     const long long Lq = (over + g.G - 1) / g.G * g.G;
@@ -215,6 +237,8 @@ kivi_status kivi_append(kivi_cache_t c, const void* k, const void* v, kivi_strea
     const kivi::Geometry& g = c->geo;
     if (c->n_quant + c->n_resid + 1 > g.max_tokens)
         return fail(KIVI_ERR_CAPACITY, "cache already holds max_tokens (%lld) tokens", g.max_tokens);
+    const kivi_status sdev = ensure_device(c);
+    if (sdev != KIVI_OK) return sdev;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (c->value_queue) {
         bool unused;
@@ -272,18 +296,6 @@ kivi_status decode_checks(kivi_cache_t c, const void* q, void* out, float softma
     return KIVI_OK;
 }
 
-// The device and its SM count, queried once per handle.
-kivi_status ensure_device(kivi_cache_t c) {
-    if (c->device < 0) {
-        int dev = 0, sms = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return cuda_fail(e, "device query");
-        c->device = dev;
-        c->num_sms = sms;
-    }
-    return KIVI_OK;
-}
 
 // Launch a decode call over n_resid residual rows (fa.row < n_resid: a fused append's row).
 kivi_status decode_launch(kivi_cache_t c, const void* q, void* out, float softmax_scale, void* workspace,
@@ -431,6 +443,8 @@ namespace kivi {
 kivi_status report_error(kivi_status st, const char* msg) { return fail(st, "%s", msg); }
 
 void count_launches(int n) { g_launches += (unsigned long long)n; }
+
+kivi_status cache_device(kivi_cache* c) { return ensure_device(c); }
 
 size_t decode_workspace_need(const kivi_cache* c) {
     const Geometry& g = c->geo;

@@ -233,5 +233,7 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
 kivi_status report_error(kivi_status st, const char* msg);
 void count_launches(int n);   // adds to kivi_launch_count()
 size_t decode_workspace_need(const struct ::kivi_cache* c);
+// Checks that the cache's device is current (recording it at the first call).
+kivi_status cache_device(struct ::kivi_cache* c);
 
 }  // namespace kivi

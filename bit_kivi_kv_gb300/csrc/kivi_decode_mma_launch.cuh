@@ -3,31 +3,52 @@
 // instances of one head_dim; included by the per-head_dim instantiation files.
 #pragma once
 
+#include <mutex>
+
 #include "kivi_decode_mma.cuh"
 
 namespace kivi {
 namespace mma_launch {
+
+// Per-device set-up of one kernel instance: the opt-in to its dynamic shared
+// memory and its resident CTAs per SM are properties of a device, so they are
+// taken once per device (with that device current) and kept per device.
+constexpr int kMaxDevices = 64;
+struct InstanceSetup {
+    std::mutex mu;
+    int per_sm[kMaxDevices] = {};        // 0: not set up on that device yet
+};
 
 template <int D, int BB, int NN, int GG, int MODE>
 cudaError_t launch_one(typename mma_detail::ArgsOf<MODE>::type& a, int num_sms, cudaStream_t st) {
     using namespace mma_detail;
     using C = Cfg<D, BB, NN, GG>;
     constexpr int kDyn = C::DYN_SMEM + (MODE == kModeFifo ? kMixBytes : 0);
-    // opt in to the dynamic shared memory of the copy ring and size the
-    // persistent grid from the occupancy, once per instance
-    static int per_sm = -1;
-    static cudaError_t init = [] {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BB, NN, GG, MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BB, NN, GG, MODE>,
-                                                              kThreads, kDyn);
-        return e;
-    }();
-    if (init != cudaSuccess) return init;
+    static InstanceSetup setup;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int per_sm;
+    {
+        std::lock_guard<std::mutex> lock(setup.mu);
+        per_sm = setup.per_sm[dev];
+        if (per_sm == 0) {
+            // opt in to the dynamic shared memory of the copy ring and size the
+            // persistent grid from the occupancy on this device
+            e = cudaFuncSetAttribute(decode_mma_kernel<D, BB, NN, GG, MODE>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BB, NN, GG, MODE>,
+                                                                  kThreads, kDyn);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) per_sm = 1;
+            setup.per_sm[dev] = per_sm;
+        }
+    }
     // slots of the largest weight (paged calls: wm.Ws is the largest slot's)
     const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;
-    long long n = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
+    long long n = (long long)num_sms * per_sm;
     if (a.wm.n > 0 && a.wm.n < n) n = a.wm.n;                         // the caller's cap on the grid
     const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
     if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every CTA owns a unit

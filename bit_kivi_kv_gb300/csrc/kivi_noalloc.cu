@@ -40,6 +40,9 @@ extern "C" kivi_status kivi_decode_attn_static_ws(kivi_cache_t cache, const void
                  need, kStaticWorkspaceBytes);
         return kivi::report_error(KIVI_ERR_CAPACITY, msg);
     }
+    // the workspace must be the cache's device's array: that device must be current
+    const kivi_status sdev = kivi::cache_device(cache);
+    if (sdev != KIVI_OK) return sdev;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -49,14 +52,18 @@ extern "C" kivi_status kivi_decode_attn_static_ws(kivi_cache_t cache, const void
     if (dev < 0 || dev >= kMaxDevices) return kivi::report_error(KIVI_ERR_UNSUPPORTED, "device index too large");
     void* ws = nullptr;
     {
-        // First call on this device (with it current): look up the array's address.
+        // First call on this device (with it current): look up the array's
+        // address.  The library's modules load lazily, so this lookup is also
+        // what loads the array onto the device and reserves its bytes there.
         std::lock_guard<std::mutex> lock(g_setup_mutex);
         ws = g_scratch_addr[dev];
         if (!ws) {
             e = cudaGetSymbolAddress(&ws, kivi_static_decode_workspace);
             if (e != cudaSuccess || !ws) {
-                snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the static workspace: %s",
-                         cudaGetErrorString(e));
+                snprintf(msg, sizeof msg,
+                         "could not load the %zu-byte static decode workspace on device %d "
+                         "(cudaGetSymbolAddress: %s)",
+                         kStaticWorkspaceBytes, dev, cudaGetErrorString(e));
                 return kivi::report_error(KIVI_ERR_CUDA, msg);
             }
             g_scratch_addr[dev] = ws;

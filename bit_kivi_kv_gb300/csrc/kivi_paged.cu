@@ -94,14 +94,20 @@ struct kivi_paged {
 
 namespace {
 
+// The cache's device: the device current at the handle's first launching
+// call; later launching calls must find it current.
 kivi_status paged_device(kivi_paged* c) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
     if (c->device < 0) {
-        int dev = 0, sms = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "device query");
         c->device = dev;
         c->num_sms = sms;
+    } else if (dev != c->device) {
+        return failf(KIVI_ERR_INVALID_ARG, "the cache is on device %d but device %d is current", c->device, dev);
     }
     return KIVI_OK;
 }
@@ -192,6 +198,10 @@ kivi_status kivi_paged_add(kivi_paged_t c, const void* K, const void* V, long lo
                      nblk, g.NB);
     if (nblk > (long long)c->free_pages.size())
         return failf(KIVI_ERR_CAPACITY, "prompt needs %lld pages, %zu are free", nblk, c->free_pages.size());
+    if (L > 0) {
+        const kivi_status sdev = paged_device(c);
+        if (sdev != KIVI_OK) return sdev;
+    }
     const int s = c->free_seqs.back();
     SeqState& sq = c->seqs[(size_t)s];
     sq.pages.clear();

@@ -273,15 +273,20 @@ class KiviCache:
 
     def __init__(self, batch, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_tokens,
                  device="cuda"):
-        import torch
         self.cfg = make_config(batch, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_tokens)
         nbytes = kivi_cache_bytes(self.cfg)
         if nbytes == 0:
             raise KiviError(KIVI_ERR_INVALID_ARG, kivi_last_error_string())
         self.layout = kivi_cache_layout(self.cfg)
-        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        self.workspace = torch.empty(kivi_decode_workspace_bytes(self.cfg), dtype=torch.uint8, device=device)
+        self.buffer = self._alloc(nbytes, device)
+        self.workspace = self._alloc(kivi_decode_workspace_bytes(self.cfg), device)
         self.handle = kivi_cache_create(self.cfg, self.buffer.data_ptr(), nbytes)
+
+    def _alloc(self, nbytes, device):
+        """Device bytes for the cache buffer and the workspace (256-byte aligned);
+        a subclass may place them differently (the tests put guard bands around them)."""
+        import torch
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -343,17 +348,21 @@ class KiviPagedCache:
 
     def __init__(self, max_seqs, n_q_heads, n_kv_heads, head_dim, bits, group, residual, max_blocks_per_seq,
                  n_pages, device="cuda"):
-        import torch
         self.cfg = make_paged_config(max_seqs, n_q_heads, n_kv_heads, head_dim, bits, group, residual,
                                      max_blocks_per_seq, n_pages)
         nbytes = kivi_paged_bytes(self.cfg)
         if nbytes == 0:
             raise KiviError(KIVI_ERR_INVALID_ARG, kivi_last_error_string())
         self.layout = kivi_paged_cache_layout(self.cfg)
-        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        self.workspace = torch.empty(kivi_paged_workspace_bytes(self.cfg, min(max_seqs, KIVI_PAGED_MAX_CALL_SEQS)),
-                                     dtype=torch.uint8, device=device)
+        self.buffer = self._alloc(nbytes, device)
+        self.workspace = self._alloc(kivi_paged_workspace_bytes(self.cfg, min(max_seqs, KIVI_PAGED_MAX_CALL_SEQS)),
+                                     device)
         self.handle = kivi_paged_create(self.cfg, self.buffer.data_ptr(), nbytes)
+
+    def _alloc(self, nbytes, device):
+        """Device bytes for the buffer and the workspace (see KiviCache._alloc)."""
+        import torch
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
     def __del__(self):
         h = getattr(self, "handle", None)

@@ -19,9 +19,12 @@
  *         z        = (fp16) mn
  *         s        = (fp16) ((fp32)(mx - mn) / (2^B - 1))        IEEE fp32, RN
  *         code(x)  = s == 0 ? 0 : clamp(rint(((fp32)x - z) / s), 0, 2^B - 1)
- *         x_hat    = code * s + z
  *     each fp32 operation rounded to nearest-even separately (no FMA); the
- *     rint tie rule is ties-to-even.
+ *     rint tie rule is ties-to-even.  The dequantized value is the exact real
+ *     number x_hat = code * s + z of the stored fp16 s and z: the decode
+ *     kernels never round it to a float of their own (they fold s into the
+ *     query or the attention weights and add z on the side), and their output
+ *     is held to attention over these exact values.
  *   - The newest tokens (at most R) stay in an fp16 residual window; when the
  *     window is full it is quantized as one batch and emptied ([explainer]
  *     3.1, [axis-guide] "the system tax").  A prompt of L tokens keeps
@@ -38,6 +41,10 @@
  *   - Device pointers are CUDA device addresses on the current device.  The
  *     caller allocates and owns ALL device memory: the cache buffer, inputs,
  *     outputs and workspace.  The library owns only the small host handle.
+ *   - A handle's device is the device current at its first call that launches
+ *     work; every later launching call must find that device current
+ *     (KIVI_ERR_INVALID_ARG otherwise).  Handles on different devices may be
+ *     used in one process.
  *   - Calls that take a stream enqueue kernels on it and return without
  *     synchronizing.  Token counts live on the host handle, so no call reads
  *     device memory back.  Buffers passed in must stay valid until the
@@ -288,11 +295,17 @@ kivi_status kivi_cache_set_value_residual(kivi_cache_t cache, int mode);
  * loads the library holds until the process exits.  Shapes whose
  * kivi_decode_workspace_bytes() exceeds 16 MiB (batch * n_q_heads above 488
  * at head_dim 128, above 948 at head_dim 64) get KIVI_ERR_CAPACITY.
+ * The cache's device must be current (KIVI_ERR_INVALID_ARG otherwise).
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  No call
- * allocates memory.  All calls on a device share the one workspace, so two
- * calls whose kernels overlap on the GPU (different streams, no ordering
- * between them) race and may return wrong results; serialize them.
+ * device current).  The library's device code loads lazily, so that first
+ * call is also when the driver loads the array onto the device and reserves
+ * its 16 MiB there; it can fail (KIVI_ERR_CUDA, with a message naming the
+ * workspace) if the device is out of memory, and it may synchronize.  Make
+ * that first call during set-up, before any stream capture and before a
+ * framework takes the device's free memory.  After it no call allocates
+ * memory.  All calls on a device share the one workspace, so two calls whose
+ * kernels overlap on the GPU (different streams, no ordering between them)
+ * race and may return wrong results; serialize them.
  */
 kivi_status kivi_decode_attn_static_ws(kivi_cache_t cache, const void* q, void* out,
                                        float softmax_scale, kivi_stream_t stream);

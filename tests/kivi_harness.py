@@ -5,8 +5,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from bit_kivi_kv_gb300.kivi import KiviCache
 from bit_kivi_kv_gb300.synth import RANGE_2_6_X10_50, SynthKV
+from guards import GuardedCache
 from oracle import layout
 from oracle.attention import decode_attention
 from oracle.cache import OracleCache, OracleCacheFifo
@@ -21,25 +21,32 @@ def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RA
     with fused, those steps append and decode in one kivi_append_decode call;
     with vqueue, the cache keeps its value residual as a queue).
 
+    The cache buffer, the workspace and every output sit between guard bands,
+    checked after every call.
     Returns dict(cache, K, V, steps=[(q,k,v)], outs={step: out fp16 cpu}).
     """
     syn = SynthKV(B, Hq, Hkv, D, seed, outliers=outliers, sink=sink, device="cuda")
     K, V = prompt if prompt is not None else syn.prompt(L)
-    cache = KiviCache(B, Hq, Hkv, D, bits, G, R, max_tokens or max(L + n_app, 1))
+    cache = GuardedCache(B, Hq, Hkv, D, bits, G, R, max_tokens or max(L + n_app, 1))
     cache.set_decode_kernel(decode_kernel)
     if vqueue:
         cache.set_value_residual(1)
     cache.prefill(K, V)
+    cache.bands.check("after the prefill")
     steps, outs = [], {}
     for s in range(n_app):
         q, k, v = syn.step(s)
         steps.append((q, k, v))
         if fused and s in decode_at:
-            outs[s] = cache.append_decode(k, v, q).cpu()
+            out = cache.bands.like(q)
+            outs[s] = cache.append_decode(k, v, q, out=out).cpu()
+            cache.bands.check(f"after the fused call of step {s}")
             continue
         cache.append(k, v)
         if s in decode_at:
-            outs[s] = cache.decode_attn(q).cpu()
+            out = cache.bands.like(q)
+            outs[s] = cache.decode_attn(q, out=out).cpu()
+        cache.bands.check(f"after step {s}")
     torch.cuda.synchronize()
     return dict(cache=cache, K=K, V=V, steps=steps, outs=outs, B=B, Hq=Hq, Hkv=Hkv, D=D,
                 bits=bits, G=G, R=R, L=L, vqueue=vqueue)

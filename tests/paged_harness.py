@@ -7,8 +7,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from bit_kivi_kv_gb300.kivi import KiviPagedCache
 from bit_kivi_kv_gb300.synth import RANGE_2_6_X10_50, SynthKV
+from guards import GuardedPagedCache
 from kivi_harness import assert_close
 from oracle import layout
 from oracle.attention import decode_attention
@@ -21,7 +21,8 @@ class PagedRun:
         self.Hq, self.Hkv, self.D, self.bits, self.G, self.R = Hq, Hkv, D, bits, G, R
         self.max_blocks, self.seed, self.outliers = max_blocks, seed, outliers
         self.check_heads = list(range(Hkv)) if check_heads is None else list(check_heads)
-        self.cache = KiviPagedCache(max_seqs, Hq, Hkv, D, bits, G, R, max_blocks, n_pages)
+        # pool, workspace and outputs between guard bands, checked after every call
+        self.cache = GuardedPagedCache(max_seqs, Hq, Hkv, D, bits, G, R, max_blocks, n_pages)
         self.live = {}       # seq id -> record
         self.n_made = 0
         self.checked = 0     # sequences checked (released or at the end)
@@ -34,6 +35,7 @@ class PagedRun:
         K, V = syn.prompt(L)
         K, V = K[0].contiguous(), V[0].contiguous()
         s = self.cache.add(K, V)
+        self.cache.bands.check(f"after adding a prompt of {L} tokens")
         assert s not in self.live
         self.live[s] = dict(syn=syn, K=K.cpu().numpy(), V=V.cpu().numpy(), events=[], n_steps=0)
         return s
@@ -49,7 +51,8 @@ class PagedRun:
         Q = torch.stack(qs).contiguous()
         Kn = torch.stack(ks).contiguous() if append else None
         Vn = torch.stack(vs).contiguous() if append else None
-        out = self.cache.append_decode(seqs, Kn, Vn, Q)
+        out = self.cache.append_decode(seqs, Kn, Vn, Q, out=self.cache.bands.like(Q))
+        self.cache.bands.check(f"after the call over {list(seqs)}")
         out = out.cpu().numpy()
         for i, s in enumerate(seqs):
             ev = self.live[s]["events"]
