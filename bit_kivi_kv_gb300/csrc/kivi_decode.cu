@@ -348,10 +348,10 @@ namespace {
 
 // Launch the merge kernel as a programmatic dependent of the decode kernel.
 template <typename K, typename A>
-cudaError_t launch_finish(K kernel, const A& f, long long ctas, int D, cudaStream_t st) {
+cudaError_t launch_finish(K kernel, const A& f, long long ctas, cudaStream_t st) {
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3((unsigned)ctas);
-    lc.blockDim = dim3((unsigned)D);
+    lc.blockDim = dim3(mma_detail::kMergeThreads);
     lc.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -415,8 +415,8 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
     f.wm = m.wm;   // with the grid size the launch chose
     f.n_seqs = n;
     for (int i = 0; i < n; ++i) f.seqs[i] = m.seqs[i];
-    e = g.D == 128 ? launch_finish(mma_detail::finish_paged_kernel<128>, f, (long long)n * g.Hq, g.D, st)
-                   : launch_finish(mma_detail::finish_paged_kernel<64>, f, (long long)n * g.Hq, g.D, st);
+    e = g.D == 128 ? launch_finish(mma_detail::finish_paged_kernel<128>, f, (long long)n * g.Hq, st)
+                   : launch_finish(mma_detail::finish_paged_kernel<64>, f, (long long)n * g.Hq, st);
     if (e != cudaSuccess) return e;
     *launches = 2;
     return cudaSuccess;
@@ -456,20 +456,11 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         if (e != cudaSuccess) return e;
         mma_detail::FinishArgs f{workspace, out, g.Hq, g.Hkv, nq, m.wm};
         // the merge may start while the main kernel drains; it waits for it on the GPU
-        cudaLaunchConfig_t lc{};
-        lc.gridDim = dim3((unsigned)((long long)g.B * g.Hq));
-        lc.blockDim = dim3((unsigned)g.D);
-        lc.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
-        e = g.D == 128 ? cudaLaunchKernelEx(&lc, mma_detail::finish_kernel<128>, f)
-                       : cudaLaunchKernelEx(&lc, mma_detail::finish_kernel<64>, f);
+        const long long heads = (long long)g.B * g.Hq;
+        e = g.D == 128 ? launch_finish(mma_detail::finish_kernel<128>, f, heads, st)
+                       : launch_finish(mma_detail::finish_kernel<64>, f, heads, st);
         *launches = 2;
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
+        return e;
     }
     DecodeArgs a{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                  g.k_resid_off, g.v_resid_off, g.R, g.G, g.Hq, g.Hkv,

@@ -153,6 +153,32 @@ __device__ __forceinline__ uint2 ldg_stream2(const void* p) {
     return v;
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held as one fragment (lane l:
+// row l/4, columns 2(l%4), 2(l%4)+1) into the same fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+    return d;
+}
+
+// A fragment (m16n8k16) of V^T for m-tile mt from 16 fp16 rows (tokens) of D
+// channels: vg / vg8 are rows g and g+8 of the tile (ok: the row exists, else
+// zeros).  Each lane loads the row-major 8x8 fragments of rows x channels
+// like a key tile, and movmatrix transposes them to channels x rows.
+template <int D>
+__device__ __forceinline__ void vt_frag_rows(const __half* vg, const __half* vg8, bool okg, bool okg8, int mt, int i,
+                                             uint32_t (&af)[4]) {
+    const int ch = 16 * mt + 2 * i;
+    const uint32_t x0 = okg ? *reinterpret_cast<const uint32_t*>(vg + ch) : 0u;        // tokens 0-7, channels 0-7
+    const uint32_t x1 = okg8 ? *reinterpret_cast<const uint32_t*>(vg8 + ch) : 0u;      // tokens 8-15, channels 0-7
+    const uint32_t x2 = okg ? *reinterpret_cast<const uint32_t*>(vg + ch + 8) : 0u;    // tokens 0-7, channels 8-15
+    const uint32_t x3 = okg8 ? *reinterpret_cast<const uint32_t*>(vg8 + ch + 8) : 0u;  // tokens 8-15, channels 8-15
+    af[0] = movmatrix_trans(x0);   // channels 0-7, tokens 0-7
+    af[1] = movmatrix_trans(x2);   // channels 8-15, tokens 0-7
+    af[2] = movmatrix_trans(x1);   // channels 0-7, tokens 8-15
+    af[3] = movmatrix_trans(x3);   // channels 8-15, tokens 8-15
+}
+
 // ---- shared-memory loads through 32-bit shared addresses ----
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
@@ -299,18 +325,22 @@ struct Cfg {
     static constexpr int ENT = 16 * NGRP * 4;         // value (step, zero) entries of one tile
     static constexpr int KSZ = 4 * D;                 // key (step, zero) entries of one block
     static constexpr int STAGES = 2;                  // ring depth per warp (stages of 2 tiles)
-    // a stage: key words of 2 tiles, value words of 2 tiles, their value
-    // entries, and the block's key entries
+    // a stage: key words of 2 tiles, the block's key entries, value words of
+    // 2 tiles, their value entries.  With G = 32 a tile pair is a whole block,
+    // and the key part and the value part of a block are each one contiguous
+    // run in this order, so a stage takes two bulk copies.
+    static constexpr int KT = 0, KE = 2 * TILE, VT = 2 * TILE + KSZ, VE = 4 * TILE + KSZ;
     static constexpr int STAGE_BYTES = 4 * TILE + 2 * ENT + KSZ;
     static constexpr int DYN_SMEM = kWarps * STAGES * STAGE_BYTES;
+    static constexpr bool WHOLE = TPB == 2;
 };
 
 // Build this warp's Qt B fragments (fp16 hi + lo parts of q_h * step) and
 // its beta = sum_c q_h[c] * zero_c, from the block's key steps and zeros
 // (D fp16 steps, then D fp16 zeros); entries == nullptr means step 1, zero 0
-// (the fp16 residual).  qh/ql hold the fp16 hi/lo parts of the scaled query
-// per channel pair (for the quantized tiles already multiplied by the
-// channel's code scale 2^-(BITS*pos)); with s exact in fp16, hi = rn(qh*s)
+// (the fp16 residual: the parts are split from the fp32 query qf).  qh/ql hold
+// the fp16 hi/lo parts of the scaled query per channel pair, already
+// multiplied by the channel's code scale 2^-(BITS*pos); with s exact in fp16, hi = rn(qh*s)
 // and lo = rn(ql*s + (qh*s - hi)), the inner residual exact, so hi + lo =
 // q*s to about 22 bits.  Lane l handles channel pairs CPL*l + j; off[j] is
 // the table offset of pair CPL*l + j (head 0, hi column).  With entries,
@@ -352,13 +382,17 @@ __device__ __forceinline__ void build_q_frags(const uint8_t* entries, const floa
             }
         }
     } else {
+        // the fp16 residual: hi / lo parts of the scaled query itself
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             const int cp = CPL * lane + j;
 #pragma unroll
             for (int h = 0; h < NQ; ++h) {
-                qfrag[off[j] + h * HEAD] = qh[h][cp];
-                qfrag[off[j] + h * HEAD + LOC] = ql[h][cp];
+                const float2 x = *reinterpret_cast<const float2*>(&qf[h][2 * cp]);
+                const uint32_t hi = pack_f16x2(x.x, x.y);
+                const float2 hf = unpack_f16x2(hi);
+                qfrag[off[j] + h * HEAD] = hi;
+                qfrag[off[j] + h * HEAD + LOC] = pack_f16x2(x.x - hf.x, x.y - hf.y);
             }
         }
     }
@@ -399,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     using C = Cfg<D, BITS, NQ, G>;
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
     __shared__ __align__(16) float qf[NQ][D];
-    __shared__ uint32_t qh_s[NQ][D / 2], ql_s[NQ][D / 2];   // fp16 hi / lo of the scaled query
-    __shared__ uint32_t qhc_s[NQ][D / 2], qlc_s[NQ][D / 2]; // the same times the code scale 2^-(BITS*pos)
+    // fp16 hi / lo parts of the scaled query times the code scale 2^-(BITS*pos)
+    __shared__ uint32_t qhc_s[NQ][D / 2], qlc_s[NQ][D / 2];
     __shared__ __align__(16) uint32_t qfrag_all[kWarps][32 * C::QSTRIDE];
     __shared__ float red_m[kWarps][NQ], red_l[kWarps][NQ];
     __shared__ float red_o[kWarps][NQ][D];
@@ -448,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     const long long tiles_bytes = (long long)C::TPB * a.tile_bytes;
 
     float m = -INFINITY, l = 0.f;
+    bool fresh = true;    // no tile of the current segment has been counted yet
     float o[KS][4];
     float zeta[NBF];
     uint32_t qb[2 * KS];
@@ -463,7 +498,10 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
         const float mn = fmaxf(m, mt * unit);
-        if (__any_sync(kFull, mn > m)) {
+        if (fresh) {
+            m = mn;          // the segment's first tiles: o, zeta and l are still zero
+            fresh = false;
+        } else if (__any_sync(kFull, mn > m)) {
             const float alpha = fast_exp2(m - mn);
             l *= alpha;
             const float ao = __shfl_sync(kFull, alpha, (lane & ~3) | (hO < NQ ? hO : 0));
@@ -616,11 +654,18 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 kp = kcur;
             }
             const uint8_t* vcur = kp + vdelta;
-            mbar_expect_tx_u32(bar, 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
-            tma_1d_u32(dst, kp + tcur * C::TILE, 2 * C::TILE, bar);
-            tma_1d_u32(dst + 2 * C::TILE, vcur + tcur * C::TILE, 2 * C::TILE, bar);
-            tma_1d_u32(dst + 4 * C::TILE, vcur + tiles_bytes + tcur * C::ENT, 2 * C::ENT, bar);
-            if (kz) tma_1d_u32(dst + 4 * C::TILE + 2 * C::ENT, kp + tiles_bytes, C::KSZ, bar);
+            if constexpr (C::WHOLE) {
+                // the block's key part and value part, each one contiguous copy
+                mbar_expect_tx_u32(bar, C::STAGE_BYTES);
+                tma_1d_u32(dst + C::KT, kp, 2 * C::TILE + C::KSZ, bar);
+                tma_1d_u32(dst + C::VT, vcur, 2 * C::TILE + 2 * C::ENT, bar);
+            } else {
+                mbar_expect_tx_u32(bar, 4 * C::TILE + 2 * C::ENT + (kz ? C::KSZ : 0));
+                tma_1d_u32(dst + C::KT, kp + tcur * C::TILE, 2 * C::TILE, bar);
+                if (kz) tma_1d_u32(dst + C::KE, kp + tiles_bytes, C::KSZ, bar);
+                tma_1d_u32(dst + C::VT, vcur + tcur * C::TILE, 2 * C::TILE, bar);
+                tma_1d_u32(dst + C::VE, vcur + tiles_bytes + tcur * C::ENT, 2 * C::ENT, bar);
+            }
             first = false;
             tcur += 2;
             if (tcur == C::TPB) {
@@ -689,10 +734,6 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             const float x0 = qv.x * a.scale_log2, x1 = qv.y * a.scale_log2;
             qf[j][2 * cp] = x0;
             qf[j][2 * cp + 1] = x1;
-            const uint32_t hi = pack_f16x2(x0, x1);
-            const float2 hf = unpack_f16x2(hi);
-            qh_s[j][cp] = hi;
-            ql_s[j][cp] = pack_f16x2(x0 - hf.x, x1 - hf.y);
             // channels 2cp, 2cp+1 have class cp / 4: their codes read as code * 2^(BITS*pos - 24)
             const float cs = pow2i(-BITS * ((cp >> 2) % (8 / BITS)));
             const float y0 = x0 * cs, y1 = x1 * cs;
@@ -704,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         __syncthreads();
 
         m = -INFINITY; l = 0.f;
+        fresh = true;
 #pragma unroll
         for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
 #pragma unroll
@@ -718,8 +760,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             const uint32_t stage_u32 = ring_u32 + st * C::STAGE_BYTES;
             const int pr = wb + k;
             if (need_ksz(pr))
-                build_q_frags<C, D, NQ>(stage + 4 * C::TILE + 2 * C::ENT, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb,
-                                        beta);
+                build_q_frags<C, D, NQ>(stage + C::KE, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);
             // keys: logits of tokens g, g+8 of both tiles for head i
             float sc[4];
             if constexpr (BITS == 8) {
@@ -728,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 float cb[4] = {beta, 0.f, beta, 0.f};
                 {
                     uint32_t w[W];
-                    lds_words(stage_u32, w);
+                    lds_words(stage_u32 + C::KT, w);
 #pragma unroll
                     for (int kk = 0; kk < KS; ++kk) {
                         uint32_t fa[4];
@@ -738,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 }
                 {
                     uint32_t w[W];
-                    lds_words(stage_u32 + C::TILE, w);
+                    lds_words(stage_u32 + C::KT + C::TILE, w);
 #pragma unroll
                     for (int kk = 0; kk < KS; ++kk) {
                         uint32_t fb[4];
@@ -752,8 +793,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 sc[3] = cb[2] + cb[3];
             } else {
                 uint32_t wa[W], wbw[W], wa8[W], wb8[W];
-                lds_words(stage_u32, wa);
-                lds_words(stage_u32 + C::TILE, wbw);
+                lds_words(stage_u32 + C::KT, wa);
+                lds_words(stage_u32 + C::KT + C::TILE, wbw);
 #pragma unroll
                 for (int x = 0; x < W; ++x) { wa8[x] = wa[x] >> 8; wb8[x] = wbw[x] >> 8; }
                 float ca[4] = {beta, 0.f, beta, 0.f};
@@ -795,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     gather(p[2 * t], p[2 * t + 1], prb);
                     uint32_t ph01, ph89, pl01, pl89;
                     split_p(prb, ph01, ph89, pl01, pl89);
-                    const uint32_t ve = stage_u32 + 4 * C::TILE + t * C::ENT + eoff;
+                    const uint32_t ve = stage_u32 + C::VE + t * C::ENT + eoff;
                     uint32_t pb[NBF][2];
 #pragma unroll
                     for (int f = 0; f < NBF; ++f) {
@@ -803,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                         p_frag(prb, ph01, ph89, pl01, pl89, sv, zv, pb[f][0], pb[f][1], zeta[f]);
                     }
                     uint32_t wv[W];
-                    lds_words(stage_u32 + (2 + t) * C::TILE, wv);
+                    lds_words(stage_u32 + C::VT + t * C::TILE, wv);
                     if constexpr (BITS == 8) {
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
@@ -871,24 +912,14 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     uint32_t ph01, ph89, pl01, pl89;
                     split_p(prb, ph01, ph89, pl01, pl89);
                     const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
-                    const long long tA = t0 + 16 * t + 2 * i, tB = tA + 8;
-                    auto row = [&](long long tok) { return ring_v + (tok % a.R) * D; };
-                    const __half* vA0 = row(tA);
-                    const __half* vA1 = row(tA + 1);
-                    const __half* vB0 = row(tB);
-                    const __half* vB1 = row(tB + 1);
-                    const bool okA0 = tA >= a.lqv, okA1 = tA + 1 >= a.lqv, okB0 = tB >= a.lqv, okB1 = tB + 1 >= a.lqv;
-                    auto ld = [&](bool ok, const __half* r, int ch) -> uint32_t {
-                        return ok ? (uint32_t)__half_as_ushort(r[ch]) : 0u;
-                    };
+                    // rows g, g+8 of the 16 tokens: queued values sit at ring row token % R
+                    const long long tg = t0 + 16 * t + g, tg8 = tg + 8;
+                    const __half* vg = ring_v + (tg % a.R) * D;
+                    const __half* vg8 = ring_v + (tg8 % a.R) * D;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
-                        const int c0 = 16 * mt + g;
                         uint32_t af[4];
-                        af[0] = ld(okA0, vA0, c0) | (ld(okA1, vA1, c0) << 16);
-                        af[1] = ld(okA0, vA0, c0 + 8) | (ld(okA1, vA1, c0 + 8) << 16);
-                        af[2] = ld(okB0, vB0, c0) | (ld(okB1, vB1, c0) << 16);
-                        af[3] = ld(okB0, vB0, c0 + 8) | (ld(okB1, vB1, c0 + 8) << 16);
+                        vt_frag_rows<D>(vg, vg8, tg >= a.lqv, tg8 >= a.lqv, mt, i, af);
                         mma16816(o[mt], af, pb0, pb1);
                     }
                 }
@@ -910,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     return rr == nrow ? a.new_v + islot * D : vr + ((32 * P + rr) % a.R) * D;
                 return FUSED && rr == nrow ? a.new_v + islot * D : vr + (long long)rr * D;
             };
-            build_q_frags<C, D, NQ>(nullptr, qf, qh_s, ql_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
+            build_q_frags<C, D, NQ>(nullptr, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
             for (int rp = rb; rp < re; ++rp) {
                 float sc[4];
 #pragma unroll
@@ -942,40 +973,15 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     uint32_t ph01, ph89, pl01, pl89;
                     split_p(prb, ph01, ph89, pl01, pl89);
                     const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
-                    const int tA = 32 * rp + 16 * t + 2 * i, tB = tA + 8;
-                    if constexpr (FUSED) {
-                        const __half* vA0 = vrow(tA);
-                        const __half* vA1 = vrow(tA + 1);
-                        const __half* vB0 = vrow(tB);
-                        const __half* vB1 = vrow(tB + 1);
-                        const bool okA0 = tA < n, okA1 = tA + 1 < n, okB0 = tB < n, okB1 = tB + 1 < n;
-                        auto ld = [&](bool ok, const __half* row, int ch) -> uint32_t {
-                            return ok ? (uint32_t)__half_as_ushort(row[ch]) : 0u;
-                        };
+                    const int r0w = 32 * rp + 16 * t;
+                    const bool okg = r0w + g < n, okg8 = r0w + g + 8 < n;
+                    const __half* vg = FUSED ? vrow(r0w + g) : vr + (long long)(r0w + g) * D;
+                    const __half* vg8 = FUSED ? vrow(r0w + g + 8) : vr + (long long)(r0w + g + 8) * D;
 #pragma unroll
-                        for (int mt = 0; mt < KS; ++mt) {
-                            const int c0 = 16 * mt + g;
-                            uint32_t af[4];
-                            af[0] = ld(okA0, vA0, c0) | (ld(okA1, vA1, c0) << 16);
-                            af[1] = ld(okA0, vA0, c0 + 8) | (ld(okA1, vA1, c0 + 8) << 16);
-                            af[2] = ld(okB0, vB0, c0) | (ld(okB1, vB1, c0) << 16);
-                            af[3] = ld(okB0, vB0, c0 + 8) | (ld(okB1, vB1, c0 + 8) << 16);
-                            mma16816(o[mt], af, pb0, pb1);
-                        }
-                    } else {
-                        auto ld = [&](int tt, int ch) -> uint32_t {
-                            return tt < n ? (uint32_t)__half_as_ushort(vr[(long long)tt * D + ch]) : 0u;
-                        };
-#pragma unroll
-                        for (int mt = 0; mt < KS; ++mt) {
-                            const int c0 = 16 * mt + g;
-                            uint32_t af[4];
-                            af[0] = ld(tA, c0) | (ld(tA + 1, c0) << 16);
-                            af[1] = ld(tA, c0 + 8) | (ld(tA + 1, c0 + 8) << 16);
-                            af[2] = ld(tB, c0) | (ld(tB + 1, c0) << 16);
-                            af[3] = ld(tB, c0 + 8) | (ld(tB + 1, c0 + 8) << 16);
-                            mma16816(o[mt], af, pb0, pb1);
-                        }
+                    for (int mt = 0; mt < KS; ++mt) {
+                        uint32_t af[4];
+                        vt_frag_rows<D>(vg, vg8, okg, okg8, mt, i, af);
+                        mma16816(o[mt], af, pb0, pb1);
                     }
                 }
             }
@@ -1032,45 +1038,106 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     }
 }
 
-// Log-sum-exp merge of nparts partials at base into out[c] (thread c).  A
-// partial whose status is set (a cache copy timed out, a bad table entry)
-// makes the output NaN.
+// One CTA (kMergeThreads threads) per (query row, query head): the
+// log-sum-exp merge of the head's nparts partial results -> fp16 output.  The
+// values of the partials a warp sums go out first, together with the (m, l)
+// loads; one warp turns the m's into weights 2^(m_j - M) and the sum L; warp
+// w sums partials w, w + 4, ... and the four warps' sums are added in warp
+// order (a fixed order for a given partition).  A partial whose status is set
+// (a cache copy timed out, a bad table entry) makes the head's output NaN.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeWarps = kMergeThreads / 32;
 template <int D>
-__device__ __forceinline__ void merge_partials(const float* base, int nparts, __half* out, int c) {
-    float M = -INFINITY;
-    bool failed = false;
-    for (int j = 0; j < nparts; ++j) {
-        M = fmaxf(M, base[j * partial_stride(D)]);
-        failed |= base[j * partial_stride(D) + 2] != 0.f;
+__device__ __forceinline__ void merge_head(const float* base, int nparts, __half* out) {
+    constexpr int S = partial_stride(D);
+    constexpr int CPL = D / 32;                                 // channels per lane
+    constexpr int NR = (kPartialSlots + kMergeWarps - 1) / kMergeWarps;   // partials per warp, at most
+    __shared__ float e_s[kPartialSlots], l_s[kPartialSlots];
+    __shared__ __align__(16) float red[kMergeWarps][D];
+    __shared__ float lsum_s;
+    __shared__ int bad_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float v[NR][CPL];
+#pragma unroll
+    for (int u = 0; u < NR; ++u) {
+        const int j = warp + u * kMergeWarps;
+        if (j < nparts) {
+            const float* ps = base + j * S + 4 + CPL * lane;
+            if constexpr (CPL == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(ps);
+                v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(ps);
+                v[u][0] = x.x; v[u][1] = x.y;
+            }
+        }
     }
-    float acc = 0.f, lsum = 0.f;
-    for (int j = 0; j < nparts; ++j) {
-        const float* ps = base + j * partial_stride(D);
-        if (ps[0] == -INFINITY) continue;
-        const float e = fast_exp2(ps[0] - M);
-        lsum = fmaf(ps[1], e, lsum);
-        acc = fmaf(ps[4 + c], e, acc);
+    if (tid == 0) bad_s = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int j = tid; j < nparts; j += kMergeThreads) {
+        const float* ps = base + j * S;
+        e_s[j] = ps[0];
+        l_s[j] = ps[1];
+        bad |= ps[2] != 0.f;
     }
-    out[c] = failed ? __float2half_rn(NAN) : __float2half_rn(acc / lsum);
+    if (bad) bad_s = 1;
+    __syncthreads();
+    if (warp == 0) {
+        float M = -INFINITY;
+        for (int j = lane; j < nparts; j += 32) M = fmaxf(M, e_s[j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        float ls = 0.f;
+        for (int j = lane; j < nparts; j += 32) {
+            const float m = e_s[j];
+            const float e = m == -INFINITY ? 0.f : fast_exp2(m - M);
+            e_s[j] = e;
+            ls = fmaf(l_s[j], e, ls);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
+        if (lane == 0) lsum_s = ls;
+    }
+    __syncthreads();
+    float acc[CPL];
+#pragma unroll
+    for (int r = 0; r < CPL; ++r) acc[r] = 0.f;
+#pragma unroll
+    for (int u = 0; u < NR; ++u) {
+        const int j = warp + u * kMergeWarps;
+        if (j < nparts) {
+            const float e = e_s[j];
+#pragma unroll
+            for (int r = 0; r < CPL; ++r) acc[r] = fmaf(v[u][r], e, acc[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < CPL; ++r) red[warp][CPL * lane + r] = acc[r];
+    __syncthreads();
+    for (int c = tid; c < D; c += kMergeThreads) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) sum += red[w][c];
+        out[c] = bad_s ? __float2half_rn(NAN) : __float2half_rn(sum / lsum_s);
+    }
 }
 
-// One CTA (D threads) per (batch, query head): merge of the partials of the
-// head's kv slot -> fp16 output.
+// One CTA per (batch, query head): merge of the partials of the head's kv slot.
 template <int D>
-__global__ void __launch_bounds__(D) finish_kernel(FinishArgs a) {
+__global__ void __launch_bounds__(kMergeThreads) finish_kernel(FinishArgs a) {
     // launched as a programmatic dependent of the main kernel: wait until its
     // partial results are complete and visible
     griddepcontrol_wait();
     griddepcontrol_launch_dependents();   // the next decode call may start its prologue
     const long long bh = blockIdx.x;
     const long long slot = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.nq;
-    merge_partials<D>(a.ws + bh * kPartialSlots * partial_stride(D), slot_parts(a.wm, slot), a.out + bh * D,
-                      threadIdx.x);
+    merge_head<D>(a.ws + bh * kPartialSlots * partial_stride(D), slot_parts(a.wm, slot), a.out + bh * D);
 }
 
 // The same for a paged call: one CTA per (call sequence, query head).
 template <int D>
-__global__ void __launch_bounds__(D) finish_paged_kernel(const __grid_constant__ PagedFinishArgs a) {
+__global__ void __launch_bounds__(kMergeThreads) finish_paged_kernel(const __grid_constant__ PagedFinishArgs a) {
     griddepcontrol_wait();
     griddepcontrol_launch_dependents();
     const long long bh = blockIdx.x;
@@ -1080,7 +1147,7 @@ __global__ void __launch_bounds__(D) finish_paged_kernel(const __grid_constant__
     const long long w0 = sq.start + hk * (a.wm.S0 + P * a.wm.wq + PR * a.wm.wr);
     const long long last = w0 + unit_start_p(P, a.wm.wq, a.wm.wr, a.wm.S0, P + PR - 1);
     const int nparts = (int)(map_owner(a.wm, last) - map_owner(a.wm, w0 + a.wm.S0) + 1);
-    merge_partials<D>(a.ws + bh * kPartialSlots * partial_stride(D), nparts, a.out + bh * D, threadIdx.x);
+    merge_head<D>(a.ws + bh * kPartialSlots * partial_stride(D), nparts, a.out + bh * D);
 }
 
 }  // namespace mma_detail
