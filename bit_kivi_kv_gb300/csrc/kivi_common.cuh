@@ -59,28 +59,26 @@ struct PairPlace {
 // Position of token t (0..15) of a tile inside a row of its value entry tile.
 __host__ __device__ constexpr int entry_pos(int t) { return 4 * ((t & 7) >> 1) + 2 * (t >> 3) + (t & 1); }
 
-// Balanced partition of a decode call's work over the CTAs of the tensor-core
-// kernel.  Per (batch, kv-head) slot the work is a row of units: P quantized
-// tile pairs (32 tokens) of weight wq, then PR fp16 residual pairs (32 rows) of
-// weight wr (weights proportional to the bytes each reads), after a lead-in of
-// weight S0 that stands for the fixed cost a CTA pays per slot it works on
-// (query setup, ring fill, warp merge): the CTA whose range takes in a slot's
-// start is given that much less of the units.  Slots follow each other; CTA c
-// covers weight positions [c*Wt/n, (c+1)*Wt/n) and owns the units that start
-// there.  n <= Wt / max(wq, wr) guarantees that every CTA between the first and
-// the last unit of a slot owns one of them.
+// Balanced partition of a decode call's work over the warps of the
+// tensor-core kernel (the map's workers; a CTA's warps work independently).
+// Per (batch, kv-head) slot the work is a row of units: P quantized tile pairs
+// (32 tokens) of weight wq, then PR fp16 residual pairs (32 rows) of weight wr
+// (weights proportional to the bytes each reads), after a lead-in of weight S0
+// that stands for the fixed cost a worker pays per slot it works on (query
+// setup, ring fill, partial write): the worker whose range takes in a slot's
+// start is given that much less of the units.  Slots follow each other; worker
+// c covers weight positions [c*Wt/n, (c+1)*Wt/n) and owns the units that start
+// there.  n <= Wt / max(wq, wr) guarantees that every worker between the first
+// and the last unit of a slot owns one of them.
 struct WorkMap {
     long long P, PR, wq, wr, Ws, Wt, n, S0;
 };
 // The lead-in in quantized pairs, used when the call's shortest slot is shorter
-// than a CTA's share (with ~4 CTAs per SM), so that CTAs cover several slot
-// starts: measured on GB300, 10 pairs take ragged prompts of 512..7680 tokens
-// from 41.5 to 36.9 us per call and grouped-query slots of ~0.9 shares from
-// 119.9 to 117.6 us, while for slots of 2.4 shares (Llama-2-7B layer) any
-// lead-in is slower (33.9 -> 34.4 us at 5 pairs).
-constexpr long long kSegmentLeadPairs = 10;
+// than a worker's share (with ~16 warps per SM), so that workers cover several
+// slot starts.
+constexpr long long kSegmentLeadPairs = 4;
 __host__ inline long long segment_lead(long long wq, long long ws_min, long long wt, int num_sms) {
-    const long long n_est = 4LL * (num_sms > 0 ? num_sms : 1);
+    const long long n_est = 16LL * (num_sms > 0 ? num_sms : 1);
     return ws_min * n_est < wt ? kSegmentLeadPairs * wq : 0;
 }
 // unit u of a slot of P quantized pairs (slots of ragged sequences differ)
@@ -103,11 +101,11 @@ __host__ __device__ inline long long first_unit_at(const WorkMap& m, long long y
     return first_unit_at_p(m.P, m.wq, m.wr, m.S0, y);
 }
 __host__ __device__ inline long long map_begin(const WorkMap& m, long long c) { return c * m.Wt / m.n; }
-// the CTA whose range holds weight position x
+// the worker whose range holds weight position x
 __host__ __device__ inline long long map_owner(const WorkMap& m, long long x) {
     return ((x + 1) * m.n + m.Wt - 1) / m.Wt - 1;
 }
-// partials of slot s: CTAs [owner of its first unit's start, owner of its last unit's start]
+// partials of slot s: workers [owner of its first unit's start, owner of its last unit's start]
 __host__ __device__ inline long long slot_first_cta(const WorkMap& m, long long s) {
     return map_owner(m, s * m.Ws + m.S0);
 }

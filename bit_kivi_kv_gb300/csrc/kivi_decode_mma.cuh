@@ -432,19 +432,19 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     constexpr bool FUSED = MODE != kModePlain, PAGED = MODE == kModePaged, FIFO = MODE == kModeFifo;
     using C = Cfg<D, BITS, NQ, G>;
     constexpr int KS = C::KSTEPS, W = C::W, NGRP = C::NGRP, GB = C::GB, NBF = C::NBF;
-    __shared__ __align__(16) float qf[NQ][D];
-    // fp16 hi / lo parts of the scaled query times the code scale 2^-(BITS*pos)
-    __shared__ uint32_t qhc_s[NQ][D / 2], qlc_s[NQ][D / 2];
+    // per warp: the scaled query (fp32) and the fp16 hi / lo parts of it times
+    // the code scale 2^-(BITS*pos), for the slot the warp works on
+    __shared__ __align__(16) float qf_all[kWarps][NQ][D];
+    __shared__ uint32_t qhc_all[kWarps][NQ][D / 2], qlc_all[kWarps][NQ][D / 2];
     __shared__ __align__(16) uint32_t qfrag_all[kWarps][32 * C::QSTRIDE];
-    __shared__ float red_m[kWarps][NQ], red_l[kWarps][NQ];
-    __shared__ float red_o[kWarps][NQ][D];
-    __shared__ float red_z[kWarps][NQ][NGRP];
     __shared__ __align__(8) uint64_t full_bar[kWarps][C::STAGES];
-    __shared__ uint32_t red_status;
     extern __shared__ __align__(128) uint8_t dyn_smem[];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, i = lane & 3;
+#define qf (qf_all[warp])
+#define qhc_s (qhc_all[warp])
+#define qlc_s (qlc_all[warp])
     uint32_t* qfrag = qfrag_all[warp];
     uint8_t* ring = dyn_smem + warp * C::STAGES * C::STAGE_BYTES;
     float4* mixbuf = reinterpret_cast<float4*>(dyn_smem + C::DYN_SMEM) + warp * kMaxMixPairs * 32;   // FIFO only
@@ -458,8 +458,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         if (a.stall_bytes && blockIdx.x == 0 && warp == 0) mbar_expect_tx_only(smem_u32(&bars[0]), (uint32_t)a.stall_bytes);
         fence_mbar_init();
     }
-    if (tid == 0) red_status = 0u;
-    __syncthreads();
+    __syncwarp();
 
     int qoff[D / 64];     // this lane's Qt table offsets (channel pairs (D/64)*lane + j)
 #pragma unroll
@@ -560,13 +559,62 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         }
     };
 
-    // This CTA's share of the call's work: the units starting in its weight range
-    // [pos, pe); one partial result per slot it touches.
+    // This warp's share of the call's work: the units starting in its weight
+    // range [pos, pe); one partial result per slot it touches.  Warps are the
+    // workers of the map (wm.n of them); the warps of a CTA share nothing but
+    // the SM.
     const WorkMap& wm = a.wm;
     const long long cta = blockIdx.x;
-    long long pos = map_begin(wm, cta);
-    const long long pe = map_begin(wm, cta + 1);
+    const long long gw = cta * kWarps + warp;
+    long long pos = gw < wm.n ? map_begin(wm, gw) : wm.Wt;
+    const long long pe = gw < wm.n ? map_begin(wm, gw + 1) : wm.Wt;
     bool first_seg = true;
+    // The programmatic-dependent launch point: wait for the preceding kernel,
+    // let the merge kernel start launching, store the fused append's rows.
+    // Every warp passes it once (its first segment, or after its loop if it
+    // has none), after issuing its first copies: with early_ok those read only
+    // quantized blocks, which the preceding kernel never writes (the library's
+    // last kernel on a cache copies residual rows, or is a decode); the query,
+    // the residual rows and the workspace are touched only after it.
+    auto dependency_point = [&]() {
+        griddepcontrol_wait();
+        griddepcontrol_launch_dependents();       // the merge kernel may start launching
+        if constexpr (PAGED) {
+            // the fused append of a paged call: each sequence's own new row
+            constexpr int CPR = D * 2 / 16;
+            if (a.new_k != nullptr) {
+                const long long nsl = (long long)a.n_seqs * a.Hkv;
+                for (long long idx = cta * kThreads + tid; idx < nsl * 2 * CPR;
+                     idx += (long long)gridDim.x * kThreads) {
+                    const long long sl = idx / (2 * CPR);
+                    const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
+                    const int si = (int)(sl / a.Hkv), h2 = (int)(sl % a.Hkv);
+                    const int nr = a.seqs[si].new_row;
+                    if (nr < 0) continue;
+                    const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
+                    uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
+                    const long long drow = ((long long)a.seqs[si].seq * a.Hkv + h2) * a.R + nr;
+                    reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + drow * D)[c16] = *src;
+                }
+            }
+        } else if (FUSED && a.new_row >= 0) {
+            // the fused append: store every slot's new row in the cache, 16
+            // bytes a thread over the grid (this call reads that row from the
+            // inputs, never from the cache)
+            constexpr int CPR = D * 2 / 16;       // 16-byte chunks per row
+            const long long nslots = (long long)(wm.Wt / wm.Ws);
+            for (long long idx = cta * kThreads + tid; idx < nslots * 2 * CPR;
+                 idx += (long long)gridDim.x * kThreads) {
+                const long long sl = idx / (2 * CPR);
+                const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
+                const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
+                uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
+                // value queue: the new value goes to ring row (its slot position) % R
+                const long long vr_row = FIFO && is_v ? (32 * wm.P + a.new_row) % a.R : a.new_row;
+                reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + (sl * a.R + vr_row) * D)[c16] = *src;
+            }
+        }
+    };
     bool bad_page = false;   // lane 0: a block-table entry was out of range (sticky)
     while (pos < pe) {
         // the slot holding weight position pos: weights [w0, w0 + Ws), P quantized
@@ -613,10 +661,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         const long long u1 = first_unit_at_p(P, wm.wq, wm.wr, wm.S0, min(pe - w0, Ws));
         const int p0 = (int)min(u0, P), p1 = (int)min(u1, P);                  // quantized pairs
         const int r0 = (int)(max(u0, P) - P), r1 = (int)(max(u1, P) - P);      // residual pairs
-        const int part = (int)(cta - map_owner(wm, w0 + wm.S0));
-        // ---- this warp's contiguous run of pairs, two tiles per ring stage ----
-        const int pw = (p1 - p0 + kWarps - 1) / kWarps;
-        const int wb = min(p0 + warp * pw, p1), we = min(wb + pw, p1);
+        const int part = (int)(gw - map_owner(wm, w0 + wm.S0));
+        // ---- this warp's run of pairs, two tiles per ring stage ----
+        const int wb = p0, we = p1;
         const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
         // value queue: this warp's pairs from mix0 on have quantized keys and queued values
         const int mix0 = FIFO ? max(wb, (int)(a.lqv / 32)) : 0;
@@ -683,51 +730,11 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
         }
         if (first_seg) {
-            // launched as a programmatic dependent: with early_ok the copies above
-            // read only quantized blocks, which the preceding kernel never writes
-            // (the library's last kernel on a cache copies residual rows, or is
-            // a decode); the query, the residual rows and the workspace are
-            // touched only after this
-            griddepcontrol_wait();
-            griddepcontrol_launch_dependents();       // the merge kernel may start launching
             first_seg = false;
-            if constexpr (PAGED) {
-                // the fused append of a paged call: each sequence's own new row
-                constexpr int CPR = D * 2 / 16;
-                if (a.new_k != nullptr) {
-                    const long long nsl = (long long)a.n_seqs * a.Hkv;
-                    for (long long idx = cta * kThreads + tid; idx < nsl * 2 * CPR;
-                         idx += (long long)gridDim.x * kThreads) {
-                        const long long sl = idx / (2 * CPR);
-                        const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
-                        const int si = (int)(sl / a.Hkv), h2 = (int)(sl % a.Hkv);
-                        const int nr = a.seqs[si].new_row;
-                        if (nr < 0) continue;
-                        const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
-                        uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
-                        const long long drow = ((long long)a.seqs[si].seq * a.Hkv + h2) * a.R + nr;
-                        reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + drow * D)[c16] = *src;
-                    }
-                }
-            } else if (FUSED && a.new_row >= 0) {
-                // the fused append: store every slot's new row in the cache, 16
-                // bytes a thread over the grid (this call reads that row from the
-                // inputs, never from the cache)
-                constexpr int CPR = D * 2 / 16;       // 16-byte chunks per row
-                const long long nslots = (long long)(wm.Wt / wm.Ws);
-                for (long long idx = cta * kThreads + tid; idx < nslots * 2 * CPR;
-                     idx += (long long)gridDim.x * kThreads) {
-                    const long long sl = idx / (2 * CPR);
-                    const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
-                    const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
-                    uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
-                    // value queue: the new value goes to ring row (its slot position) % R
-                    const long long vr_row = FIFO && is_v ? (32 * wm.P + a.new_row) % a.R : a.new_row;
-                    reinterpret_cast<uint4*>(reinterpret_cast<__half*>(rows) + (sl * a.R + vr_row) * D)[c16] = *src;
-                }
-            }
+            dependency_point();
         }
-        for (int idx = tid; idx < NQ * D / 2; idx += kThreads) {
+        __syncwarp();
+        for (int idx = lane; idx < NQ * D / 2; idx += 32) {
             const int j = idx / (D / 2), cp = idx % (D / 2);
             const float2 qv = __half22float2(
                 *reinterpret_cast<const __half2*>(a.q + ((long long)b * a.Hq + hk * NQ + j) * D + 2 * cp));
@@ -742,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             qhc_s[j][cp] = hic;
             qlc_s[j][cp] = pack_f16x2(y0 - hcf.x, y1 - hcf.y);
         }
-        __syncthreads();
+        __syncwarp();
 
         m = -INFINITY; l = 0.f;
         fresh = true;
@@ -925,9 +932,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 }
             }
         }
-        // ---- this warp's residual pairs: 32 fp16 rows each, A operands straight from memory ----
-        const int rw = (r1 - r0 + kWarps - 1) / kWarps;
-        const int rb = min(r0 + warp * rw, r1), re = min(rb + rw, r1);
+        // ---- the segment's residual pairs: 32 fp16 rows each, A operands straight from memory ----
+        const int rb = r0, re = r1;
         if (rb < re) {
             const __half* kr = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + rslot * a.R * D;
             const __half* vr = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + rslot * a.R * D;
@@ -987,7 +993,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             }
         }
 
-        // ---- merge the warps, write the slot's partial (m, l, status, o) ----
+        // ---- the segment's partial result (m, l, status, o) per query head ----
+        const uint32_t st_all = (uint32_t)__reduce_or_sync(kFull, status | (PAGED && bad_page ? 2u : 0u));
 #pragma unroll
         for (int f = 0; f < NBF; ++f) {
             zeta[f] += __shfl_xor_sync(kFull, zeta[f], 1);
@@ -997,46 +1004,39 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         lt += __shfl_xor_sync(kFull, lt, 4);
         lt += __shfl_xor_sync(kFull, lt, 8);
         lt += __shfl_xor_sync(kFull, lt, 16);
-        if (g == 0 && i < NQ) { red_m[warp][i] = m; red_l[warp][i] = lt; }
-        if (status && lane == 0) atomicOr(&red_status, status);
-        if (PAGED && bad_page) atomicOr(&red_status, 2u);
-        if (i == 0 && !lo_col && col_ok) {
+        // the zero-point sums of this lane's output column i sit in lanes 8i .. 8i+3
+        float zo[NBF];
 #pragma unroll
-            for (int f = 0; f < NBF; ++f) red_z[warp][hP][f * GB + jP] = zeta[f];
-        }
+        for (int f = 0; f < NBF; ++f) zo[f] = __shfl_sync(kFull, zeta[f], 8 * i);
+        auto partial = [&](int h) -> float* {
+            return a.ws + ((long long)(b * a.Hq + hk * NQ + h) * kPartialSlots + part) * partial_stride(D);
+        };
         if (hO < NQ) {
+            float* pw = partial(hO);
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int gr = 16 * mt / G;
                 if (gr % GB == jO) {
-                    red_o[warp][hO][16 * mt + g] = o[mt][0] + o[mt][1];
-                    red_o[warp][hO][16 * mt + g + 8] = o[mt][2] + o[mt][3];
+                    const float z = zo[gr / GB];
+                    pw[4 + 16 * mt + g] = o[mt][0] + o[mt][1] + z;
+                    pw[4 + 16 * mt + g + 8] = o[mt][2] + o[mt][3] + z;
                 }
             }
         }
-        __syncthreads();
-        for (int idx = tid; idx < NQ * D; idx += kThreads) {
-            const int j = idx / D, c = idx % D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][j]);
-            float acc = 0.f, lsum = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                if (red_m[w][j] == -INFINITY) continue;
-                const float e = exp2f(red_m[w][j] - M);
-                acc = fmaf(red_o[w][j][c] + red_z[w][j][c / G], e, acc);
-                lsum = fmaf(red_l[w][j], e, lsum);
-            }
-            float* pw = a.ws + ((long long)(b * a.Hq + hk * NQ + j) * kPartialSlots + part) * partial_stride(D);
-            if (c == 0) { pw[0] = M; pw[1] = lsum; }
-            if (c == 1) pw[2] = (float)red_status;
-            pw[4 + c] = acc;
+        if (g == 0 && i < NQ) {
+            float* pw = partial(i);
+            pw[0] = m;
+            pw[1] = lt;
+            pw[2] = (float)st_all;
         }
-        __syncthreads();                               // qf and red_* are reused by the next segment
         pos = u1 >= NU ? w0 + Ws : w0 + unit_start_p(P, wm.wq, wm.wr, wm.S0, u1);
     }
+    if (first_seg) dependency_point();   // a warp without a segment still stores its share of the rows
 }
+
+#undef qf
+#undef qhc_s
+#undef qlc_s
 
 // One CTA (kMergeThreads threads) per (query row, query head): the
 // log-sum-exp merge of the head's nparts partial results -> fp16 output.  The

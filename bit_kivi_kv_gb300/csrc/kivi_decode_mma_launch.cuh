@@ -46,19 +46,21 @@ cudaError_t launch_one(typename mma_detail::ArgsOf<MODE>::type& a, int num_sms, 
             setup.per_sm[dev] = per_sm;
         }
     }
-    // slots of the largest weight (paged calls: wm.Ws is the largest slot's)
-    const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;
-    long long n = (long long)num_sms * per_sm;
-    if (a.wm.n > 0 && a.wm.n < n) n = a.wm.n;                         // the caller's cap on the grid
+    // the workers of the map are warps: the resident warps of a persistent grid
+    // (or the caller's cap on CTAs, times the warps of a CTA)
+    const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;   // slots of the largest weight
+    long long n = (long long)num_sms * per_sm * kWarps;
+    if (a.wm.n > 0 && a.wm.n * kWarps < n) n = a.wm.n * kWarps;
     const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
-    if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every CTA owns a unit
+    if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every warp owns a unit
     if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot
     if (n < 1) n = 1;
     a.wm.n = n;
+    const long long ctas = (n + kWarps - 1) / kWarps;
     // a programmatic dependent of the preceding kernel: the kernel's prologue
     // and first cache copies overlap that kernel's tail
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3((unsigned)n);
+    lc.gridDim = dim3((unsigned)ctas);
     lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = kDyn;
     lc.stream = st;

@@ -1,8 +1,8 @@
 // Host-only check of the decode partition (the work map in kivi_common.cuh),
 // built and run by tests/test_partition.py.  For random dense and ragged calls
-// it walks every CTA's weight range the way the decode kernel does and checks
-// that every unit (tile pair or residual pair) of every slot is owned by
-// exactly one CTA, that a slot's partial indices are 0 .. parts-1 with no gap,
+// it walks every worker's (warp's) weight range the way the decode kernel does
+// and checks that every unit (tile pair or residual pair) of every slot is
+// owned by exactly one worker, that a slot's partial indices are 0 .. parts-1 with no gap,
 // and that no slot has more partials than the workspace holds.
 #include <cstdio>
 #include <random>
@@ -18,10 +18,11 @@ struct Slot {
     long long P, PR, w0, Ws;
 };
 
-// the grid size rule of the launch (occupancy, then the two bounds, then a cap)
+// the worker-count rule of the launch: resident warps (4 a CTA), or the
+// caller's cap on CTAs times 4, then the two bounds
 long long grid_size(long long Wt, long long wmax, long long slots_of_max, long long resident, long long cap) {
-    long long n = resident;
-    if (cap > 0 && cap < n) n = cap;
+    long long n = resident * 4;
+    if (cap > 0 && cap * 4 < n) n = cap * 4;
     if (n > Wt / wmax) n = Wt / wmax;
     if (n > (kMaxSplits - 1) * slots_of_max) n = (kMaxSplits - 1) * slots_of_max;
     return n < 1 ? 1 : n;
