@@ -657,7 +657,20 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         const long long NU = P + PR;
         const long long u0 = first_unit_at_p(P, wm.wq, wm.wr, wm.S0, pos - w0);
         if (u0 >= NU) { pos = w0 + Ws; continue; }
-        if (w0 + unit_start_p(P, wm.wq, wm.wr, wm.S0, u0) >= pe) break;
+        if (w0 + unit_start_p(P, wm.wq, wm.wr, wm.S0, u0) >= pe) {
+            // no unit of the slot starts in this warp's range: if the range lies
+            // between the slot's first and last unit starts, the slot still
+            // counts this warp's partial, so write it empty (weight 0)
+            if (u0 > 0) {
+                const long long part = gw - map_owner(wm, w0 + wm.S0);
+                for (int idx = lane; idx < NQ * (D + 4); idx += 32) {
+                    const int h = idx / (D + 4), c = idx % (D + 4);
+                    float* pw = a.ws + ((long long)(b * a.Hq + hk * NQ + h) * kPartialSlots + part) * partial_stride(D);
+                    pw[c] = c == 0 ? -INFINITY : 0.f;
+                }
+            }
+            break;
+        }
         const long long u1 = first_unit_at_p(P, wm.wq, wm.wr, wm.S0, min(pe - w0, Ws));
         const int p0 = (int)min(u0, P), p1 = (int)min(u1, P);                  // quantized pairs
         const int r0 = (int)(max(u0, P) - P), r1 = (int)(max(u1, P) - P);      // residual pairs
@@ -772,8 +785,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             float sc[4];
             if constexpr (BITS == 8) {
                 // one tile at a time: a lane's 16 words per tile, shifted in place
-                float ca[4] = {beta, 0.f, beta, 0.f};
-                float cb[4] = {beta, 0.f, beta, 0.f};
+                float ca[4] = {0.f, 0.f, 0.f, 0.f};
+                float cb[4] = {0.f, 0.f, 0.f, 0.f};
                 {
                     uint32_t w[W];
                     lds_words(stage_u32 + C::KT, w);
@@ -794,18 +807,20 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                         mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
                     }
                 }
-                sc[0] = ca[0] + ca[1];
-                sc[1] = ca[2] + ca[3];
-                sc[2] = cb[0] + cb[1];
-                sc[3] = cb[2] + cb[3];
+                // the block's zero-point term joins after the MMAs, so its
+                // reduction over the lanes runs beside them
+                sc[0] = ca[0] + (ca[1] + beta);
+                sc[1] = ca[2] + (ca[3] + beta);
+                sc[2] = cb[0] + (cb[1] + beta);
+                sc[3] = cb[2] + (cb[3] + beta);
             } else {
                 uint32_t wa[W], wbw[W], wa8[W], wb8[W];
                 lds_words(stage_u32 + C::KT, wa);
                 lds_words(stage_u32 + C::KT + C::TILE, wbw);
 #pragma unroll
                 for (int x = 0; x < W; ++x) { wa8[x] = wa[x] >> 8; wb8[x] = wbw[x] >> 8; }
-                float ca[4] = {beta, 0.f, beta, 0.f};
-                float cb[4] = {beta, 0.f, beta, 0.f};
+                float ca[4] = {0.f, 0.f, 0.f, 0.f};
+                float cb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     uint32_t fa[4], fb[4];
@@ -814,10 +829,12 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
                     mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
                 }
-                sc[0] = ca[0] + ca[1];
-                sc[1] = ca[2] + ca[3];
-                sc[2] = cb[0] + cb[1];
-                sc[3] = cb[2] + cb[3];
+                // the block's zero-point term joins after the MMAs, so its
+                // reduction over the lanes runs beside them
+                sc[0] = ca[0] + (ca[1] + beta);
+                sc[1] = ca[2] + (ca[3] + beta);
+                sc[2] = cb[0] + (cb[1] + beta);
+                sc[3] = cb[2] + (cb[3] + beta);
             }
             bool live = true;                          // the pair has a token to count in this pass
             if constexpr (FIFO) {
@@ -1106,8 +1123,9 @@ __device__ __forceinline__ void merge_head(const float* base, int nparts, __half
 #pragma unroll
     for (int u = 0; u < NR; ++u) {
         const int j = warp + u * kMergeWarps;
-        if (j < nparts) {
-            const float e = e_s[j];
+        // a weight of 0 (an empty partial, m = -inf) adds nothing, whatever its values hold
+        const float e = j < nparts ? e_s[j] : 0.f;
+        if (e != 0.f) {
 #pragma unroll
             for (int r = 0; r < CPL; ++r) acc[r] = fmaf(v[u][r], e, acc[r]);
         }

@@ -51,9 +51,11 @@ cudaError_t launch_one(typename mma_detail::ArgsOf<MODE>::type& a, int num_sms, 
     const long long slots = a.wm.Ws > 0 ? a.wm.Wt / a.wm.Ws : 1;   // slots of the largest weight
     long long n = (long long)num_sms * per_sm * kWarps;
     if (a.wm.n > 0 && a.wm.n * kWarps < n) n = a.wm.n * kWarps;
-    const long long wmax = a.wm.wq > a.wm.wr ? a.wm.wq : a.wm.wr;
-    if (n > a.wm.Wt / wmax) n = a.wm.Wt / wmax;                       // every warp owns a unit
-    if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;   // at most kMaxSplits partials per slot
+    // (a warp whose range holds no unit start inside a slot writes an empty
+    // partial; at most kMaxSplits partials per slot)
+    if (n > (kMaxSplits - 1) * slots) n = (kMaxSplits - 1) * slots;
+    const long long units = a.wm.Wt / (a.wm.wq < a.wm.wr ? a.wm.wq : a.wm.wr);
+    if (n > units) n = units;                                          // no more warps than units
     if (n < 1) n = 1;
     a.wm.n = n;
     const long long ctas = (n + kWarps - 1) / kWarps;

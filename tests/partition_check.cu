@@ -2,8 +2,10 @@
 // built and run by tests/test_partition.py.  For random dense and ragged calls
 // it walks every worker's (warp's) weight range the way the decode kernel does
 // and checks that every unit (tile pair or residual pair) of every slot is
-// owned by exactly one worker, that a slot's partial indices are 0 .. parts-1 with no gap,
-// and that no slot has more partials than the workspace holds.
+// owned by exactly one worker, that a slot's partial indices (workers with
+// units, and workers inside the slot without a unit start, which write an
+// empty partial) are 0 .. parts-1 once each, and that no slot has more
+// partials than the workspace holds.
 #include <cstdio>
 #include <random>
 #include <vector>
@@ -20,16 +22,16 @@ struct Slot {
 
 // the worker-count rule of the launch: resident warps (4 a CTA), or the
 // caller's cap on CTAs times 4, then the two bounds
-long long grid_size(long long Wt, long long wmax, long long slots_of_max, long long resident, long long cap) {
+long long grid_size(long long Wt, long long wmin, long long slots_of_max, long long resident, long long cap) {
     long long n = resident * 4;
     if (cap > 0 && cap * 4 < n) n = cap * 4;
-    if (n > Wt / wmax) n = Wt / wmax;
     if (n > (kMaxSplits - 1) * slots_of_max) n = (kMaxSplits - 1) * slots_of_max;
+    if (n > Wt / wmin) n = Wt / wmin;
     return n < 1 ? 1 : n;
 }
 
 bool check(const std::vector<Slot>& slots, const WorkMap& wm, int trial) {
-    std::vector<std::vector<int>> owner(slots.size()), part(slots.size());
+    std::vector<std::vector<int>> owner(slots.size()), part(slots.size()), empty(slots.size());
     for (size_t s = 0; s < slots.size(); ++s) {
         owner[s].assign((size_t)(slots[s].P + slots[s].PR), -1);
         part[s].assign((size_t)(slots[s].P + slots[s].PR), -1);
@@ -45,7 +47,11 @@ bool check(const std::vector<Slot>& slots, const WorkMap& wm, int trial) {
             const long long NU = sl.P + sl.PR;
             const long long u0 = first_unit_at_p(sl.P, wm.wq, wm.wr, wm.S0, pos - sl.w0);
             if (u0 >= NU) { pos = sl.w0 + sl.Ws; continue; }
-            if (sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, u0) >= pe) break;
+            if (sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, u0) >= pe) {
+                // no unit start in the range: inside the slot, an empty partial
+                if (u0 > 0) empty[si].push_back((int)(c - map_owner(wm, sl.w0 + wm.S0)));
+                break;
+            }
             const long long u1 = first_unit_at_p(sl.P, wm.wq, wm.wr, wm.S0, pe - sl.w0 < sl.Ws ? pe - sl.w0 : sl.Ws);
             const long long p = c - map_owner(wm, sl.w0 + wm.S0);
             for (long long u = u0; u < u1; ++u) {
@@ -66,6 +72,10 @@ bool check(const std::vector<Slot>& slots, const WorkMap& wm, int trial) {
             if (owner[s][u] < 0) { std::printf("trial %d: unit not owned\n", trial); return false; }
             if (part[s][u] < 0 || part[s][u] >= nparts) { std::printf("trial %d: part out of range\n", trial); return false; }
             seen[(size_t)part[s][u]] = 1;
+        }
+        for (int p : empty[s]) {
+            if (p < 0 || p >= nparts || seen[(size_t)p]) { std::printf("trial %d: bad empty part %d\n", trial, p); return false; }
+            seen[(size_t)p] = 1;
         }
         for (long long p = 0; p < nparts; ++p)
             if (!seen[(size_t)p]) { std::printf("trial %d: part %lld has no unit\n", trial, p); return false; }
@@ -109,7 +119,7 @@ int main() {
         wm.P = slots[0].P;
         wm.PR = slots[0].PR;
         const long long resident = (long long)num_sms * pick(1, 4);
-        wm.n = grid_size(wm.Wt, wm.wq > wm.wr ? wm.wq : wm.wr, wm.Wt / ws_max, resident,
+        wm.n = grid_size(wm.Wt, wm.wq < wm.wr ? wm.wq : wm.wr, wm.Wt / ws_max, resident,
                          trial % 5 == 0 ? pick(1, 64) : 0);
         if (!check(slots, wm, trial)) return 1;
         if (!ragged) {
