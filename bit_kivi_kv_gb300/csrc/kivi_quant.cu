@@ -53,6 +53,48 @@ __device__ __forceinline__ uint32_t nearest_code_r(float x, float s, float r, fl
     return (uint32_t)min(c, L);
 }
 
+// ---- 2-bit codes from per-group thresholds ----
+// The fixed formula code(x) = clamp(rint(rn(rn(x - z) / s)), 0, L) is
+// non-decreasing in x (each rounded step is monotone for s > 0), so a group's
+// code of x is the number of levels c = 1..L whose threshold T_c, the least
+// fp16 value with code(T_c) >= c, x reaches.  T_c is found next to the real
+// crossing z + (c - 1/2) s by evaluating the formula itself (IEEE division) on
+// fp16 neighbours, so the codes are those of the formula bit for bit; the
+// elements are then compared with the thresholds two at a time in fp16.
+
+// fp16 values in order as integers (-0 and +0 both 0) and back
+__device__ __forceinline__ int half_ord(__half h) {
+    const int b = __half_as_ushort(h);
+    return (b & 0x8000) ? -(b & 0x7FFF) : b;
+}
+__device__ __forceinline__ __half ord_half(int o) {
+    return __ushort_as_half((unsigned short)(o >= 0 ? o : (0x8000 | -o)));
+}
+
+// T_c of a group with stored step s > 0 and zero z (fp32 values of fp16
+// entries).  The probes sit next to a half-step by construction, so they take
+// the IEEE division directly.
+__device__ __forceinline__ __half level_threshold(int c, float s, float z, int L) {
+    auto reaches = [&](int o) { return (int)nearest_code(__half2float(ord_half(o)), s, z, L) >= c; };
+    int o = half_ord(__float2half_rn(__fmaf_rn((float)c - 0.5f, s, z)));
+    // the crossing is within a few fp16 steps of the estimate; the walks are bounded
+    // (o stays inside the finite range, where the formula reaches L at the group max)
+    if (reaches(o)) {
+        for (int k = 0; k < 64 && o > -0x7BFF && reaches(o - 1); ++k) --o;
+    } else {
+        for (int k = 0; k < 64 && o < 0x7BFF && !reaches(o); ++k) ++o;
+    }
+    return ord_half(o);
+}
+
+// Two 2-bit codes (lo and hi halves) of x against half2 thresholds: each half
+// of the result holds 0x6400 + code (the code in bits 0-1).
+__device__ __forceinline__ uint32_t codes2_from_thresholds(__half2 x, __half2 t1, __half2 t2, __half2 t3) {
+    const __half2 one024 = __half2half2(__ushort_as_half(0x6400));   // 1024: its ulp is 1
+    const __half2 c = __hadd2(__hadd2(__hge2(x, t1), __hge2(x, t2)), __hadd2(__hge2(x, t3), one024));
+    return *reinterpret_cast<const uint32_t*>(&c);
+}
+
 struct QuantArgs {
     uint8_t* cache;
     const __half* src_k;
@@ -101,6 +143,9 @@ __global__ void __launch_bounds__(kQuantThreads)
     __half* xs = reinterpret_cast<__half*>(smem);            // [G][DP]
     // per group: (step, rn(1 / step), zero, unused); D groups for keys and for values
     float4* szr = reinterpret_cast<float4*>(xs + G * DP);
+    // 2-bit codes: the groups' level thresholds T_1..T_3 (fp16), [3][D] each:
+    // keys by channel, values by (channel group, token)
+    __half* thr = reinterpret_cast<__half*>(szr + D);
 
     const int tid = threadIdx.x;
     const __half* blk_k;   // the block's G rows of keys / values
@@ -157,8 +202,43 @@ __global__ void __launch_bounds__(kQuantThreads)
         float sc, zc;
         group_step_zero(half ? mn.y : mn.x, half ? mx.y : mx.x, L, &sc, &zc, &ent[c], &ent[D + c]);
         szr[c] = make_float4(sc, sc != 0.0f ? __frcp_rn(sc) : 0.0f, zc, 0.0f);
+        if constexpr (BITS == 2) {
+#pragma unroll
+            for (int lv = 1; lv <= 3; ++lv)
+                thr[(lv - 1) * D + c] = sc == 0.0f ? __ushort_as_half(0x7C00) : level_threshold(lv, sc, zc, L);
+        }
     }
     __syncthreads();
+    if constexpr (BITS == 2) {
+        // each thread packs one word position of every tile: 8 code pairs, each
+        // two adjacent channels of one token, compared with their thresholds
+        using PP = PairPlace<BITS, false>;
+        for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
+            const int lane = wt / W, wl = wt - lane * W;
+            const int g = lane >> 2, i = lane & 3;
+            int off[PER], bit[PER];
+            __half2 t1[PER], t2[PER], t3[PER];
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int k = PP::k_of(wl, u), r = PP::r_of(wl, u);
+                const int ch = 16 * k + 2 * i + 8 * (r >> 1);
+                off[u] = (g + 8 * (r & 1)) * DP + ch;
+                bit[u] = PP::bit(k, r);
+                t1[u] = *reinterpret_cast<const __half2*>(thr + ch);
+                t2[u] = *reinterpret_cast<const __half2*>(thr + D + ch);
+                t3[u] = *reinterpret_cast<const __half2*>(thr + 2 * D + ch);
+            }
+            for (int tt = 0; tt < TPB; ++tt) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int u = 0; u < PER; ++u) {
+                    const __half2 x = *reinterpret_cast<const __half2*>(xs + tt * 16 * DP + off[u]);
+                    word |= (codes2_from_thresholds(x, t1[u], t2[u], t3[u]) & 0x00030003u) << bit[u];
+                }
+                reinterpret_cast<uint32_t*>(part_k)[tt * TILE_WORDS + wt] = word;
+            }
+        }
+    } else
     for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
         using PP = PairPlace<BITS, false>;
         const int lane = wt / W, wl = wt - lane * W;
@@ -199,10 +279,14 @@ __global__ void __launch_bounds__(kQuantThreads)
         const int t = e / ngrp, gr = e % ngrp;
         const __half* row = xs + t * DP + gr * G;
         __half2 mn2 = __half2half2(__ushort_as_half(0x7C00)), mx2 = __half2half2(__ushort_as_half(0xFC00));
-        for (int jj = 0; jj < G / 2; ++jj) {           // channel pairs; the rotated start spreads banks
-            const __half2 v = *reinterpret_cast<const __half2*>(row + 2 * ((jj + tid + 4 * t) & (G / 2 - 1)));
-            mn2 = __hmin2(mn2, v);
-            mx2 = __hmax2(mx2, v);
+        for (int jj = 0; jj < G / 8; ++jj) {           // 8 channels a load; the rotated start spreads banks
+            const uint4 v4 = *reinterpret_cast<const uint4*>(row + 8 * ((jj + tid) & (G / 8 - 1)));
+            const __half2* h = reinterpret_cast<const __half2*>(&v4);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                mn2 = __hmin2(mn2, h[q]);
+                mx2 = __hmax2(mx2, h[q]);
+            }
         }
         const float2 mnf = __half22float2(mn2), mxf = __half22float2(mx2);
         float mn = fminf(mnf.x, mnf.y), mx = fmaxf(mxf.x, mxf.y);
@@ -216,8 +300,54 @@ __global__ void __launch_bounds__(kQuantThreads)
         float se, ze;
         group_step_zero(mn, mx, L, &se, &ze, &ent[at], &ent[16 * ngrp + at]);
         szr[e] = make_float4(se, se != 0.0f ? __frcp_rn(se) : 0.0f, ze, 0.0f);
+        if constexpr (BITS == 2) {
+#pragma unroll
+            for (int lv = 1; lv <= 3; ++lv)
+                thr[(lv - 1) * D + gr * G + t] = se == 0.0f ? __ushort_as_half(0x7C00) : level_threshold(lv, se, ze, L);
+        }
     }
     __syncthreads();
+    if constexpr (BITS == 2) {
+        // each thread packs one word position of every tile: 8 code pairs, each
+        // one channel of two consecutive tokens, compared with the tokens' thresholds
+        using PP = PairPlace<BITS, true>;
+        for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
+            const int lane = wt / W, wl = wt - lane * W;
+            const int g = lane >> 2, i = lane & 3;
+            // the word's channels 16k + g (+8), k in {2wl, 2wl+1}, lie in one group of
+            // G >= 32 channels; its tokens are 2i, 2i+1 (r < 2) and 2i+8, 2i+9 (r >= 2)
+            int off[PER], bit[PER];
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int k = PP::k_of(wl, u), r = PP::r_of(wl, u);
+                const int ch = 16 * k + g + 8 * (r & 1);
+                off[u] = (2 * i + 8 * (r >> 1)) * DP + ch;
+                bit[u] = PP::bit(k, r);
+            }
+            const int tgrp = ((16 * PP::k_of(wl, 0)) / G) * G + 2 * i;   // thresholds of (group, token 2i)
+            for (int tt = 0; tt < TPB; ++tt) {
+                const __half* tp = thr + tgrp + tt * 16;
+                const __half2 a1 = *reinterpret_cast<const __half2*>(tp);
+                const __half2 a2 = *reinterpret_cast<const __half2*>(tp + D);
+                const __half2 a3 = *reinterpret_cast<const __half2*>(tp + 2 * D);
+                const __half2 b1 = *reinterpret_cast<const __half2*>(tp + 8);
+                const __half2 b2 = *reinterpret_cast<const __half2*>(tp + 8 + D);
+                const __half2 b3 = *reinterpret_cast<const __half2*>(tp + 8 + 2 * D);
+                uint32_t word = 0;
+#pragma unroll
+                for (int u = 0; u < PER; ++u) {
+                    // r = PP::r_of(wl, u) = (u & 1) + 2 * (u >> 2) for 2-bit codes (wl * 4 is even)
+                    const bool first_tokens = (u >> 2) == 0;
+                    const __half* xp = xs + tt * 16 * DP + off[u];
+                    const __half2 x = __halves2half2(xp[0], xp[DP]);
+                    const uint32_t c2 = first_tokens ? codes2_from_thresholds(x, a1, a2, a3)
+                                                     : codes2_from_thresholds(x, b1, b2, b3);
+                    word |= (c2 & 0x00030003u) << bit[u];
+                }
+                reinterpret_cast<uint32_t*>(part_v)[tt * TILE_WORDS + wt] = word;
+            }
+        }
+    } else
     for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
         using PP = PairPlace<BITS, true>;
         const int lane = wt / W, wl = wt - lane * W;
@@ -340,7 +470,8 @@ __global__ void __launch_bounds__(128) copy_rows_kernel(uint8_t* cache, const __
 
 template <bool PAGED>
 cudaError_t launch_q(const typename QuantArgsOf<PAGED>::type& a, const Geometry& g, dim3 grid, cudaStream_t st) {
-    const size_t smem = (size_t)g.G * (g.D + 8) * 2 + 16 * (size_t)g.D;   // staged rows + (step, 1/step, zero) per group
+    // staged rows + (step, 1/step, zero) per group + three fp16 level thresholds per group
+    const size_t smem = (size_t)g.G * (g.D + 8) * 2 + 16 * (size_t)g.D + 6 * (size_t)g.D;
 #define KIVI_Q(DD, BB)                                                                          \
     if (g.D == DD && g.bits == BB) {                                                            \
         quantize_blocks_kernel<DD, BB, PAGED><<<grid, kQuantThreads, smem, st>>>(a);            \
