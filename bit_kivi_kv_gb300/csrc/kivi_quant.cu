@@ -75,8 +75,20 @@ __device__ __forceinline__ __half ord_half(int o) {
 // entries).  The probes sit next to a half-step by construction, so they take
 // the IEEE division directly.
 __device__ __forceinline__ __half level_threshold(int c, float s, float z, int L) {
+    // The real crossing is y = z + (c - 1/2) s.  For fp16 x at least delta above
+    // y, rn(rn(x - z) / s) > c - 1/2 (two roundings of relative 2^-24 each, and
+    // y's own rounding), so code(x) >= c; at least delta below, code(x) < c.  So
+    // when no fp16 value lies within delta of y, T_c is the least fp16 >= y.
+    const float y = __fmaf_rn((float)c - 0.5f, s, z);
+    const float delta = __fmaf_rn((float)c, s, fabsf(y)) * 0x1p-20f;
+    const __half up = __float2half_ru(y);
+    const int ou = half_ord(up);
+    if (ou > -0x7BFF && ou <= 0x7BFF) {
+        const float above = __half2float(up), below = __half2float(ord_half(ou - 1));
+        if (above - y > delta && y - below > delta) return up;
+    }
     auto reaches = [&](int o) { return (int)nearest_code(__half2float(ord_half(o)), s, z, L) >= c; };
-    int o = half_ord(__float2half_rn(__fmaf_rn((float)c - 0.5f, s, z)));
+    int o = half_ord(__float2half_rn(y));
     // the crossing is within a few fp16 steps of the estimate; the walks are bounded
     // (o stays inside the finite range, where the formula reaches L at the group max)
     if (reaches(o)) {
@@ -129,7 +141,7 @@ struct QuantArgsOf<true> { using type = PagedQuantArgs; };
 // thread packs the same word position of every 16-token tile, so the
 // coordinates of its codes (and, for keys, their steps and zeros) are fixed
 // once per block.
-template <int D, int BITS, bool PAGED>
+template <int D, int BITS, int G, bool PAGED>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_blocks_kernel(const __grid_constant__ typename QuantArgsOf<PAGED>::type a) {
     constexpr int L = (1 << BITS) - 1;
@@ -138,8 +150,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     constexpr int TILE_WORDS = 32 * W;
     constexpr int DP = D + 8;               // staged row stride, halves
     extern __shared__ __align__(16) unsigned char smem[];
-    const int G = a.G;
-    const int TPB = G / 16;
+    constexpr int TPB = G / 16;
     __half* xs = reinterpret_cast<__half*>(smem);            // [G][DP]
     // per group: (step, rn(1 / step), zero, unused); D groups for keys and for values
     float4* szr = reinterpret_cast<float4*>(xs + G * DP);
@@ -211,10 +222,12 @@ __global__ void __launch_bounds__(kQuantThreads)
     __syncthreads();
     if constexpr (BITS == 2) {
         // each thread packs one word position of every tile: 8 code pairs, each
-        // two adjacent channels of one token, compared with their thresholds
+        // two adjacent channels of one token, compared with their thresholds.  A
+        // warp takes one word column (wl) of all 32 lanes, so its rows (tokens g,
+        // g + 8) and channel pairs fall in distinct banks.
         using PP = PairPlace<BITS, false>;
         for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
-            const int lane = wt / W, wl = wt - lane * W;
+            const int lane = wt & 31, wl = wt >> 5;
             const int g = lane >> 2, i = lane & 3;
             int off[PER], bit[PER];
             __half2 t1[PER], t2[PER], t3[PER];
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(kQuantThreads)
                     const __half2 x = *reinterpret_cast<const __half2*>(xs + tt * 16 * DP + off[u]);
                     word |= (codes2_from_thresholds(x, t1[u], t2[u], t3[u]) & 0x00030003u) << bit[u];
                 }
-                reinterpret_cast<uint32_t*>(part_k)[tt * TILE_WORDS + wt] = word;
+                reinterpret_cast<uint32_t*>(part_k)[tt * TILE_WORDS + lane * W + wl] = word;
             }
         }
     } else
@@ -309,10 +322,11 @@ __global__ void __launch_bounds__(kQuantThreads)
     __syncthreads();
     if constexpr (BITS == 2) {
         // each thread packs one word position of every tile: 8 code pairs, each
-        // one channel of two consecutive tokens, compared with the tokens' thresholds
+        // one channel of two consecutive tokens, compared with the tokens'
+        // thresholds; a warp takes one word column of all 32 lanes
         using PP = PairPlace<BITS, true>;
         for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
-            const int lane = wt / W, wl = wt - lane * W;
+            const int lane = wt & 31, wl = wt >> 5;
             const int g = lane >> 2, i = lane & 3;
             // the word's channels 16k + g (+8), k in {2wl, 2wl+1}, lie in one group of
             // G >= 32 channels; its tokens are 2i, 2i+1 (r < 2) and 2i+8, 2i+9 (r >= 2)
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(kQuantThreads)
                                                      : codes2_from_thresholds(x, b1, b2, b3);
                     word |= (c2 & 0x00030003u) << bit[u];
                 }
-                reinterpret_cast<uint32_t*>(part_v)[tt * TILE_WORDS + wt] = word;
+                reinterpret_cast<uint32_t*>(part_v)[tt * TILE_WORDS + lane * W + wl] = word;
             }
         }
     } else
@@ -472,12 +486,14 @@ template <bool PAGED>
 cudaError_t launch_q(const typename QuantArgsOf<PAGED>::type& a, const Geometry& g, dim3 grid, cudaStream_t st) {
     // staged rows + (step, 1/step, zero) per group + three fp16 level thresholds per group
     const size_t smem = (size_t)g.G * (g.D + 8) * 2 + 16 * (size_t)g.D + 6 * (size_t)g.D;
-#define KIVI_Q(DD, BB)                                                                          \
-    if (g.D == DD && g.bits == BB) {                                                            \
-        quantize_blocks_kernel<DD, BB, PAGED><<<grid, kQuantThreads, smem, st>>>(a);            \
+#define KIVI_Q(DD, BB, GG)                                                                      \
+    if (g.D == DD && g.bits == BB && g.G == GG) {                                               \
+        quantize_blocks_kernel<DD, BB, GG, PAGED><<<grid, kQuantThreads, smem, st>>>(a);        \
         return cudaGetLastError();                                                              \
     }
-    KIVI_Q(128, 2) KIVI_Q(128, 4) KIVI_Q(128, 8) KIVI_Q(64, 2) KIVI_Q(64, 4) KIVI_Q(64, 8)
+#define KIVI_QG(DD, BB) KIVI_Q(DD, BB, 32) KIVI_Q(DD, BB, 64) if (DD >= 128) { KIVI_Q(128, BB, 128) }
+    KIVI_QG(128, 2) KIVI_QG(128, 4) KIVI_QG(128, 8) KIVI_QG(64, 2) KIVI_QG(64, 4) KIVI_QG(64, 8)
+#undef KIVI_QG
 #undef KIVI_Q
     return cudaErrorInvalidValue;
 }
