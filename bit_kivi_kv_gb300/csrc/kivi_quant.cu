@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
                 for (int u = 0; u < PER; ++u) {
                     const __half2 x = *reinterpret_cast<const __half2*>(xs + tt * 16 * DP + off[u]);
-                    word |= (codes2_from_thresholds(x, t1[u], t2[u], t3[u]) & 0x00030003u) << bit[u];
+                    word |= (codes2_from_thresholds(x, t1[u], t2[u], t3[u]) << bit[u]) & (0x00030003u << bit[u]);
                 }
                 reinterpret_cast<uint32_t*>(part_k)[tt * TILE_WORDS + lane * W + wl] = word;
             }
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kQuantThreads)
                     const __half2 x = __halves2half2(xp[0], xp[DP]);
                     const uint32_t c2 = first_tokens ? codes2_from_thresholds(x, a1, a2, a3)
                                                      : codes2_from_thresholds(x, b1, b2, b3);
-                    word |= (c2 & 0x00030003u) << bit[u];
+                    word |= (c2 << bit[u]) & (0x00030003u << bit[u]);
                 }
                 reinterpret_cast<uint32_t*>(part_v)[tt * TILE_WORDS + lane * W + wl] = word;
             }
