@@ -77,9 +77,10 @@ kivi_status ensure_device(kivi_cache_t c) {
 
 // Value queue, before an append stores its token: flush the key residual when
 // full (its blocks get their values as not quantized yet: they are all still
-// queued), then quantize the oldest queued value, whose ring row the new token
-// takes.  *wrote: a kernel that writes quantized blocks was launched.
-static kivi_status queue_before_append(kivi_cache* c, cudaStream_t st, bool* wrote);
+// queued), then, with pop, quantize the oldest queued value, whose ring row
+// the new token takes (a fused append-and-decode leaves that to its decode
+// kernel).  *wrote: a kernel that writes quantized blocks was launched.
+static kivi_status queue_before_append(kivi_cache* c, cudaStream_t st, bool pop, bool* wrote);
 
 namespace kivi {
 
@@ -242,7 +243,7 @@ kivi_status kivi_append(kivi_cache_t c, const void* k, const void* v, kivi_strea
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (c->value_queue) {
         bool unused;
-        const kivi_status sq = queue_before_append(c, st, &unused);
+        const kivi_status sq = queue_before_append(c, st, true, &unused);
         if (sq != KIVI_OK) return sq;
         const long long L = c->n_quant + c->n_resid;
         const cudaError_t e = kivi::launch_copy_rows_ring(g, c->buf, static_cast<const __half*>(k),
@@ -364,15 +365,18 @@ kivi_status kivi_append_decode(kivi_cache_t c, const void* k, const void* v, con
     cudaStream_t sp = reinterpret_cast<cudaStream_t>(stream);
     bool flushed = false;
     if (c->value_queue) {
-        const kivi_status sq = queue_before_append(c, sp, &flushed);
+        const kivi_status sq = queue_before_append(c, sp, false, &flushed);
         if (sq != KIVI_OK) return sq;
-        const long long L = c->n_quant + c->n_resid + 1;   // with the new token
+        // the decode kernel pops position L - R (quantizes that value into its
+        // block, counts it as quantized) and stores the new value in its ring row
+        const long long L = c->n_quant + c->n_resid;   // before the new token
         kivi::FusedAppend fa;
         fa.k = static_cast<const __half*>(k);
         fa.v = static_cast<const __half*>(v);
         fa.row = (int)c->n_resid;
         fa.early_ok = flushed ? 0 : 1;
-        fa.lqv = L > g.R ? L - g.R : 0;
+        fa.lqv = L >= g.R ? L + 1 - g.R : 0;
+        fa.pop = L >= g.R ? L - g.R : -1;
         const kivi_status sd = decode_launch(c, q, out, softmax_scale, workspace, c->n_resid + 1, variant, stream, fa);
         if (sd != KIVI_OK) return sd;
         c->n_resid += 1;
@@ -453,7 +457,7 @@ size_t decode_workspace_need(const kivi_cache* c) {
 
 }  // namespace kivi
 
-static kivi_status queue_before_append(kivi_cache* c, cudaStream_t st, bool* wrote) {
+static kivi_status queue_before_append(kivi_cache* c, cudaStream_t st, bool pop, bool* wrote) {
     const kivi::Geometry& g = c->geo;
     *wrote = false;
     const long long L = c->n_quant + c->n_resid;
@@ -470,7 +474,7 @@ static kivi_status queue_before_append(kivi_cache* c, cudaStream_t st, bool* wro
         c->n_resid = 0;
         *wrote = true;
     }
-    if (L >= g.R) {
+    if (pop && L >= g.R) {
         const cudaError_t e = kivi::launch_pop_values(g, c->buf, L - g.R, st);
         if (e != cudaSuccess) return cuda_fail(e, "value queue launch");
         g_launches++;

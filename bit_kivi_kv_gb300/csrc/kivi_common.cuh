@@ -59,19 +59,47 @@ struct PairPlace {
 // Position of token t (0..15) of a tile inside a row of its value entry tile.
 __host__ __device__ constexpr int entry_pos(int t) { return 4 * ((t & 7) >> 1) + 2 * (t >> 3) + (t & 1); }
 
+// ---- the quantization arithmetic written out at the top of kivi.h, shared
+// by every kernel that writes codes ----
+
+// Step and zero of one group from its fp32 min / max (fp16 inputs, exact).
+// A -0 min or max becomes +0; every operation is a separately rounded RN op.
+__device__ __forceinline__ void group_step_zero(float mn, float mx, int L, float* s, float* z,
+                                                __half* s_out, __half* z_out) {
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), (float)L);
+    const __half s16 = __float2half_rn(s32);
+    const __half z16 = __float2half_rn(mn);
+    *s = __half2float(s16);
+    *z = __half2float(z16);
+    *s_out = s16;
+    *z_out = z16;
+}
+
+// Nearest level of the stored grid: clamp(rint((x - z) / s), 0, L); 0 when s == 0.
+__device__ __forceinline__ uint32_t nearest_code(float x, float s, float z, int L) {
+    if (s == 0.0f) return 0u;
+    const int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, z), s));
+    return (uint32_t)min(max(c, 0), L);
+}
+
 // Balanced partition of a decode call's work over the warps of the
 // tensor-core kernel (the map's workers; a CTA's warps work independently).
 // Per (batch, kv-head) slot the work is a row of units: P quantized tile pairs
-// (32 tokens) of weight wq, then PR fp16 residual pairs (32 rows) of weight wr
-// (weights proportional to the bytes each reads), after a lead-in of weight S0
-// that stands for the fixed cost a worker pays per slot it works on (query
-// setup, ring fill, partial write): the worker whose range takes in a slot's
-// start is given that much less of the units.  Slots follow each other; worker
-// c covers weight positions [c*Wt/n, (c+1)*Wt/n) and owns the units that start
-// there.  n <= Wt / max(wq, wr) guarantees that every worker between the first
-// and the last unit of a slot owns one of them.
+// (32 tokens) of weight wq, the last M of them of weight wq + wx (value queue:
+// pairs that also read their queued values as fp16 rows), then PR fp16
+// residual pairs (32 rows) of weight wr (weights proportional to the bytes each
+// reads), after a lead-in of weight S0 that stands for the fixed cost a worker
+// pays per slot it works on (query setup, ring fill, partial write): the
+// worker whose range takes in a slot's start is given that much less of the
+// units.  Slots follow each other; worker c covers weight positions
+// [c*Wt/n, (c+1)*Wt/n) and owns the units that start there.  A worker whose
+// range lies inside a slot without holding a unit start writes an empty
+// partial for it.
 struct WorkMap {
     long long P, PR, wq, wr, Ws, Wt, n, S0;
+    long long M = 0, wx = 0;   // dense calls: the slots' mixed pairs and their extra weight
 };
 // The lead-in in quantized pairs, used when the call's shortest slot is shorter
 // than a worker's share (with ~16 warps per SM), so that workers cover several
@@ -81,24 +109,35 @@ __host__ inline long long segment_lead(long long wq, long long ws_min, long long
     const long long n_est = 16LL * (num_sms > 0 ? num_sms : 1);
     return ws_min * n_est < wt ? kSegmentLeadPairs * wq : 0;
 }
-// unit u of a slot of P quantized pairs (slots of ragged sequences differ)
-__host__ __device__ inline long long unit_start_p(long long P, long long wq, long long wr, long long S0,
-                                                  long long u) {
-    return S0 + (u < P ? u * wq : P * wq + (u - P) * wr);
+// weight of a slot's units (without the lead-in): P quantized pairs, the last M
+// of them mixed, and PR residual pairs
+__host__ __device__ inline long long slot_weight(const WorkMap& m, long long P, long long M, long long PR) {
+    return P * m.wq + M * m.wx + PR * m.wr;
+}
+// unit u of a slot of P quantized pairs, the last M of them mixed (slots of
+// ragged sequences differ; they have no mixed pairs)
+__host__ __device__ inline long long unit_start_p(const WorkMap& m, long long P, long long M, long long u) {
+    const long long Q = P - M, wm = m.wq + m.wx;
+    if (u <= Q) return m.S0 + u * m.wq;
+    if (u <= P) return m.S0 + Q * m.wq + (u - Q) * wm;
+    return m.S0 + Q * m.wq + M * wm + (u - P) * m.wr;
 }
 // first unit of a slot starting at or after weight offset y (0 <= y <= Ws); P + PR if none
-__host__ __device__ inline long long first_unit_at_p(long long P, long long wq, long long wr, long long S0,
-                                                     long long y) {
-    y -= S0;
+__host__ __device__ inline long long first_unit_at_p(const WorkMap& m, long long P, long long M, long long y) {
+    y -= m.S0;
     if (y <= 0) return 0;
-    if (y <= P * wq) return (y + wq - 1) / wq;
-    return P + (y - P * wq + wr - 1) / wr;
+    const long long Q = P - M, wm = m.wq + m.wx;
+    if (y <= Q * m.wq) return (y + m.wq - 1) / m.wq;
+    y -= Q * m.wq;
+    if (y <= M * wm) return Q + (y + wm - 1) / wm;
+    y -= M * wm;
+    return P + (y + m.wr - 1) / m.wr;
 }
 __host__ __device__ inline long long unit_start(const WorkMap& m, long long u) {
-    return unit_start_p(m.P, m.wq, m.wr, m.S0, u);
+    return unit_start_p(m, m.P, m.M, u);
 }
 __host__ __device__ inline long long first_unit_at(const WorkMap& m, long long y) {
-    return first_unit_at_p(m.P, m.wq, m.wr, m.S0, y);
+    return first_unit_at_p(m, m.P, m.M, y);
 }
 __host__ __device__ inline long long map_begin(const WorkMap& m, long long c) { return c * m.Wt / m.n; }
 // the worker whose range holds weight position x
@@ -165,6 +204,10 @@ struct FusedAppend {
     // value queue (tensor-core kernel only): >= 0 selects it; values of slot
     // positions below lqv are quantized, the rest sit in the residual ring
     long long lqv = -1;
+    // value queue with a fused append: slot position pop (== lqv - 1) leaves
+    // the queue in this call (the kernel quantizes its value into its block,
+    // and the appended value takes its ring row); -1: no pop
+    long long pop = -1;
     // failure-detection test hook (kivi_cache_set_fault): bytes the first ring
     // stage of CTA 0, warp 0 waits for beyond its copies
     int stall_bytes = 0;

@@ -379,7 +379,7 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
     long long wt0 = 0, ws_min = -1;
     for (int i = 0; i < n; ++i) {
         if (seqs[i].P + seqs[i].n_resid <= 0) return cudaErrorInvalidValue;   // a sequence without tokens
-        const long long w = seqs[i].P * wm.wq + (long long)((seqs[i].n_resid + 31) / 32) * wm.wr;
+        const long long w = slot_weight(wm, seqs[i].P, 0, (seqs[i].n_resid + 31) / 32);
         wt0 += g.Hkv * w;
         if (ws_min < 0 || w < ws_min) ws_min = w;
     }
@@ -388,7 +388,7 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
     long long start = 0, ws_max = 0;
     for (int i = 0; i < n; ++i) {
         PagedSeq s = seqs[i];
-        const long long Ws = wm.S0 + s.P * wm.wq + (long long)((s.n_resid + 31) / 32) * wm.wr;
+        const long long Ws = wm.S0 + slot_weight(wm, s.P, 0, (s.n_resid + 31) / 32);
         s.start = start;
         start += g.Hkv * Ws;
         if (Ws > ws_max) ws_max = Ws;
@@ -438,14 +438,21 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         wm.PR = (n_resid + 31) / 32;
         wm.wq = (long long)g.D * g.bits / 4 + 8LL * g.D / g.G;   // bytes of a quantized pair / 32
         wm.wr = 4LL * g.D;                                        // bytes of a residual pair / 32
-        const long long ws0 = wm.P * wm.wq + wm.PR * wm.wr;
+        if (fa.lqv >= 0) {
+            // value queue: pairs from lqv / 32 on also read up to 32 fp16 value
+            // rows, 64 D bytes, weighted as 48 D bytes: measured on the 7B layer
+            // shape, the warps that read them finish last with the full weight
+            wm.M = wm.P - (fa.lqv / 32 < wm.P ? fa.lqv / 32 : wm.P);
+            wm.wx = 3LL * g.D / 2;
+        }
+        const long long ws0 = slot_weight(wm, wm.P, wm.M, wm.PR);
         wm.S0 = segment_lead(wm.wq, ws0, slots * ws0, plan.num_sms);
         wm.Ws = wm.S0 + ws0;
         wm.n = plan.max_ctas;   // 0: the launch sizes the grid
         wm.Wt = slots * wm.Ws;
         mma_detail::Args m{cache, q, workspace, g.NB, g.part_bytes, g.slot_bytes, g.tile_bytes,
                            g.k_resid_off, g.v_resid_off, g.R, g.Hq, g.Hkv, (int)n_resid, wm, scale_log2,
-                           fa.k, fa.v, fa.row, fa.early_ok, fa.lqv, fa.stall_bytes};
+                           fa.k, fa.v, fa.row, fa.early_ok, fa.lqv, fa.pop, fa.stall_bytes};
         const bool fused = fa.row >= 0, fifo = fa.lqv >= 0;
         using L = cudaError_t (*)(mma_detail::Args&, int, int, int, int, cudaStream_t);
         const L launch = g.D == 128 ? (fifo ? launch_decode_mma_d128q : fused ? launch_decode_mma_d128f

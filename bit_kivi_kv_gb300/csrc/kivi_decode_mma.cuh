@@ -62,6 +62,9 @@ struct Args {
     // value queue (kModeFifo): values of slot positions >= lqv are in the
     // residual ring (row = position % R), those below are quantized
     long long lqv = -1;
+    // value queue with a fused append: position pop (== lqv - 1) leaves the
+    // queue in this call, so it counts as quantized already; -1: none
+    long long pop = -1;
     // failure-detection test hook: the first ring stage of CTA 0, warp 0 expects
     // this many bytes more than its copies bring, so its bounded wait runs out
     int stall_bytes = 0;
@@ -232,6 +235,25 @@ __device__ __forceinline__ void tma_1d_u32(uint32_t dst, const void* src, uint32
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).  L2
+// is coherent for the whole GPU, so a prefetch may run ahead of the kernel
+// that writes the data: the later loads still see the written bytes.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// rows [first, first + n) (mod R, n <= R) of a ring of R rows of D fp16 at base
+template <int D>
+__device__ __forceinline__ void prefetch_ring_rows(const __half* base, int first, int n, int R) {
+    if (n <= 0) return;
+    const int a0 = first % R, n0 = min(n, R - a0);
+    prefetch_l2(base + (long long)a0 * D, (uint32_t)(n0 * D * 2));
+    if (n > n0) prefetch_l2(base, (uint32_t)((n - n0) * D * 2));
+}
+// 16 bytes global -> shared, asynchronous (completed by cp_async_wait_all)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -417,10 +439,99 @@ __device__ __forceinline__ void build_q_frags(const uint8_t* entries, const floa
 
 // Register budget: four CTAs per SM (128 registers a thread); at head_dim 128
 // with four query heads per kv head three, which leaves enough registers.
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 template <int D, int NQ>
 struct MinCtas {
     static constexpr int value = (D == 128 && NQ == 4) ? 3 : 4;
 };
+
+// The value queue's pop, done by one warp: quantize the value of the popped
+// token (block token tt; its fp16 row xs, a shared copy of ring row `row`)
+// per token over groups of G channels with the shared formula, write its
+// steps / zeros into its entry tile and OR its codes into its code tile
+// (placement as in kivi.h, "Code tile": channel c = 16k + g + 8(r%2) and token
+// tt%16 = 2i + 8(r/2) + half go to lane 4g + i, word PairPlace::word(k, r),
+// bit PairPlace::bit(k, r) + 16 half), keep the codes (codes[c]) and the group
+// steps / zeros (sz[j], sz[NGRP + j]) for queue_patch, then overwrite the ring
+// row with ns (a shared copy of the appended value, which takes that row).
+// Lane l handles channels [l*D/32, (l+1)*D/32).
+template <int D, int BITS, int G>
+__device__ __forceinline__ void queue_pop(uint8_t* part_v, __half* row, const __half* xs, const __half* ns, int tt,
+                                          int lane, uint8_t* codes, __half* sz) {
+    constexpr int CPL = D / 32, L = (1 << BITS) - 1, NGRP = D / G, W = D * BITS / 64;
+    constexpr int TILE = 2 * D * BITS;
+    using PP = PairPlace<BITS, true>;
+    float x[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; j += 2) {
+        const float2 v = unpack_f16x2(*reinterpret_cast<const uint32_t*>(xs + CPL * lane + j));
+        x[j] = v.x;
+        x[j + 1] = v.y;
+    }
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int j = 1; j < CPL; ++j) { mn = fminf(mn, x[j]); mx = fmaxf(mx, x[j]); }
+#pragma unroll
+    for (int o = 1; o < G / CPL; o <<= 1) {     // the lanes of one channel group
+        mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    }
+    const int c0 = CPL * lane, gr = c0 / G, tile = tt / 16, tok = tt % 16;
+    float s, z;
+    __half s16, z16;
+    group_step_zero(mn, mx, L, &s, &z, &s16, &z16);
+    if (c0 % G == 0) {
+        __half* ent = reinterpret_cast<__half*>(part_v + (G / 16) * TILE + tile * 64 * NGRP);
+        const int at = gr * 16 + entry_pos(tok);
+        ent[at] = s16;
+        ent[16 * NGRP + at] = z16;
+        sz[gr] = s16;
+        sz[NGRP + gr] = z16;
+    }
+    uint32_t* words = reinterpret_cast<uint32_t*>(part_v + tile * TILE);
+    const int r_hi = 2 * (tok / 8), ii = (tok % 8) / 2, half = tok % 2;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int c = c0 + j, k = c / 16, cc = c % 16;
+        const int r = cc / 8 + r_hi;
+        const uint32_t code = nearest_code(x[j], s, z, L);
+        codes[c] = (uint8_t)code;
+        atomicOr(&words[(4 * (cc % 8) + ii) * W + PP::word(k, r)], code << (PP::bit(k, r) + 16 * half));
+    }
+    if constexpr (D == 128)
+        *reinterpret_cast<uint2*>(row + 4 * lane) = *reinterpret_cast<const uint2*>(ns + 4 * lane);
+    else
+        *reinterpret_cast<uint32_t*>(row + 2 * lane) = *reinterpret_cast<const uint32_t*>(ns + 2 * lane);
+}
+
+// The popped token in the warp's staged copy of its tile pair (value code
+// tiles at vt, their entry tiles at ve; tp = the token's index in the pair):
+// the copy may predate the pop's writes, so its codes and entries go in here
+// too (OR and equal stores: a copy that already has them is unchanged).
+template <int D, int BITS, int G>
+__device__ __forceinline__ void queue_patch(uint8_t* vt, uint8_t* ve, int tp, int lane, const uint8_t* codes,
+                                            const __half* sz) {
+    constexpr int CPL = D / 32, NGRP = D / G, W = D * BITS / 64, TILE = 2 * D * BITS;
+    using PP = PairPlace<BITS, true>;
+    const int tile = tp / 16, tok = tp % 16;
+    uint32_t* words = reinterpret_cast<uint32_t*>(vt + tile * TILE);
+    const int r_hi = 2 * (tok / 8), ii = (tok % 8) / 2, half = tok % 2;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int c = CPL * lane + j, k = c / 16, cc = c % 16;
+        const int r = cc / 8 + r_hi;
+        atomicOr(&words[(4 * (cc % 8) + ii) * W + PP::word(k, r)], (uint32_t)codes[c] << (PP::bit(k, r) + 16 * half));
+    }
+    if (lane < NGRP) {
+        __half* ent = reinterpret_cast<__half*>(ve + tile * 64 * NGRP);
+        ent[lane * 16 + entry_pos(tok)] = sz[lane];
+        ent[16 * NGRP + lane * 16 + entry_pos(tok)] = sz[NGRP + lane];
+    }
+}
 
 // MODE kModeFused: the call appends a token (Args::new_row) the kernel reads
 // from its inputs and stores in the cache; kModePaged: blocks are addressed
@@ -438,6 +549,11 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     __shared__ uint32_t qhc_all[kWarps][NQ][D / 2], qlc_all[kWarps][NQ][D / 2];
     __shared__ __align__(16) uint32_t qfrag_all[kWarps][32 * C::QSTRIDE];
     __shared__ __align__(8) uint64_t full_bar[kWarps][C::STAGES];
+    // value queue, per warp: the popped token's fp16 row and the appended value
+    // (shared copies), its codes and group steps / zeros
+    __shared__ __align__(16) __half poprow_all[FIFO ? kWarps : 1][2][D];
+    __shared__ uint8_t popc_all[FIFO ? kWarps : 1][D];
+    __shared__ __half popsz_all[FIFO ? kWarps : 1][2 * NGRP];
     extern __shared__ __align__(128) uint8_t dyn_smem[];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -447,7 +563,10 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
 #define qlc_s (qlc_all[warp])
     uint32_t* qfrag = qfrag_all[warp];
     uint8_t* ring = dyn_smem + warp * C::STAGES * C::STAGE_BYTES;
-    float4* mixbuf = reinterpret_cast<float4*>(dyn_smem + C::DYN_SMEM) + warp * kMaxMixPairs * 32;   // FIFO only
+    // value queue: the warp's logits of its mixed pairs, kept for the second pass
+    auto mixbuf = [&](int idx) {
+        return reinterpret_cast<float4*>(dyn_smem + C::DYN_SMEM) + warp * kMaxMixPairs * 32 + idx;
+    };
     uint64_t* bars = full_bar[warp];
     for (int idx = lane; idx < 32 * C::QSTRIDE; idx += 32) qfrag[idx] = 0u;   // unused columns stay 0
     if (lane == 0) {
@@ -574,8 +693,10 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     // Every warp passes it once (its first segment, or after its loop if it
     // has none), after issuing its first copies: with early_ok those read only
     // quantized blocks, which the preceding kernel never writes (the library's
-    // last kernel on a cache copies residual rows, or is a decode); the query,
-    // the residual rows and the workspace are touched only after it.
+    // last kernel on a cache copies residual rows, or is a decode's merge,
+    // which lets this kernel launch only after that decode, a writer of blocks
+    // when it pops the value queue, has finished); the query, the residual
+    // rows and the workspace are touched only after it.
     auto dependency_point = [&]() {
         griddepcontrol_wait();
         griddepcontrol_launch_dependents();       // the merge kernel may start launching
@@ -607,6 +728,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                  idx += (long long)gridDim.x * kThreads) {
                 const long long sl = idx / (2 * CPR);
                 const int rem = (int)(idx - sl * 2 * CPR), is_v = rem >= CPR, c16 = rem % CPR;
+                // value queue with a pop: the new value takes the popped token's
+                // ring row, written by the warp that quantizes that token
+                if (FIFO && is_v && a.pop >= 0) continue;
                 const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k) + sl * D) + c16;
                 uint8_t* rows = const_cast<uint8_t*>(a.cache) + (is_v ? a.v_resid_off : a.k_resid_off);
                 // value queue: the new value goes to ring row (its slot position) % R
@@ -619,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     while (pos < pe) {
         // the slot holding weight position pos: weights [w0, w0 + Ws), P quantized
         // pairs then PR residual pairs
-        long long w0, Ws, P, PR;
+        long long w0, Ws, P, PR, M = 0;   // M: mixed pairs (value queue)
         int b, hk;               // query / output row (batch row or call sequence), kv head
         long long rslot, islot;  // residual slot; row of the fused append's inputs
         int n_res, nrow;         // residual rows; the fused append's row (-1: none)
@@ -633,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             const PagedSeq& sq = a.seqs[lo];
             P = sq.P;
             PR = (sq.n_resid + 31) / 32;
-            Ws = wm.S0 + P * wm.wq + PR * wm.wr;
+            Ws = wm.S0 + slot_weight(wm, P, 0, PR);
             hk = (int)((pos - sq.start) / Ws);
             w0 = sq.start + hk * Ws;
             b = lo;
@@ -648,6 +772,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             Ws = wm.Ws;
             P = wm.P;
             PR = wm.PR;
+            M = wm.M;
             b = (int)(slot / a.Hkv);
             hk = (int)(slot % a.Hkv);
             rslot = islot = slot;
@@ -655,9 +780,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             nrow = a.new_row;
         }
         const long long NU = P + PR;
-        const long long u0 = first_unit_at_p(P, wm.wq, wm.wr, wm.S0, pos - w0);
+        const long long u0 = first_unit_at_p(wm, P, M, pos - w0);
         if (u0 >= NU) { pos = w0 + Ws; continue; }
-        if (w0 + unit_start_p(P, wm.wq, wm.wr, wm.S0, u0) >= pe) {
+        if (w0 + unit_start_p(wm, P, M, u0) >= pe) {
             // no unit of the slot starts in this warp's range: if the range lies
             // between the slot's first and last unit starts, the slot still
             // counts this warp's partial, so write it empty (weight 0)
@@ -671,15 +796,16 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             }
             break;
         }
-        const long long u1 = first_unit_at_p(P, wm.wq, wm.wr, wm.S0, min(pe - w0, Ws));
+        const long long u1 = first_unit_at_p(wm, P, M, min(pe - w0, Ws));
         const int p0 = (int)min(u0, P), p1 = (int)min(u1, P);                  // quantized pairs
         const int r0 = (int)(max(u0, P) - P), r1 = (int)(max(u1, P) - P);      // residual pairs
         const int part = (int)(gw - map_owner(wm, w0 + wm.S0));
         // ---- this warp's run of pairs, two tiles per ring stage ----
         const int wb = p0, we = p1;
         const int npairs = status ? 0 : we - wb;   // after a failed copy: no more copies
-        // value queue: this warp's pairs from mix0 on have quantized keys and queued values
-        const int mix0 = FIFO ? max(wb, (int)(a.lqv / 32)) : 0;
+        // value queue: this warp's pairs from mix_first() on have quantized keys
+        // and queued values (recomputed where used, not held across the loop)
+        auto mix_first = [&]() { return max(wb, (int)(a.lqv >> 5)); };
         auto need_ksz = [&](int pr) { return pr == wb || ((2 * pr) % C::TPB) == 0; };
         // the preceding kernel wrote blocks (and, paged, block-table entries): wait
         // before the first copy and before the first table read
@@ -741,10 +867,41 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         };
         if (lane == 0) {
             for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
+            // the fp16 rows this segment reads with plain loads, into L2 ahead
+            // of them: its residual pairs' key and value rows (value queue:
+            // ring rows) and, with the value queue, the queued values of its
+            // mixed pairs and the popped token's row
+            const __half* kr0 = reinterpret_cast<const __half*>(a.cache + a.k_resid_off) + rslot * a.R * D;
+            const __half* vr0 = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + rslot * a.R * D;
+            const int nr = min(32 * r1, n_res) - 32 * r0;
+            if (nr > 0) {
+                prefetch_l2(kr0 + 32LL * r0 * D, (uint32_t)(nr * D * 2));
+                if constexpr (FIFO) prefetch_ring_rows<D>(vr0, (int)(32 * P) + 32 * r0, nr, a.R);
+                else prefetch_l2(vr0 + 32LL * r0 * D, (uint32_t)(nr * D * 2));
+            }
+            if constexpr (FIFO) {
+                const int tlo = (int)max(a.lqv, 32LL * mix_first()), thi = 32 * we;
+                prefetch_ring_rows<D>(vr0, tlo, thi - tlo, a.R);
+                if (a.pop >= 0 && wb <= a.pop / 32 && a.pop / 32 < we) prefetch_ring_rows<D>(vr0, (int)a.pop, 1, a.R);
+            }
         }
         if (first_seg) {
             first_seg = false;
             dependency_point();
+        }
+        // value queue: the warp owning the pair of position a.pop quantizes that
+        // value into its block when its pair loop reaches that pair (the ring
+        // row then takes the appended value); both rows are on their way to
+        // shared memory from here on
+        const int tpop = FIFO && a.pop >= 0 && wb <= a.pop / 32 && a.pop / 32 < we ? (int)(a.pop / 32) : -1;
+        if constexpr (FIFO) {
+            constexpr int CPR = D * 2 / 16;          // 16-byte chunks per row
+            if (tpop >= 0 && lane < 2 * CPR) {
+                const __half* src = lane < CPR ? reinterpret_cast<const __half*>(a.cache + a.v_resid_off) +
+                                                     (rslot * a.R + (int)a.pop % a.R) * D
+                                               : a.new_v + islot * D;
+                cp_async16(&poprow_all[warp][lane / CPR][8 * (lane % CPR)], src + 8 * (lane % CPR));
+            }
         }
         __syncwarp();
         for (int idx = lane; idx < NQ * D / 2; idx += 32) {
@@ -762,6 +919,18 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             qhc_s[j][cp] = hic;
             qlc_s[j][cp] = pack_f16x2(y0 - hcf.x, y1 - hcf.y);
         }
+        if constexpr (FIFO) {
+            if (tpop >= 0) {
+                // the pop (this pair's staged copy gets its codes in the pair loop)
+                cp_async_wait_all();
+                __syncwarp();
+                uint8_t* part_v = const_cast<uint8_t*>(a.cache) + rslot * a.slot_bytes + (a.NB + a.pop / G) * a.part_bytes;
+                __half* row = reinterpret_cast<__half*>(const_cast<uint8_t*>(a.cache) + a.v_resid_off) +
+                              (rslot * a.R + (int)a.pop % a.R) * D;
+                queue_pop<D, BITS, G>(part_v, row, poprow_all[warp][0], poprow_all[warp][1], (int)(a.pop % G), lane,
+                                      popc_all[warp], popsz_all[warp]);
+            }
+        }
         __syncwarp();
 
         m = -INFINITY; l = 0.f;
@@ -772,13 +941,33 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         for (int f = 0; f < NBF; ++f) zeta[f] = 0.f;
 
         int k = 0;
-        for (; k < npairs; ++k) {
+        // The pair loop, in two runs for the value queue: pairs from kq on (the
+        // mixed pairs and the popped token's pair) take the queue's steps, the
+        // pairs before them the plain body, so that the common case carries none
+        // of the queue's branches.
+        int kq = npairs;
+        if constexpr (FIFO) {
+            int first = (int)(a.lqv >> 5);                 // the first pair with queued values
+            if (tpop >= 0 && tpop < first) first = tpop;
+            kq = min(max(first - wb, 0), npairs);
+        }
+        auto pair_run = [&](auto queue_steps, int kend) {
+        constexpr bool QS = decltype(queue_steps)::value;
+        for (; k < kend; ++k) {
             const uint32_t it = item + k;
             const int st = (int)(it % C::STAGES);
             if (!__all_sync(kFull, mbar_wait(&bars[st], (it / C::STAGES) & 1u))) break;
             const uint8_t* stage = ring + st * C::STAGE_BYTES;
             const uint32_t stage_u32 = ring_u32 + st * C::STAGE_BYTES;
             const int pr = wb + k;
+            if constexpr (FIFO && QS) {
+                if (a.pop >= 0 && pr == (int)(a.pop >> 5)) {   // only the popping warp has this pair
+                    // the popped token's codes into this pair's staged copy
+                    queue_patch<D, BITS, G>(const_cast<uint8_t*>(stage) + C::VT, const_cast<uint8_t*>(stage) + C::VE,
+                                            (int)(a.pop % 32), lane, popc_all[warp], popsz_all[warp]);
+                    __syncwarp();
+                }
+            }
             if (need_ksz(pr))
                 build_q_frags<C, D, NQ>(stage + C::KE, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);
             // keys: logits of tokens g, g+8 of both tiles for head i
@@ -837,12 +1026,12 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 sc[3] = cb[2] + (cb[3] + beta);
             }
             bool live = true;                          // the pair has a token to count in this pass
-            if constexpr (FIFO) {
+            if constexpr (FIFO && QS) {
                 const long long t0 = 32LL * pr;
                 if (t0 + 32 > a.lqv) {
                     // keys quantized, some values still in the queue: keep the logits
                     // for the second pass; here only the value-quantized tokens count
-                    mixbuf[(pr - mix0) * 32 + lane] = make_float4(sc[0], sc[1], sc[2], sc[3]);
+                    *mixbuf((pr - mix_first()) * 32 + lane) = make_float4(sc[0], sc[1], sc[2], sc[3]);
                     if (t0 + g >= a.lqv) sc[0] = -INFINITY;
                     if (t0 + g + 8 >= a.lqv) sc[1] = -INFINITY;
                     if (t0 + 16 + g >= a.lqv) sc[2] = -INFINITY;
@@ -897,6 +1086,11 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 issue_next(it + C::STAGES);
             }
         }
+        };
+        pair_run(BoolTag<false>{}, kq);
+        if constexpr (FIFO) {
+            if (k == kq) pair_run(BoolTag<true>{}, npairs);
+        }
         if (k < npairs) {
             // a copy timed out: flag it, wait (bounded) for this warp's copies in
             // flight, and issue no more copies in this kernel
@@ -919,8 +1113,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             // logits kept in the first pass and the values from the ring's fp16 rows ----
             const int me = wb + k;                    // pairs this warp processed
             const __half* ring_v = reinterpret_cast<const __half*>(a.cache + a.v_resid_off) + rslot * a.R * D;
+            const int mix0 = mix_first();
             for (int pr = mix0; pr < me; ++pr) {
-                const float4 s4 = mixbuf[(pr - mix0) * 32 + lane];
+                const float4 s4 = *mixbuf((pr - mix0) * 32 + lane);
                 float sc[4] = {s4.x, s4.y, s4.z, s4.w};
                 const long long t0 = 32LL * pr;       // the first pass counted the tokens below lqv
                 if (t0 + g < a.lqv) sc[0] = -INFINITY;
@@ -938,8 +1133,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     const uint32_t pb0 = lo_col ? pl01 : ph01, pb1 = lo_col ? pl89 : ph89;
                     // rows g, g+8 of the 16 tokens: queued values sit at ring row token % R
                     const long long tg = t0 + 16 * t + g, tg8 = tg + 8;
-                    const __half* vg = ring_v + (tg % a.R) * D;
-                    const __half* vg8 = ring_v + (tg8 % a.R) * D;
+                    const __half* vg = ring_v + (long long)((int)tg % a.R) * D;
+                    const __half* vg8 = ring_v + (long long)((int)tg8 % a.R) * D;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
                         uint32_t af[4];
@@ -961,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             };
             auto vrow = [&](int rr) {
                 if constexpr (FIFO)   // residual row rr is slot position 32P + rr: ring row (32P + rr) % R
-                    return rr == nrow ? a.new_v + islot * D : vr + ((32 * P + rr) % a.R) * D;
+                    return rr == nrow ? a.new_v + islot * D : vr + (long long)(((int)(32 * P) + rr) % a.R) * D;
                 return FUSED && rr == nrow ? a.new_v + islot * D : vr + (long long)rr * D;
             };
             build_q_frags<C, D, NQ>(nullptr, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
@@ -1046,7 +1241,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             pw[1] = lt;
             pw[2] = (float)st_all;
         }
-        pos = u1 >= NU ? w0 + Ws : w0 + unit_start_p(P, wm.wq, wm.wr, wm.S0, u1);
+        pos = u1 >= NU ? w0 + Ws : w0 + unit_start_p(wm, P, M, u1);
     }
     if (first_seg) dependency_point();   // a warp without a segment still stores its share of the rows
 }
@@ -1162,8 +1357,8 @@ __global__ void __launch_bounds__(kMergeThreads) finish_paged_kernel(const __gri
     const int i = (int)(bh / a.Hq), hk = (int)((bh % a.Hq) / a.nq);
     const PagedSeq& sq = a.seqs[i];
     const long long P = sq.P, PR = (sq.n_resid + 31) / 32;
-    const long long w0 = sq.start + hk * (a.wm.S0 + P * a.wm.wq + PR * a.wm.wr);
-    const long long last = w0 + unit_start_p(P, a.wm.wq, a.wm.wr, a.wm.S0, P + PR - 1);
+    const long long w0 = sq.start + hk * (a.wm.S0 + slot_weight(a.wm, P, 0, PR));
+    const long long last = w0 + unit_start_p(a.wm, P, 0, P + PR - 1);
     const int nparts = (int)(map_owner(a.wm, last) - map_owner(a.wm, w0 + a.wm.S0) + 1);
     merge_head<D>(a.ws + bh * kPartialSlots * partial_stride(D), nparts, a.out + bh * D);
 }

@@ -13,28 +13,6 @@ namespace {
 
 constexpr int kQuantThreads = 128;
 
-// Step and zero of one group from its fp32 min / max (fp16 inputs, exact).
-// A -0 min or max becomes +0; every operation is a separately rounded RN op.
-__device__ __forceinline__ void group_step_zero(float mn, float mx, int L, float* s, float* z,
-                                                __half* s_out, __half* z_out) {
-    mn = __fadd_rn(mn, 0.0f);
-    mx = __fadd_rn(mx, 0.0f);
-    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), (float)L);
-    const __half s16 = __float2half_rn(s32);
-    const __half z16 = __float2half_rn(mn);
-    *s = __half2float(s16);
-    *z = __half2float(z16);
-    *s_out = s16;
-    *z_out = z16;
-}
-
-// Nearest level of the stored grid: clamp(rint((x - z) / s), 0, L); 0 when s == 0.
-__device__ __forceinline__ uint32_t nearest_code(float x, float s, float z, int L) {
-    if (s == 0.0f) return 0u;
-    const int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, z), s));
-    return (uint32_t)min(max(c, 0), L);
-}
-
 // The same code as nearest_code with the division done as a multiply by
 // r = rn(1/s) plus one FMA correction, which lands within 1.5 ulp of the IEEE
 // quotient rn((x - z) / s).  Rounding to the nearest level can then differ

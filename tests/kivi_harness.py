@@ -5,6 +5,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+from bit_kivi_kv_gb300.kivi import kivi_cache_set_max_ctas
 from bit_kivi_kv_gb300.synth import RANGE_2_6_X10_50, SynthKV
 from guards import GuardedCache
 from oracle import layout
@@ -16,10 +17,12 @@ RTOL_L2 = 1e-3   # ||out - oracle||_2 / ||oracle||_2
 
 
 def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RANGE_2_6_X10_50,
-            sink=True, max_tokens=None, prompt=None, decode_kernel=0, fused=False, vqueue=False):
+            sink=True, max_tokens=None, prompt=None, decode_kernel=0, fused=False, vqueue=False,
+            max_ctas=0):
     """Prefill L tokens, then n_app x append (decoding at the steps in decode_at;
-    with fused, those steps append and decode in one kivi_append_decode call;
-    with vqueue, the cache keeps its value residual as a queue).
+    with fused, those steps append and decode in one kivi_append_decode call,
+    fused may also be the set of steps that do; with vqueue, the cache keeps
+    its value residual as a queue; max_ctas caps the decode grid).
 
     The cache buffer, the workspace and every output sit between guard bands,
     checked after every call.
@@ -29,6 +32,8 @@ def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RA
     K, V = prompt if prompt is not None else syn.prompt(L)
     cache = GuardedCache(B, Hq, Hkv, D, bits, G, R, max_tokens or max(L + n_app, 1))
     cache.set_decode_kernel(decode_kernel)
+    if max_ctas:
+        kivi_cache_set_max_ctas(cache.handle, max_ctas)
     if vqueue:
         cache.set_value_residual(1)
     cache.prefill(K, V)
@@ -37,7 +42,8 @@ def run_gpu(B, Hq, Hkv, D, bits, G, R, L, n_app, seed, decode_at=(), outliers=RA
     for s in range(n_app):
         q, k, v = syn.step(s)
         steps.append((q, k, v))
-        if fused and s in decode_at:
+        fuse = (s in fused) if isinstance(fused, (set, frozenset)) else fused
+        if fuse and s in decode_at:
             out = cache.bands.like(q)
             outs[s] = cache.append_decode(k, v, q, out=out).cpu()
             cache.bands.check(f"after the fused call of step {s}")

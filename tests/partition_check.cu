@@ -1,6 +1,7 @@
 // Host-only check of the decode partition (the work map in kivi_common.cuh),
 // built and run by tests/test_partition.py.  For random dense and ragged calls
-// it walks every worker's (warp's) weight range the way the decode kernel does
+// (dense ones with mixed pairs, as a value-queue cache has) it walks every
+// worker's (warp's) weight range the way the decode kernel does
 // and checks that every unit (tile pair or residual pair) of every slot is
 // owned by exactly one worker, that a slot's partial indices (workers with
 // units, and workers inside the slot without a unit start, which write an
@@ -17,7 +18,7 @@ using namespace kivi;
 namespace {
 
 struct Slot {
-    long long P, PR, w0, Ws;
+    long long P, PR, w0, Ws, M = 0;   // M: mixed pairs (the last M of the P)
 };
 
 // the worker-count rule of the launch: resident warps (4 a CTA), or the
@@ -45,26 +46,26 @@ bool check(const std::vector<Slot>& slots, const WorkMap& wm, int trial) {
             while (si > 0 && slots[si].w0 > pos) --si;
             const Slot& sl = slots[si];
             const long long NU = sl.P + sl.PR;
-            const long long u0 = first_unit_at_p(sl.P, wm.wq, wm.wr, wm.S0, pos - sl.w0);
+            const long long u0 = first_unit_at_p(wm, sl.P, sl.M, pos - sl.w0);
             if (u0 >= NU) { pos = sl.w0 + sl.Ws; continue; }
-            if (sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, u0) >= pe) {
+            if (sl.w0 + unit_start_p(wm, sl.P, sl.M, u0) >= pe) {
                 // no unit start in the range: inside the slot, an empty partial
                 if (u0 > 0) empty[si].push_back((int)(c - map_owner(wm, sl.w0 + wm.S0)));
                 break;
             }
-            const long long u1 = first_unit_at_p(sl.P, wm.wq, wm.wr, wm.S0, pe - sl.w0 < sl.Ws ? pe - sl.w0 : sl.Ws);
+            const long long u1 = first_unit_at_p(wm, sl.P, sl.M, pe - sl.w0 < sl.Ws ? pe - sl.w0 : sl.Ws);
             const long long p = c - map_owner(wm, sl.w0 + wm.S0);
             for (long long u = u0; u < u1; ++u) {
                 if (owner[si][(size_t)u] != -1) { std::printf("trial %d: unit owned twice\n", trial); return false; }
                 owner[si][(size_t)u] = (int)c;
                 part[si][(size_t)u] = (int)p;
             }
-            pos = u1 >= NU ? sl.w0 + sl.Ws : sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, u1);
+            pos = u1 >= NU ? sl.w0 + sl.Ws : sl.w0 + unit_start_p(wm, sl.P, sl.M, u1);
         }
     }
     for (size_t s = 0; s < slots.size(); ++s) {
         const Slot& sl = slots[s];
-        const long long last = sl.w0 + unit_start_p(sl.P, wm.wq, wm.wr, wm.S0, sl.P + sl.PR - 1);
+        const long long last = sl.w0 + unit_start_p(wm, sl.P, sl.M, sl.P + sl.PR - 1);
         const long long nparts = map_owner(wm, last) - map_owner(wm, sl.w0 + wm.S0) + 1;
         if (nparts < 1 || nparts > kPartialSlots) { std::printf("trial %d: %lld parts\n", trial, nparts); return false; }
         std::vector<int> seen((size_t)nparts, 0);
@@ -88,7 +89,7 @@ bool check(const std::vector<Slot>& slots, const WorkMap& wm, int trial) {
 int main() {
     std::mt19937_64 rng(12345);
     auto pick = [&](long long lo, long long hi) { return lo + (long long)(rng() % (unsigned long long)(hi - lo + 1)); };
-    const long long wqs[] = {40, 64, 96, 136, 288}, wrs[] = {256, 512};
+    const long long wqs[] = {40, 64, 96, 136, 288}, wrs[] = {256, 512}, wxs[] = {1, 128, 256};
     for (int trial = 0; trial < 4000; ++trial) {
         WorkMap wm{};
         wm.wq = wqs[pick(0, 4)];
@@ -98,19 +99,24 @@ int main() {
         std::vector<Slot> slots((size_t)nslots);
         long long start = 0, ws_min = -1, ws_max = 0;
         const long long P0 = pick(0, 400), PR0 = pick(P0 == 0 ? 1 : 0, 4);
+        // dense calls of a value-queue cache: the last M0 (<= 4) pairs are mixed
+        const long long M0 = ragged || trial % 3 == 0 ? 0 : pick(0, P0 < 4 ? P0 : 4);
+        wm.M = M0;
+        wm.wx = M0 ? wxs[pick(0, 2)] : 0;
         for (auto& s : slots) {
             s.P = ragged ? pick(0, 400) : P0;
             s.PR = ragged ? pick(s.P == 0 ? 1 : 0, 4) : PR0;
-            const long long w = s.P * wm.wq + s.PR * wm.wr;
+            s.M = M0;
+            const long long w = slot_weight(wm, s.P, s.M, s.PR);
             if (ws_min < 0 || w < ws_min) ws_min = w;
         }
         long long wt0 = 0;
-        for (auto& s : slots) wt0 += s.P * wm.wq + s.PR * wm.wr;
+        for (auto& s : slots) wt0 += slot_weight(wm, s.P, s.M, s.PR);
         const int num_sms = (int)pick(1, 152);
         wm.S0 = segment_lead(wm.wq, ws_min, wt0, num_sms);
         for (auto& s : slots) {
             s.w0 = start;
-            s.Ws = wm.S0 + s.P * wm.wq + s.PR * wm.wr;
+            s.Ws = wm.S0 + slot_weight(wm, s.P, s.M, s.PR);
             start += s.Ws;
             if (s.Ws > ws_max) ws_max = s.Ws;
         }

@@ -245,6 +245,19 @@ def test_every_value_queue_instantiation(combo):
     check_slots(run, [(0, 0), (1, 1)], steps)
 
 
+@pytest.mark.parametrize("max_ctas", [1, 5, 0])
+def test_value_queue_mixed_calls(max_ctas):
+    """Fused calls (whose decode kernel pops the oldest queued value) mixed with
+    separate appends (whose own kernel pops it) and plain decodes right after
+    a fused pop, on grids from one CTA (one warp pops for many slots) up."""
+    B, Hq, Hkv, D, bits, G, R, L, n = 3, 8, 4, 128, 2, 32, 64, 500, 90
+    steps = {s for s in range(n) if s % 5 != 4}
+    fused = {s for s in range(n) if s % 3 != 2}
+    run = run_gpu(B, Hq, Hkv, D, bits, G, R, L, n, seed=707 + max_ctas, decode_at=steps,
+                  decode_kernel=KIVI_DECODE_TENSOR_CORE, fused=fused, vqueue=True, max_ctas=max_ctas)
+    check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
+
+
 def test_value_queue_llama2_7b_layer_full_size():
     """B8 H32 D128 2-bit G32 R128, prompt 4096, 64 fused appends with the value queue."""
     steps = {0, 1, 63}
