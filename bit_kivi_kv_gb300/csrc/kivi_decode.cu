@@ -441,7 +441,7 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         if (fa.lqv >= 0) {
             // value queue: pairs from lqv / 32 on also read up to 32 fp16 value
             // rows, 64 D bytes, weighted as 48 D bytes: measured on the 7B layer
-            // shape, the warps that read them finish last with the full weight
+            // shape, with the full weight the warps that read them finish early
             wm.M = wm.P - (fa.lqv / 32 < wm.P ? fa.lqv / 32 : wm.P);
             wm.wx = 3LL * g.D / 2;
         }
