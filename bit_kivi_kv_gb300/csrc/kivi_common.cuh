@@ -266,7 +266,7 @@ cudaError_t launch_copy_rows_slots(const Geometry& g, uint8_t* cache, const __ha
 // new_k / new_v: the fused append's tokens [n][Hkv][D], or null.
 cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, const PagedSeq* seqs, int n,
                                 const __half* q, __half* out, float scale_log2, float* workspace,
-                                const __half* new_k, const __half* new_v, int early_ok, int num_sms,
+                                const __half* new_k, const __half* new_v, int early_ok, int num_sms, int max_ctas,
                                 cudaStream_t st, int* launches);
 
 // Host-side helpers of the C ABI (kivi_api.cu): set the calling thread's

@@ -367,7 +367,7 @@ cudaError_t launch_finish(K kernel, const A& f, long long ctas, cudaStream_t st)
 
 cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, const PagedSeq* seqs, int n,
                                 const __half* q, __half* out, float scale_log2, float* workspace,
-                                const __half* new_k, const __half* new_v, int early_ok, int num_sms,
+                                const __half* new_k, const __half* new_v, int early_ok, int num_sms, int max_ctas,
                                 cudaStream_t st, int* launches) {
     const Geometry& g = pg.g;
     *launches = 0;
@@ -396,6 +396,7 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
     }
     wm.Ws = ws_max;
     wm.Wt = start;
+    wm.n = max_ctas;   // 0: the launch sizes the grid
     static_cast<mma_detail::Args&>(m) =
         mma_detail::Args{buf, q, workspace, g.NB, g.part_bytes, 0, g.tile_bytes, g.k_resid_off, g.v_resid_off,
                          g.R, g.Hq, g.Hkv, 0, wm, scale_log2, new_k, new_v, -1, early_ok};

@@ -84,6 +84,30 @@ constexpr int kModePlain = 0, kModeFused = 1, kModePaged = 2, kModeFifo = 3;
 // value queue: tile pairs with quantized keys but queued values, per warp at
 // most R / 32 (R <= 128); their logits wait in shared memory for the second pass
 constexpr int kMaxMixPairs = 4;
+// paged: a warp's block-table entries turned into block offsets, kept per segment
+constexpr int kPageCache = 128;
+struct PageCache {
+    long long off[kPageCache];   // byte offset of block (first + j)'s key part
+    const int* trow;             // the sequence's block-table row
+    long long hoff;              // byte offset of the kv head's block in a page
+    int first;                   // block of off[0]
+    int last;                    // the segment's last block
+    int bad;                     // an entry was outside the pool (read as page 0)
+};
+// Fill a warp's page cache with blocks [first, first + n) of table row trow
+// (n <= kPageCache); entries outside the pool become page 0 and set bad.
+// Called by all lanes (lane_step 32) or by one lane alone (lane_step 1).
+__device__ __forceinline__ void fill_pages(PageCache& pc, const int* trow, int first, int n, int max_blocks,
+                                           int n_pages, long long pstride, long long hoff, int lane0, int lane_step) {
+    bool bad = false;
+    for (int j = lane0; j < n; j += lane_step) {
+        const int pg = __ldg(trow + min(first + j, max_blocks - 1));
+        const bool ok = (unsigned)pg < (unsigned)n_pages;
+        bad |= !ok;
+        pc.off[j] = (long long)(ok ? pg : 0) * pstride + hoff;
+    }
+    if (bad) pc.bad = 1;
+}
 constexpr int kMixBytes = kWarps * kMaxMixPairs * 32 * 16;
 
 // Paged call: cache = the page pool (and the buffer holding residual rows and
@@ -549,6 +573,10 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     __shared__ uint32_t qhc_all[kWarps][NQ][D / 2], qlc_all[kWarps][NQ][D / 2];
     __shared__ __align__(16) uint32_t qfrag_all[kWarps][32 * C::QSTRIDE];
     __shared__ __align__(8) uint64_t full_bar[kWarps][C::STAGES];
+    // paged, per warp: the segment's block-table entries as byte offsets of the
+    // blocks' key parts (refilled past kPageCache blocks) and the sticky flag
+    // of an entry outside the pool
+    __shared__ PageCache pc_all[PAGED ? kWarps : 1];
     // value queue, per warp: the popped token's fp16 row and the appended value
     // (shared copies), its codes and group steps / zeros
     __shared__ __align__(16) __half poprow_all[FIFO ? kWarps : 1][2][D];
@@ -576,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         // on its first stage, so its first bounded wait runs out
         if (a.stall_bytes && blockIdx.x == 0 && warp == 0) mbar_expect_tx_only(smem_u32(&bars[0]), (uint32_t)a.stall_bytes);
         fence_mbar_init();
+        if constexpr (PAGED) pc_all[warp].bad = 0;
     }
     __syncwarp();
 
@@ -739,7 +768,6 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             }
         }
     };
-    bool bad_page = false;   // lane 0: a block-table entry was out of range (sticky)
     while (pos < pe) {
         // the slot holding weight position pos: weights [w0, w0 + Ws), P quantized
         // pairs then PR residual pairs
@@ -811,15 +839,25 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         // before the first copy and before the first table read
         if (first_seg && !a.early_ok) griddepcontrol_wait();
         // lane 0's copy cursor: key part of the block of the next pair to fetch, tile in block
-        // (paged: the block's page pg and the next block's page pgn, loaded one block ahead)
+        // (paged: the block's page pg; the segment's table entries are loaded by
+        // the whole warp up front, so no copy waits on a table load of its own)
         const uint8_t* kcur;
-        int pg = 0, pgn = 0, blk = 0;
+        int pidx = 0;            // paged: lane 0's entry of the page cache
         if constexpr (PAGED) {
             kcur = a.cache;
-            if (lane == 0 && npairs > 0) {
-                blk = (2 * wb) / C::TPB;
-                pg = __ldg(a.table + trow + blk);
-                pgn = __ldg(a.table + trow + min(blk + 1, a.max_blocks - 1));
+            if (npairs > 0) {
+                PageCache& pcw = pc_all[warp];
+                const int blk0 = (2 * wb) / C::TPB;
+                const int nb = min((2 * we - 1) / C::TPB - blk0 + 1, kPageCache);
+                const long long pstride = (long long)a.Hkv * 2 * a.part_bytes, hoff = (long long)hk * 2 * a.part_bytes;
+                fill_pages(pcw, a.table + trow, blk0, nb, a.max_blocks, a.n_pages, pstride, hoff, lane, 32);
+                if (lane == 0) {
+                    pcw.trow = a.table + trow;
+                    pcw.hoff = hoff;
+                    pcw.first = blk0;
+                    pcw.last = (2 * we - 1) / C::TPB;
+                }
+                __syncwarp();
             }
         } else {
             kcur = a.cache + rslot * a.slot_bytes + (long long)((2 * wb) / C::TPB) * a.part_bytes;
@@ -833,9 +871,16 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             const uint8_t* kp;
             if constexpr (PAGED) {
                 // an entry outside the pool is flagged and read from page 0 instead
-                const bool okp = (unsigned)pg < (unsigned)a.n_pages;
-                bad_page |= !okp;
-                kp = a.cache + ((long long)(okp ? pg : 0) * a.Hkv + hk) * 2 * a.part_bytes;
+                PageCache& pcw = pc_all[warp];
+                if (pidx == kPageCache) {
+                    // past the cached blocks (a segment longer than kPageCache blocks)
+                    // (up to the segment's last block: later table entries are not the sequence's)
+                    pcw.first += kPageCache;
+                    fill_pages(pcw, pcw.trow, pcw.first, min(pcw.last - pcw.first + 1, kPageCache),
+                               a.max_blocks, a.n_pages, (long long)a.Hkv * 2 * a.part_bytes, pcw.hoff, 0, 1);
+                    pidx = 0;
+                }
+                kp = a.cache + pcw.off[pidx];
             } else {
                 kp = kcur;
             }
@@ -857,9 +902,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             if (tcur == C::TPB) {
                 tcur = 0;
                 if constexpr (PAGED) {
-                    ++blk;
-                    pg = pgn;
-                    pgn = __ldg(a.table + trow + min(blk + 1, a.max_blocks - 1));
+                    ++pidx;
                 } else {
                     kcur += a.part_bytes;
                 }
@@ -1206,7 +1249,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         }
 
         // ---- the segment's partial result (m, l, status, o) per query head ----
-        const uint32_t st_all = (uint32_t)__reduce_or_sync(kFull, status | (PAGED && bad_page ? 2u : 0u));
+        const uint32_t st_all = (uint32_t)__reduce_or_sync(kFull, status | (PAGED && pc_all[warp].bad ? 2u : 0u));
 #pragma unroll
         for (int f = 0; f < NBF; ++f) {
             zeta[f] += __shfl_xor_sync(kFull, zeta[f], 1);

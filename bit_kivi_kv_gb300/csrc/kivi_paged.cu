@@ -90,6 +90,7 @@ struct kivi_paged {
     unsigned stamp = 0;
     int device = -1;
     int num_sms = 0;
+    int max_ctas = 0;              // decode grid cap (0: the launch sizes it)
 };
 
 namespace {
@@ -273,6 +274,13 @@ kivi_status kivi_paged_free(kivi_paged_t c, long long* free_pages, int* free_seq
     return ok();
 }
 
+kivi_status kivi_paged_set_max_ctas(kivi_paged_t c, int max_ctas) {
+    if (!c) return failf(KIVI_ERR_INVALID_ARG, "null handle");
+    if (max_ctas < 0) return failf(KIVI_ERR_INVALID_ARG, "max_ctas must be >= 0");
+    c->max_ctas = max_ctas;
+    return ok();
+}
+
 size_t kivi_paged_workspace_bytes(const kivi_paged_config* cfg, int n) {
     kivi::PagedGeometry pg;
     const char* why;
@@ -363,7 +371,7 @@ kivi_status kivi_paged_append_decode(kivi_paged_t c, const int* seqs, int n, con
     const cudaError_t e = kivi::launch_decode_paged(
         c->pg, c->buf, call.data(), n, static_cast<const __half*>(q), static_cast<__half*>(out),
         scale * 1.4426950408889634f, static_cast<float*>(workspace), static_cast<const __half*>(k),
-        static_cast<const __half*>(v), flush_pages ? 0 : 1, c->num_sms, st, &nl);
+        static_cast<const __half*>(v), flush_pages ? 0 : 1, c->num_sms, c->max_ctas, st, &nl);
     kivi::count_launches(nl);
     // the flushes were enqueued: their pages belong to the sequences whatever the decode launch did
     size_t used = 0;

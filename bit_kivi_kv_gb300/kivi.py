@@ -90,6 +90,7 @@ def _load():
         "kivi_paged_seq_pages": (I, [P, I, IP, I, IP]),
         "kivi_paged_free": (I, [P, ctypes.POINTER(LL), IP]),
         "kivi_paged_workspace_bytes": (SZ, [pcfgp, I]),
+        "kivi_paged_set_max_ctas": (I, [P, I]),
         "kivi_paged_append_decode": (I, [P, IP, I, P, P, P, P, F, P, SZ, P]),
     }
     for name, (res, args) in sigs.items():
@@ -246,6 +247,10 @@ def kivi_paged_free(h: int):
     a, b = ctypes.c_longlong(), ctypes.c_int()
     _check(lib.kivi_paged_free(h, ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def kivi_paged_set_max_ctas(h: int, max_ctas: int):
+    _check(lib.kivi_paged_set_max_ctas(h, max_ctas))
 
 
 def kivi_paged_workspace_bytes(cfg: kivi_paged_config, n: int) -> int:

@@ -410,6 +410,11 @@ kivi_status kivi_paged_seq_pages(kivi_paged_t cache, int seq, int* pages, int ca
 /* Free pages and free sequence slots. */
 kivi_status kivi_paged_free(kivi_paged_t cache, long long* free_pages, int* free_seqs);
 
+/* Cap the decode kernel's persistent grid at max_ctas CTAs for this cache's
+ * calls (0, the default: SMs x resident CTAs per SM); as
+ * kivi_cache_set_max_ctas.  Host-only; KIVI_ERR_INVALID_ARG for a negative cap. */
+kivi_status kivi_paged_set_max_ctas(kivi_paged_t cache, int max_ctas);
+
 /* Workspace bytes of a call over n sequences (n <= KIVI_PAGED_MAX_CALL_SEQS);
  * 0 if cfg or n is invalid.  Host-only. */
 size_t kivi_paged_workspace_bytes(const kivi_paged_config* cfg, int n);

@@ -155,6 +155,11 @@ def test_paged_allocator_and_checks_without_gpu(K):
     h = K.kivi_paged_create(cfg, fake, n)
     try:
         assert K.kivi_paged_free(h) == (6, 3)
+        K.kivi_paged_set_max_ctas(h, 2)
+        K.kivi_paged_set_max_ctas(h, 0)
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_paged_set_max_ctas(h, -1)
+        assert e.value.status == K.KIVI_ERR_INVALID_ARG
         # empty prompts: no launch; slots handed out 0, 1, 2
         seqs = [K.kivi_paged_add(h, 0, 0, 0, 0) for _ in range(3)]
         assert seqs == [0, 1, 2] and K.kivi_paged_free(h) == (6, 0)

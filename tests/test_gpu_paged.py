@@ -69,6 +69,21 @@ def test_every_paged_instantiation(combo):
     serve(run, [3 * G + R + 5, R // 2, G + R], 24, rng, churn_at={12}, new_lengths=[2 * G + R])
 
 
+@pytest.mark.parametrize("shape", [(128, 2, 32, 6000), (64, 4, 64, 9500)], ids=["D128b2G32", "D64b4G64"])
+def test_paged_one_cta_grid_long_segments(shape):
+    """A one-CTA grid: each warp's share of a sequence runs past the 128 block
+    offsets a warp caches per segment, so the cache is refilled mid-segment."""
+    from bit_kivi_kv_gb300.kivi import kivi_paged_set_max_ctas
+    D, bits, G, L = shape
+    nb = (L + 40) // G + 2
+    run = PagedRun(Hq=4, Hkv=2, D=D, bits=bits, G=G, R=2 * G, max_seqs=2, max_blocks=nb, n_pages=2 * nb, seed=11)
+    kivi_paged_set_max_ctas(run.cache.handle, 1)
+    a, b = run.add(L), run.add(L - 700)
+    for t in range(12):
+        run.step([a, b] if t % 2 == 0 else [b, a])
+    run.check_all()
+
+
 def test_paged_equals_dense_for_equal_lengths():
     """Sequences of equal length, listed in slot order, give the dense cache's
     outputs exactly: the weight partition and every kernel's arithmetic are the
