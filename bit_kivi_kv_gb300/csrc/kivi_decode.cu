@@ -375,7 +375,7 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
     const int nq = g.Hq / g.Hkv;
     WorkMap wm{};
     wm.wq = (long long)g.D * g.bits / 4 + 8LL * g.D / g.G;
-    wm.wr = 4LL * g.D;
+    wm.wr = 5LL * g.D / 2;   // the dense call's weights (below), so equal lengths split alike
     long long wt0 = 0, ws_min = -1;
     for (int i = 0; i < n; ++i) {
         if (seqs[i].P + seqs[i].n_resid <= 0) return cudaErrorInvalidValue;   // a sequence without tokens
@@ -438,7 +438,13 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
         wm.P = n_quant / 32;
         wm.PR = (n_resid + 31) / 32;
         wm.wq = (long long)g.D * g.bits / 4 + 8LL * g.D / g.G;   // bytes of a quantized pair / 32
-        wm.wr = 4LL * g.D;                                        // bytes of a residual pair / 32
+        // a residual pair reads 128 D bytes (weight 4 D), but its rows come
+        // through plain loads that the SM overlaps with the bulk copies of the
+        // warps beside it: weighted as 80 D bytes, measured best on the 7B
+        // layer shape (4 D: +2% per call; GQA and long context within 1%).
+        // With the value queue the warps at slot ends also hold the mixed
+        // pairs, and the full 4 D measured best.
+        wm.wr = fa.lqv >= 0 ? 4LL * g.D : 5LL * g.D / 2;
         if (fa.lqv >= 0) {
             // value queue: pairs from lqv / 32 on also read up to 32 fp16 value
             // rows, 64 D bytes, weighted as 48 D bytes: measured on the 7B layer

@@ -89,11 +89,11 @@ bool check(const std::vector<Slot>& slots, const WorkMap& wm, int trial) {
 int main() {
     std::mt19937_64 rng(12345);
     auto pick = [&](long long lo, long long hi) { return lo + (long long)(rng() % (unsigned long long)(hi - lo + 1)); };
-    const long long wqs[] = {40, 64, 96, 136, 288}, wrs[] = {256, 512}, wxs[] = {1, 128, 256};
+    const long long wqs[] = {40, 64, 96, 136, 288}, wrs[] = {160, 256, 320, 512}, wxs[] = {1, 128, 256};
     for (int trial = 0; trial < 4000; ++trial) {
         WorkMap wm{};
         wm.wq = wqs[pick(0, 4)];
-        wm.wr = wrs[pick(0, 1)];
+        wm.wr = wrs[pick(0, 3)];
         const bool ragged = trial % 2 == 1;
         const long long nslots = pick(1, trial % 7 == 0 ? 2000 : 300);
         std::vector<Slot> slots((size_t)nslots);
