@@ -77,13 +77,27 @@ __device__ __forceinline__ __half level_threshold(int c, float s, float z, int L
     return ord_half(o);
 }
 
-// Two 2-bit codes (lo and hi halves) of x against half2 thresholds: each half
-// of the result holds 0x6400 + code (the code in bits 0-1).
-__device__ __forceinline__ uint32_t codes2_from_thresholds(__half2 x, __half2 t1, __half2 t2, __half2 t3) {
-    const __half2 one024 = __half2half2(__ushort_as_half(0x6400));   // 1024: its ulp is 1
-    const __half2 c = __hadd2(__hadd2(__hge2(x, t1), __hge2(x, t2)), __hadd2(__hge2(x, t3), one024));
-    return *reinterpret_cast<const uint32_t*>(&c);
+// Two 2-bit codes (lo and hi halves) of x against half2 thresholds, OR-ed into
+// word at bit b of each half.  The code is the number of thresholds x reaches;
+// T_1 <= T_2 <= T_3, so the ones reached are a prefix: bit 1 of the code is
+// [x >= T_2] and bit 0 the parity of the three comparisons.
+__device__ __forceinline__ uint32_t place_codes2(uint32_t word, __half2 x, __half2 t1, __half2 t2, __half2 t3, int b) {
+    const uint32_t m1 = __hge2_mask(x, t1), m2 = __hge2_mask(x, t2), m3 = __hge2_mask(x, t3);
+    return word | ((m1 ^ m2 ^ m3) & (0x00010001u << b)) | (m2 & (0x00020002u << b));
 }
+
+// With 2-bit codes the bit of a word's code pair u does not depend on the
+// word's column: 8 (u / 4) + 2 (u % 4) for keys and values alike.
+__host__ __device__ constexpr int code2_bit(int u) { return 8 * (u >> 2) + 2 * (u & 3); }
+template <bool VALUES>
+constexpr bool code2_bits_hold() {
+    using PP = PairPlace<2, VALUES>;
+    for (int wl = 0; wl < 128 * 2 / 64; ++wl)
+        for (int u = 0; u < 8; ++u)
+            if (PP::bit(PP::k_of(wl, u), PP::r_of(wl, u)) != code2_bit(u)) return false;
+    return true;
+}
+static_assert(code2_bits_hold<false>() && code2_bits_hold<true>(), "2-bit code placement");
 
 struct QuantArgs {
     uint8_t* cache;
@@ -207,14 +221,13 @@ __global__ void __launch_bounds__(kQuantThreads)
         for (int wt = tid; wt < TILE_WORDS; wt += kQuantThreads) {
             const int lane = wt & 31, wl = wt >> 5;
             const int g = lane >> 2, i = lane & 3;
-            int off[PER], bit[PER];
+            int off[PER];
             __half2 t1[PER], t2[PER], t3[PER];
 #pragma unroll
             for (int u = 0; u < PER; ++u) {
                 const int k = PP::k_of(wl, u), r = PP::r_of(wl, u);
                 const int ch = 16 * k + 2 * i + 8 * (r >> 1);
                 off[u] = (g + 8 * (r & 1)) * DP + ch;
-                bit[u] = PP::bit(k, r);
                 t1[u] = *reinterpret_cast<const __half2*>(thr + ch);
                 t2[u] = *reinterpret_cast<const __half2*>(thr + D + ch);
                 t3[u] = *reinterpret_cast<const __half2*>(thr + 2 * D + ch);
@@ -224,7 +237,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
                 for (int u = 0; u < PER; ++u) {
                     const __half2 x = *reinterpret_cast<const __half2*>(xs + tt * 16 * DP + off[u]);
-                    word |= (codes2_from_thresholds(x, t1[u], t2[u], t3[u]) << bit[u]) & (0x00030003u << bit[u]);
+                    word = place_codes2(word, x, t1[u], t2[u], t3[u], code2_bit(u));
                 }
                 reinterpret_cast<uint32_t*>(part_k)[tt * TILE_WORDS + lane * W + wl] = word;
             }
@@ -308,13 +321,12 @@ __global__ void __launch_bounds__(kQuantThreads)
             const int g = lane >> 2, i = lane & 3;
             // the word's channels 16k + g (+8), k in {2wl, 2wl+1}, lie in one group of
             // G >= 32 channels; its tokens are 2i, 2i+1 (r < 2) and 2i+8, 2i+9 (r >= 2)
-            int off[PER], bit[PER];
+            int off[PER];
 #pragma unroll
             for (int u = 0; u < PER; ++u) {
                 const int k = PP::k_of(wl, u), r = PP::r_of(wl, u);
                 const int ch = 16 * k + g + 8 * (r & 1);
                 off[u] = (2 * i + 8 * (r >> 1)) * DP + ch;
-                bit[u] = PP::bit(k, r);
             }
             const int tgrp = ((16 * PP::k_of(wl, 0)) / G) * G + 2 * i;   // thresholds of (group, token 2i)
             for (int tt = 0; tt < TPB; ++tt) {
@@ -332,9 +344,8 @@ __global__ void __launch_bounds__(kQuantThreads)
                     const bool first_tokens = (u >> 2) == 0;
                     const __half* xp = xs + tt * 16 * DP + off[u];
                     const __half2 x = __halves2half2(xp[0], xp[DP]);
-                    const uint32_t c2 = first_tokens ? codes2_from_thresholds(x, a1, a2, a3)
-                                                     : codes2_from_thresholds(x, b1, b2, b3);
-                    word |= (c2 << bit[u]) & (0x00030003u << bit[u]);
+                    word = first_tokens ? place_codes2(word, x, a1, a2, a3, code2_bit(u))
+                                        : place_codes2(word, x, b1, b2, b3, code2_bit(u));
                 }
                 reinterpret_cast<uint32_t*>(part_v)[tt * TILE_WORDS + lane * W + wl] = word;
             }
