@@ -224,7 +224,9 @@ kivi_status kivi_decode_attn(kivi_cache_t cache, const void* q, void* out, float
  * ws_bytes, stream) (the method's description has them as two steps; this
  * fuses them).  With the tensor-core decode kernel the new token's residual
  * row is written by the decode kernel itself, one launch fewer than the two
- * calls; with the CUDA-core kernel selected the two calls run in sequence.
+ * calls, and with the value queue (kivi_cache_set_value_residual) the decode
+ * kernel also quantizes the value that leaves the queue, another launch
+ * fewer; with the CUDA-core kernel selected the two calls run in sequence.
  * Errors as for those two calls; every check runs before anything is
  * launched.
  */
