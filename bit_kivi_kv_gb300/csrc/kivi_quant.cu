@@ -53,28 +53,49 @@ __device__ __forceinline__ __half ord_half(int o) {
 // entries).  The probes sit next to a half-step by construction, so they take
 // the IEEE division directly.
 __device__ __forceinline__ __half level_threshold(int c, float s, float z, int L) {
-    // The real crossing is y = z + (c - 1/2) s.  For fp16 x at least delta above
-    // y, rn(rn(x - z) / s) > c - 1/2 (two roundings of relative 2^-24 each, and
-    // y's own rounding), so code(x) >= c; at least delta below, code(x) < c.  So
-    // when no fp16 value lies within delta of y, T_c is the least fp16 >= y.
+    // The real crossing is y = z + (c - 1/2) s.  rn(x - z) and rn(. / s) each
+    // move the quotient by at most 2^-24 of itself, so an fp16 x more than
+    // (c - 1/2) s 2^-23 (plus y's own rounding, |y| 2^-24) above y has
+    // code(x) >= c, and one as far below has code(x) < c; delta = (c s + |y|)
+    // 2^-22 covers that twice.  So when no fp16 value lies within delta of y,
+    // T_c is the least fp16 >= y: the least fp16 >= y - delta, when that is
+    // above y + delta (the fp32 rounding of y -/+ delta is far inside the slack).
     const float y = __fmaf_rn((float)c - 0.5f, s, z);
-    const float delta = __fmaf_rn((float)c, s, fabsf(y)) * 0x1p-20f;
-    const __half up = __float2half_ru(y);
-    const int ou = half_ord(up);
-    if (ou > -0x7BFF && ou <= 0x7BFF) {
-        const float above = __half2float(up), below = __half2float(ord_half(ou - 1));
-        if (above - y > delta && y - below > delta) return up;
-    }
+    const float delta = __fmaf_rn((float)c, s, fabsf(y)) * 0x1p-22f;
+    const __half a = __float2half_ru(y - delta);
+    if (__half2float(a) > y + delta) return a;
+    // Otherwise search, probing with the formula itself: code(x) does not
+    // decrease with x, so gallop from the fp16 nearest y to neighbours lo < hi
+    // with code(lo) < c <= code(hi), then bisect.  The finite fp16 range holds
+    // both ends (code(-65504) = 0 < c <= L = code(65504) for s > 0), and
+    // near 0, where fp16 values are far denser than the rounding band, the
+    // threshold can be hundreds of fp16 steps from y.
+    constexpr int kMin = -0x7BFF, kMax = 0x7BFF;
     auto reaches = [&](int o) { return (int)nearest_code(__half2float(ord_half(o)), s, z, L) >= c; };
-    int o = half_ord(__float2half_rn(y));
-    // the crossing is within a few fp16 steps of the estimate; the walks are bounded
-    // (o stays inside the finite range, where the formula reaches L at the group max)
+    const int o = min(max(half_ord(__float2half_rn(y)), kMin), kMax);
+    int lo, hi;
     if (reaches(o)) {
-        for (int k = 0; k < 64 && o > -0x7BFF && reaches(o - 1); ++k) --o;
+        hi = o;
+        for (int step = 1;; step *= 2) {
+            lo = max(hi - step, kMin);
+            if (!reaches(lo)) break;
+            hi = lo;
+            if (lo == kMin) return ord_half(kMin);   // (not reached for s > 0)
+        }
     } else {
-        for (int k = 0; k < 64 && o < 0x7BFF && !reaches(o); ++k) ++o;
+        lo = o;
+        for (int step = 1;; step *= 2) {
+            hi = min(lo + step, kMax);
+            if (reaches(hi)) break;
+            lo = hi;
+            if (hi == kMax) return __ushort_as_half(0x7C00);   // no finite x reaches c (not for s > 0)
+        }
     }
-    return ord_half(o);
+    while (hi - lo > 1) {
+        const int mid = lo + (hi - lo) / 2;
+        if (reaches(mid)) hi = mid; else lo = mid;
+    }
+    return ord_half(hi);
 }
 
 // Two 2-bit codes (lo and hi halves) of x against half2 thresholds, OR-ed into

@@ -104,6 +104,47 @@ def test_quantizer_near_ties(bits):
     check_slots(run, [(0, 0)], {32})
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantizer_crossings_near_zero(bits):
+    """Groups with a step of 4-120 whose zero point puts a level's crossing
+    z + (c - 1/2) s exactly at 0, where fp16 values are far denser than the
+    crossing's rounding band (the threshold lies tens to hundreds of subnormal
+    steps from 0), and whose other elements are consecutive fp16 values around
+    both candidate sides: the GPU's level thresholds must give the oracle's codes
+    bit for bit."""
+    L_b = (1 << bits) - 1
+    B, H, D, G, R, L = 1, 1, 64, 32, 32, 32 * 9
+    rng = np.random.default_rng(100 + bits)
+    def ordinal(h):
+        b = int(np.float16(h).view(np.uint16))
+        return -(b & 0x7FFF) if b & 0x8000 else b
+    def from_ordinal(o):
+        return np.uint16(o if o >= 0 else 0x8000 | -o).view(np.float16)
+    def groups(n_groups, n):
+        out = np.zeros((n_groups, n), np.float16)
+        for gi in range(n_groups):
+            c0 = int(rng.integers(1, L_b + 1))                     # the level whose crossing is at 0
+            # a step of four significant bits, so z = -(c0 - 1/2) s and the max are exact fp16
+            s16 = np.float16(2.0 ** int(rng.integers(2, 6)) * (1 + int(rng.integers(0, 8)) / 8))
+            mn = np.float16(-(c0 - 0.5) * float(s16))
+            mx = np.float16(float(mn) + L_b * float(s16))
+            assert float(mn) == -(c0 - 0.5) * float(s16) and float(mx) - float(mn) == L_b * float(s16)
+            # z + (c0 - 1/2) s is exactly 0; rn(x - z) stays at (c0 - 1/2) s for |x| under half
+            # its fp32 ulp, so the threshold is about that far from 0 (its side set by the tie rule)
+            half = float(np.spacing(np.float32((c0 - 0.5) * float(s16)))) / 2
+            ot = ordinal(np.float16(half))
+            ks = list(range(ot - 7, ot + 8)) + list(range(-ot - 7, -ot + 8))
+            v = np.array([mn, mx] + [from_ordinal(k) for k in ks], np.float16)[:n]
+            out[gi] = rng.permutation(v)
+        return out
+    K = groups((L // G) * D, G).reshape(L // G, D, G).transpose(0, 2, 1).reshape(1, 1, L, D)
+    V = groups(L * (D // G), G).reshape(1, 1, L, D)
+    K = torch.from_numpy(np.ascontiguousarray(K)).cuda()
+    V = torch.from_numpy(np.ascontiguousarray(V)).cuda()
+    run = run_gpu(B, H, H, D, bits, G, R, L, 33, seed=12, decode_at={32}, prompt=(K, V))
+    check_slots(run, [(0, 0)], {32})
+
+
 def test_degenerate_groups():
     """Constant key channels / value groups (step 0) and signed zeros: codes 0, zero +0."""
     B, H, D, G, R, L = 1, 2, 128, 32, 32, 160
