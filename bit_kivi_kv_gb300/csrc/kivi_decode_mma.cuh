@@ -933,9 +933,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             dependency_point();
         }
         // value queue: the warp owning the pair of position a.pop quantizes that
-        // value into its block when its pair loop reaches that pair (the ring
-        // row then takes the appended value); both rows are on their way to
-        // shared memory from here on
+        // value into its block after the query setup below (the ring row then
+        // takes the appended value); both rows are copied to shared memory
+        // meanwhile
         const int tpop = FIFO && a.pop >= 0 && wb <= a.pop / 32 && a.pop / 32 < we ? (int)(a.pop / 32) : -1;
         if constexpr (FIFO) {
             constexpr int CPR = D * 2 / 16;          // 16-byte chunks per row
