@@ -21,7 +21,7 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU hosts t
 from bit_kivi_kv_gb300.kivi import KIVI_DECODE_CUDA_CORE, KIVI_DECODE_TENSOR_CORE  # noqa: E402
 from bit_kivi_kv_gb300.synth import SynthKV  # noqa: E402
 from guards import GuardedCache  # noqa: E402
-from kivi_harness import check_slots  # noqa: E402
+from kivi_harness import check_slots, run_gpu  # noqa: E402
 
 TC, CC = KIVI_DECODE_TENSOR_CORE, KIVI_DECODE_CUDA_CORE
 HANDLES = [
@@ -72,3 +72,46 @@ def test_many_live_handles_interleaved():
         run["cache"].bands.check(f"handle {i} after the interleaved calls")
         run["outs"] = {s: o.cpu() for s, o in run["outs"].items()}
         check_slots(run, [(0, 0), (run["B"] - 1, run["Hkv"] - 1)], decode_at)
+
+
+def test_llama2_13b_forty_layers_full_size():
+    """The 13B configuration as a step: 40 live layer caches (B32 H40 D128, 2-bit,
+    G32, R128; ~0.5 GB each), each prefilled with its own 4096-token prompt, then
+    one fused append + decode through all 40 layers with a fresh query per layer
+    (each append flushes its layer's full residual).  Four layers, spread over
+    the stack, are checked slot by slot against the oracle; the others must give
+    finite outputs and the expected token counts."""
+    from bit_kivi_kv_gb300.kivi import KiviCache
+    B, H, D, L, n_layers = 32, 40, 128, 4096, 40
+    checked = {0, 13, 26, 39}
+    runs, outs = {}, []
+    caches = []
+    for li in range(n_layers):
+        if li in checked:
+            # a checked layer keeps its prompt and step for the oracle
+            runs[li] = run_gpu(B, H, H, D, 2, 32, 128, L, 0, seed=5000 + li, max_tokens=L + 1)
+            caches.append(runs[li]["cache"])
+            continue
+        syn = SynthKV(B, H, H, D, 5000 + li, device="cuda")
+        K, V = syn.prompt(L)
+        c = KiviCache(B, H, H, D, 2, 32, 128, L + 1)
+        c.prefill(K, V)
+        del K, V
+        caches.append(c)
+    for li, c in enumerate(caches):
+        if li in checked:
+            syn = SynthKV(B, H, H, D, 5000 + li, device="cuda")
+            q, k, v = syn.step(0)
+            runs[li]["steps"].append((q, k, v))
+            runs[li]["outs"][0] = c.append_decode(k, v, q)
+        else:
+            q, k, v = SynthKV(B, H, H, D, 9000 + li, device="cuda").step(0)
+            outs.append(c.append_decode(k, v, q))
+    torch.cuda.synchronize()
+    for c in caches:
+        assert c.counts() == (L, 1)
+    for o in outs:
+        assert torch.isfinite(o.float()).all()
+    for li, run in runs.items():
+        run["outs"] = {s: o.cpu() for s, o in run["outs"].items()}
+        check_slots(run, [(0, 0), (17, 23), (31, 39)], {0})
