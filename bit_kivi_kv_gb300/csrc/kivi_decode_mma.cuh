@@ -839,8 +839,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         // before the first copy and before the first table read
         if (first_seg && !a.early_ok) griddepcontrol_wait();
         // lane 0's copy cursor: key part of the block of the next pair to fetch, tile in block
-        // (paged: the block's page pg; the segment's table entries are loaded by
-        // the whole warp up front, so no copy waits on a table load of its own)
+        // (paged: the block's offset in the warp's page cache, which the whole
+        // warp fills from the table at the segment start, so no copy waits on a
+        // table load of its own)
         const uint8_t* kcur;
         int pidx = 0;            // paged: lane 0's entry of the page cache
         if constexpr (PAGED) {
