@@ -346,6 +346,13 @@ cudaError_t launch_decode_mma_d64p(mma_detail::PagedArgs& a, int bits, int nq, i
 
 namespace {
 
+// The merge's form: a warp per head when no slot has more partials than the
+// warp form loads in one round trip (a slot meets at most Ws * n / Wt + 2
+// workers), else a CTA per head.
+inline bool merge_by_warp(const WorkMap& wm) {
+    return (double)wm.Ws * (double)wm.n / (double)wm.Wt + 2.0 <= (double)mma_detail::kMergeAhead;
+}
+
 // Launch the merge kernel as a programmatic dependent of the decode kernel.
 template <typename K, typename A>
 cudaError_t launch_finish(K kernel, const A& f, long long ctas, cudaStream_t st) {
@@ -414,10 +421,17 @@ cudaError_t launch_decode_paged(const PagedGeometry& pg, const uint8_t* buf, con
     f.Hkv = g.Hkv;
     f.nq = nq;
     f.wm = m.wm;   // with the grid size the launch chose
+    f.heads = (long long)n * g.Hq;
     f.n_seqs = n;
     for (int i = 0; i < n; ++i) f.seqs[i] = m.seqs[i];
-    e = g.D == 128 ? launch_finish(mma_detail::finish_paged_kernel<128>, f, (long long)n * g.Hq, st)
-                   : launch_finish(mma_detail::finish_paged_kernel<64>, f, (long long)n * g.Hq, st);
+    if (merge_by_warp(m.wm)) {
+        const long long ctas = (f.heads + mma_detail::kMergeWarps - 1) / mma_detail::kMergeWarps;
+        e = g.D == 128 ? launch_finish(mma_detail::finish_paged_kernel<128, true>, f, ctas, st)
+                       : launch_finish(mma_detail::finish_paged_kernel<64, true>, f, ctas, st);
+    } else {
+        e = g.D == 128 ? launch_finish(mma_detail::finish_paged_kernel<128, false>, f, f.heads, st)
+                       : launch_finish(mma_detail::finish_paged_kernel<64, false>, f, f.heads, st);
+    }
     if (e != cudaSuccess) return e;
     *launches = 2;
     return cudaSuccess;
@@ -468,11 +482,17 @@ cudaError_t launch_decode(const Geometry& g, const uint8_t* cache, long long n_q
                                                                              : launch_decode_mma_d64);
         cudaError_t e = launch(m, g.bits, nq, g.G, plan.num_sms, st);
         if (e != cudaSuccess) return e;
-        mma_detail::FinishArgs f{workspace, out, g.Hq, g.Hkv, nq, m.wm};
-        // the merge may start while the main kernel drains; it waits for it on the GPU
         const long long heads = (long long)g.B * g.Hq;
-        e = g.D == 128 ? launch_finish(mma_detail::finish_kernel<128>, f, heads, st)
-                       : launch_finish(mma_detail::finish_kernel<64>, f, heads, st);
+        mma_detail::FinishArgs f{workspace, out, g.Hq, g.Hkv, nq, m.wm, heads};
+        // the merge may start while the main kernel drains; it waits for it on the GPU
+        if (merge_by_warp(m.wm)) {
+            const long long ctas = (heads + mma_detail::kMergeWarps - 1) / mma_detail::kMergeWarps;
+            e = g.D == 128 ? launch_finish(mma_detail::finish_kernel<128, true>, f, ctas, st)
+                           : launch_finish(mma_detail::finish_kernel<64, true>, f, ctas, st);
+        } else {
+            e = g.D == 128 ? launch_finish(mma_detail::finish_kernel<128, false>, f, heads, st)
+                           : launch_finish(mma_detail::finish_kernel<64, false>, f, heads, st);
+        }
         *launches = 2;
         return e;
     }

@@ -75,6 +75,7 @@ struct FinishArgs {
     __half* out;
     int Hq, Hkv, nq;
     WorkMap wm;
+    long long heads;   // query rows x query heads
 };
 
 // Kernel modes: plain decode; decode with a fused append; paged cache with
@@ -127,6 +128,7 @@ struct PagedFinishArgs {
     __half* out;
     int Hq, Hkv, nq;
     WorkMap wm;
+    long long heads;   // call sequences x query heads
     int n_seqs;
     PagedSeq seqs[kMaxCallSeqs];
 };
@@ -1294,17 +1296,98 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
 #undef qhc_s
 #undef qlc_s
 
-// One CTA (kMergeThreads threads) per (query row, query head): the
-// log-sum-exp merge of the head's nparts partial results -> fp16 output.  The
-// values of the partials a warp sums go out first, together with the (m, l)
-// loads; one warp turns the m's into weights 2^(m_j - M) and the sum L; warp
-// w sums partials w, w + 4, ... and the four warps' sums are added in warp
-// order (a fixed order for a given partition).  A partial whose status is set
-// (a cache copy timed out, a bad table entry) makes the head's output NaN.
+// The log-sum-exp merge of a head's nparts partial results -> fp16 output, in
+// two forms; a partial whose status is set (a cache copy timed out, a bad
+// table entry) makes the head's output NaN.
+//
+// merge_head_warp: one warp per (query row, query head), for calls whose slots
+// have at most kMergeAhead partials.  The (m, l, status) of every partial and
+// the values of the first kMergeAhead partials are loaded together, so the
+// merge is one round trip; the weights 2^(m_j - M) and the sum L come from
+// shuffles, and the values are summed in partial order.
 constexpr int kMergeThreads = 128;
-constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeWarps = kMergeThreads / 32;   // heads per merge CTA in the warp form
+constexpr int kMergeAhead = 16;
 template <int D>
-__device__ __forceinline__ void merge_head(const float* base, int nparts, __half* out) {
+__device__ __forceinline__ void merge_head_warp(const float* base, int nparts, __half* out, int lane) {
+    constexpr int S = partial_stride(D);
+    constexpr int CPL = D / 32;                   // channels per lane
+    static_assert(kPartialSlots <= 96, "partials held three to a lane");
+    auto load_v = [&](int j, float (&v)[CPL]) {
+        const float* ps = base + j * S + 4 + CPL * lane;
+        if constexpr (CPL == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(ps);
+            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2*>(ps);
+            v[0] = x.x; v[1] = x.y;
+        }
+    };
+    float v[kMergeAhead][CPL];
+#pragma unroll
+    for (int u = 0; u < kMergeAhead; ++u)
+        if (u < nparts) load_v(u, v[u]);
+    float mj[3], lj[3];
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        const int j = lane + 32 * r;
+        mj[r] = -INFINITY;
+        lj[r] = 0.f;
+        if (j < nparts) {
+            const float* ps = base + j * S;
+            mj[r] = ps[0];
+            lj[r] = ps[1];
+            bad |= ps[2] != 0.f;
+        }
+    }
+    float M = fmaxf(fmaxf(mj[0], mj[1]), mj[2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float e[3], ls = 0.f;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        // a weight of 0 (an empty partial, m = -inf) adds nothing, whatever its values hold
+        e[r] = mj[r] == -INFINITY ? 0.f : fast_exp2(mj[r] - M);
+        ls = fmaf(lj[r], e[r], ls);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
+    bad = __any_sync(kFull, bad);
+    float acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+#pragma unroll
+    for (int u = 0; u < kMergeAhead; ++u) {
+        const float eu = __shfl_sync(kFull, e[0], u);
+        if (u < nparts && eu != 0.f) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(v[u][c], eu, acc[c]);
+        }
+    }
+    for (int j = kMergeAhead; j < nparts; ++j) {  // beyond the values loaded ahead
+        const float ej = __shfl_sync(kFull, j < 32 ? e[0] : (j < 64 ? e[1] : e[2]), j & 31);
+        if (ej != 0.f) {
+            float vj[CPL];
+            load_v(j, vj);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(vj[c], ej, acc[c]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < CPL; c += 2) {
+        const __half2 h = bad ? __float2half2_rn(NAN) : __floats2half2_rn(acc[c] / ls, acc[c + 1] / ls);
+        *reinterpret_cast<__half2*>(out + CPL * lane + c) = h;
+    }
+}
+
+// merge_head_cta: one CTA (kMergeThreads threads) per head, for calls with
+// more partials per slot.  The values of the partials a warp sums go out first,
+// together with the (m, l) loads; one warp turns the m's into weights and the
+// sum L; warp w sums partials w, w + 4, ... and the four warps' sums are added
+// in warp order.
+template <int D>
+__device__ __forceinline__ void merge_head_cta(const float* base, int nparts, __half* out) {
     constexpr int S = partial_stride(D);
     constexpr int CPL = D / 32;                                 // channels per lane
     constexpr int NR = (kPartialSlots + kMergeWarps - 1) / kMergeWarps;   // partials per warp, at most
@@ -1380,31 +1463,42 @@ __device__ __forceinline__ void merge_head(const float* base, int nparts, __half
     }
 }
 
-// One CTA per (batch, query head): merge of the partials of the head's kv slot.
-template <int D>
+// Merge of the partials of each (batch, query head) of a dense call: WARP, one
+// warp per head (four to a CTA), else one CTA per head.
+template <int D, bool WARP>
 __global__ void __launch_bounds__(kMergeThreads) finish_kernel(FinishArgs a) {
     // launched as a programmatic dependent of the main kernel: wait until its
     // partial results are complete and visible
     griddepcontrol_wait();
     griddepcontrol_launch_dependents();   // the next decode call may start its prologue
-    const long long bh = blockIdx.x;
+    const long long bh = WARP ? (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5) : (long long)blockIdx.x;
+    if (bh >= a.heads) return;
     const long long slot = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.nq;
-    merge_head<D>(a.ws + bh * kPartialSlots * partial_stride(D), slot_parts(a.wm, slot), a.out + bh * D);
+    const float* base = a.ws + bh * kPartialSlots * partial_stride(D);
+    if constexpr (WARP)
+        merge_head_warp<D>(base, slot_parts(a.wm, slot), a.out + bh * D, threadIdx.x & 31);
+    else
+        merge_head_cta<D>(base, slot_parts(a.wm, slot), a.out + bh * D);
 }
 
-// The same for a paged call: one CTA per (call sequence, query head).
-template <int D>
+// The same for a paged call, per (call sequence, query head).
+template <int D, bool WARP>
 __global__ void __launch_bounds__(kMergeThreads) finish_paged_kernel(const __grid_constant__ PagedFinishArgs a) {
     griddepcontrol_wait();
     griddepcontrol_launch_dependents();
-    const long long bh = blockIdx.x;
+    const long long bh = WARP ? (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5) : (long long)blockIdx.x;
+    if (bh >= a.heads) return;
     const int i = (int)(bh / a.Hq), hk = (int)((bh % a.Hq) / a.nq);
     const PagedSeq& sq = a.seqs[i];
     const long long P = sq.P, PR = (sq.n_resid + 31) / 32;
     const long long w0 = sq.start + hk * (a.wm.S0 + slot_weight(a.wm, P, 0, PR));
     const long long last = w0 + unit_start_p(a.wm, P, 0, P + PR - 1);
     const int nparts = (int)(map_owner(a.wm, last) - map_owner(a.wm, w0 + a.wm.S0) + 1);
-    merge_head<D>(a.ws + bh * kPartialSlots * partial_stride(D), nparts, a.out + bh * D);
+    const float* base = a.ws + bh * kPartialSlots * partial_stride(D);
+    if constexpr (WARP)
+        merge_head_warp<D>(base, nparts, a.out + bh * D, threadIdx.x & 31);
+    else
+        merge_head_cta<D>(base, nparts, a.out + bh * D);
 }
 
 }  // namespace mma_detail
