@@ -1086,6 +1086,14 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 }
             }
             if (live) {
+                // small tiles (at most four words a lane): both value tiles' words
+                // are loaded before the softmax, whose shuffles then hide their latency
+                constexpr bool HOIST = BITS != 8 && W <= 4;
+                uint32_t wvh[2][W];
+                if constexpr (HOIST) {
+                    lds_words(stage_u32 + C::VT, wvh[0]);
+                    lds_words(stage_u32 + C::VT + C::TILE, wvh[1]);
+                }
                 float p[4];
                 softmax(sc, p, 0x1p24f);                   // scores are in units of 2^-24
                 // values, tile by tile
@@ -1103,7 +1111,12 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                         p_frag(prb, ph01, ph89, pl01, pl89, sv, zv, pb[f][0], pb[f][1], zeta[f]);
                     }
                     uint32_t wv[W];
-                    lds_words(stage_u32 + C::VT + t * C::TILE, wv);
+                    if constexpr (HOIST) {
+#pragma unroll
+                        for (int x = 0; x < W; ++x) wv[x] = wvh[t][x];
+                    } else {
+                        lds_words(stage_u32 + C::VT + t * C::TILE, wv);
+                    }
                     if constexpr (BITS == 8) {
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
