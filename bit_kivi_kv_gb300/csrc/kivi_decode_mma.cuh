@@ -1087,12 +1087,23 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             }
             if (live) {
                 // small tiles (at most four words a lane): both value tiles' words
-                // are loaded before the softmax, whose shuffles then hide their latency
+                // and entries are loaded before the softmax, whose shuffles then
+                // hide their latency
                 constexpr bool HOIST = BITS != 8 && W <= 4;
                 uint32_t wvh[2][W];
+                uint2 svh[2][NBF], zvh[2][NBF];
                 if constexpr (HOIST) {
                     lds_words(stage_u32 + C::VT, wvh[0]);
                     lds_words(stage_u32 + C::VT + C::TILE, wvh[1]);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t ve = stage_u32 + C::VE + t * C::ENT + eoff;
+#pragma unroll
+                        for (int f = 0; f < NBF; ++f) {
+                            svh[t][f] = lds64(ve + 32u * GB * f);
+                            zvh[t][f] = lds64(ve + 32u * (NGRP + GB * f));
+                        }
+                    }
                 }
                 float p[4];
                 softmax(sc, p, 0x1p24f);                   // scores are in units of 2^-24
@@ -1107,7 +1118,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     uint32_t pb[NBF][2];
 #pragma unroll
                     for (int f = 0; f < NBF; ++f) {
-                        const uint2 sv = lds64(ve + 32u * GB * f), zv = lds64(ve + 32u * (NGRP + GB * f));
+                        const uint2 sv = HOIST ? svh[t][f] : lds64(ve + 32u * GB * f);
+                        const uint2 zv = HOIST ? zvh[t][f] : lds64(ve + 32u * (NGRP + GB * f));
                         p_frag(prb, ph01, ph89, pl01, pl89, sv, zv, pb[f][0], pb[f][1], zeta[f]);
                     }
                     uint32_t wv[W];
