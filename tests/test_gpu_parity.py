@@ -299,6 +299,34 @@ def test_value_queue_mixed_calls(max_ctas):
     check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], steps)
 
 
+def test_value_queue_pop_survives_a_failed_copy():
+    """A fused call on a value-queue cache whose copy wait runs out (the fault
+    hook: CTA 0, warp 0): the heads of the slot that warp covers come back NaN,
+    every other head finite, and the cache is still exactly the oracle's, the
+    pops included (each slot's pop runs before its warp's pair loop), so the
+    following calls are correct."""
+    from bit_kivi_kv_gb300.kivi import KIVI_FAULT_COPY_STALL, kivi_cache_set_fault
+    from kivi_harness import check_slot_bytes, oracle_slot
+    B, Hq, Hkv, D, bits, G, R, L, n = 2, 4, 4, 128, 2, 32, 64, 600, 6
+    run = run_gpu(B, Hq, Hkv, D, bits, G, R, L, 0, seed=321, max_tokens=L + n,
+                  decode_kernel=KIVI_DECODE_TENSOR_CORE, vqueue=True)
+    cache, syn = run["cache"], SynthKV(B, Hq, Hkv, D, 321, device="cuda")
+    for s in range(n):
+        q, k, v = syn.step(s)
+        run["steps"].append((q, k, v))
+        if s == 2:
+            kivi_cache_set_fault(cache.handle, KIVI_FAULT_COPY_STALL)
+        run["outs"][s] = cache.append_decode(k, v, q, out=cache.bands.like(q))
+        cache.bands.check(f"after step {s}")
+    torch.cuda.synchronize()
+    run["outs"] = {s: o.cpu() for s, o in run["outs"].items()}
+    bad = run["outs"][2].float()
+    assert torch.isnan(bad[0, 0]).all()                          # slot (0, 0): CTA 0's first slot
+    assert torch.isfinite(bad[1]).all()
+    # every byte of every slot, and the outputs of the calls after the failed one
+    check_slots(run, [(b, h) for b in range(B) for h in range(Hkv)], {3, 4, 5})
+
+
 def test_value_queue_llama2_7b_layer_full_size():
     """B8 H32 D128 2-bit G32 R128, prompt 4096, 64 fused appends with the value queue."""
     steps = {0, 1, 63}
