@@ -817,6 +817,11 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             // between the slot's first and last unit starts, the slot still
             // counts this warp's partial, so write it empty (weight 0)
             if (u0 > 0) {
+                // (the workspace only after the preceding kernel, which may read it)
+                if (first_seg) {
+                    first_seg = false;
+                    dependency_point();
+                }
                 const long long part = gw - map_owner(wm, w0 + wm.S0);
                 for (int idx = lane; idx < NQ * (D + 4); idx += 32) {
                     const int h = idx / (D + 4), c = idx % (D + 4);
