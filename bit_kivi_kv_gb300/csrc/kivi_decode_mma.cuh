@@ -392,8 +392,14 @@ struct Cfg {
 // and lo = rn(ql*s + (qh*s - hi)), the inner residual exact, so hi + lo =
 // q*s to about 22 bits.  Lane l handles channel pairs CPL*l + j; off[j] is
 // the table offset of pair CPL*l + j (head 0, hi column).  With entries,
-// beta is returned times 2^-24, the unit of the masked codes.
-template <class C, int D, int NQ>
+// beta is returned times 2^-24, the unit of the masked codes.  KEEP: the
+// fragments are also loaded into qb; otherwise they stay in the table and the
+// MMAs read each k-step's pair from it.  Measured per instance: with one query
+// head per kv head, reading from the table (fewer registers held across the
+// pair loop) made the calls 1-2% faster (7B layer, 13B layer, 131k context,
+// the value queue, the paged cache); with grouped heads the registers were
+// faster (by 0.7%).
+template <class C, int D, int NQ, bool KEEP>
 __device__ __forceinline__ void build_q_frags(const uint8_t* entries, const float (*qf)[D],
                                               const uint32_t (*qh)[D / 2], const uint32_t (*ql)[D / 2],
                                               const int (&off)[D / 64], uint32_t* qfrag, int lane,
@@ -455,11 +461,13 @@ __device__ __forceinline__ void build_q_frags(const uint8_t* entries, const floa
         }
     }
     __syncwarp();
-    const uint4* row = reinterpret_cast<const uint4*>(qfrag + lane * C::QSTRIDE);
+    if constexpr (KEEP) {
+        const uint4* row = reinterpret_cast<const uint4*>(qfrag + lane * C::QSTRIDE);
 #pragma unroll
-    for (int v = 0; v < C::KSTEPS / 2; ++v) {
-        const uint4 x = row[v];
-        qb[4 * v] = x.x; qb[4 * v + 1] = x.y; qb[4 * v + 2] = x.z; qb[4 * v + 3] = x.w;
+        for (int v = 0; v < C::KSTEPS / 2; ++v) {
+            const uint4 x = row[v];
+            qb[4 * v] = x.x; qb[4 * v + 1] = x.y; qb[4 * v + 2] = x.z; qb[4 * v + 3] = x.w;
+        }
     }
 }
 
@@ -634,7 +642,16 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
     bool fresh = true;    // no tile of the current segment has been counted yet
     float o[KS][4];
     float zeta[NBF];
+    // the key B fragments, held in registers or read from the warp's table
+    constexpr bool QB_REGS = NQ > 1;
     uint32_t qb[2 * KS];
+    // the key B fragment of k-step kk (see build_q_frags)
+    auto qbk = [&](const int kk) -> uint2 {
+        if constexpr (QB_REGS)
+            return make_uint2(qb[2 * kk], qb[2 * kk + 1]);
+        else
+            return *reinterpret_cast<const uint2*>(qfrag + lane * C::QSTRIDE + 2 * kk);
+    };
     float beta = 0.f;
     uint32_t status = 0;  // 1: a bulk copy did not complete in time (sticky)
     uint32_t item = 0;    // ring stages this warp has consumed (stage index and phase)
@@ -851,6 +868,10 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
         // table load of its own)
         const uint8_t* kcur;
         int pidx = 0;            // paged: lane 0's entry of the page cache
+        // the pairs whose copies may be issued: paged, those whose blocks are in
+        // the page cache (a longer segment runs in parts, the cache refilled
+        // between them, so that the pair loop carries no refill)
+        int kiss = npairs;
         if constexpr (PAGED) {
             kcur = a.cache;
             if (npairs > 0) {
@@ -866,6 +887,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     pcw.last = (2 * we - 1) / C::TPB;
                 }
                 __syncwarp();
+                kiss = min(npairs, (blk0 + kPageCache) * (C::TPB / 2) - wb);
             }
         } else {
             kcur = a.cache + rslot * a.slot_bytes + (long long)((2 * wb) / C::TPB) * a.part_bytes;
@@ -878,17 +900,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             const bool kz = first || tcur == 0;
             const uint8_t* kp;
             if constexpr (PAGED) {
-                // an entry outside the pool is flagged and read from page 0 instead
-                PageCache& pcw = pc_all[warp];
-                if (pidx == kPageCache) {
-                    // past the cached blocks (a segment longer than kPageCache blocks)
-                    // (up to the segment's last block: later table entries are not the sequence's)
-                    pcw.first += kPageCache;
-                    fill_pages(pcw, pcw.trow, pcw.first, min(pcw.last - pcw.first + 1, kPageCache),
-                               a.max_blocks, a.n_pages, (long long)a.Hkv * 2 * a.part_bytes, pcw.hoff, 0, 1);
-                    pidx = 0;
-                }
-                kp = a.cache + pcw.off[pidx];
+                // (an entry outside the pool was flagged and turned into page 0)
+                kp = a.cache + pc_all[warp].off[pidx];
             } else {
                 kp = kcur;
             }
@@ -917,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             }
         };
         if (lane == 0) {
-            for (int k = 0; k < C::STAGES && k < npairs; ++k) issue_next(item + k);
+            for (int k = 0; k < C::STAGES && k < kiss; ++k) issue_next(item + k);
             // the fp16 rows this segment reads with plain loads, into L2 ahead
             // of them: its residual pairs' key and value rows (value queue:
             // ring rows) and, with the value queue, the queued values of its
@@ -1020,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 }
             }
             if (need_ksz(pr))
-                build_q_frags<C, D, NQ>(stage + C::KE, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);
+                build_q_frags<C, D, NQ, QB_REGS>(stage + C::KE, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);
             // keys: logits of tokens g, g+8 of both tiles for head i
             float sc[4];
             if constexpr (BITS == 8) {
@@ -1034,7 +1047,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     for (int kk = 0; kk < KS; ++kk) {
                         uint32_t fa[4];
                         a_frag_inline<BITS, false, W>(w, kk, fa);
-                        mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
+                        const uint2 bq = qbk(kk);
+                        mma16816(ca, fa, bq.x, bq.y);
                     }
                 }
                 {
@@ -1044,7 +1058,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     for (int kk = 0; kk < KS; ++kk) {
                         uint32_t fb[4];
                         a_frag_inline<BITS, false, W>(w, kk, fb);
-                        mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
+                        const uint2 bq = qbk(kk);
+                        mma16816(cb, fb, bq.x, bq.y);
                     }
                 }
                 // the block's zero-point term joins after the MMAs, so its
@@ -1066,8 +1081,9 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     uint32_t fa[4], fb[4];
                     a_frag<BITS, false, W>(wa, wa8, kk, fa);
                     a_frag<BITS, false, W>(wbw, wb8, kk, fb);
-                    mma16816(ca, fa, qb[2 * kk], qb[2 * kk + 1]);
-                    mma16816(cb, fb, qb[2 * kk], qb[2 * kk + 1]);
+                    const uint2 bq = qbk(kk);
+                    mma16816(ca, fa, bq.x, bq.y);
+                    mma16816(cb, fb, bq.x, bq.y);
                 }
                 // the block's zero-point term joins after the MMAs, so its
                 // reduction over the lanes runs beside them
@@ -1157,21 +1173,44 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                 }
             }
             __syncwarp();                              // every lane is done with this stage
-            if (lane == 0 && k + C::STAGES < npairs) {
+            if (lane == 0 && k + C::STAGES < kiss) {
                 fence_proxy_async();
                 issue_next(it + C::STAGES);
             }
         }
         };
-        pair_run(BoolTag<false>{}, kq);
-        if constexpr (FIFO) {
-            if (k == kq) pair_run(BoolTag<true>{}, npairs);
+        if constexpr (PAGED) {
+            for (;;) {
+                pair_run(BoolTag<false>{}, kiss);
+                if (k < kiss || kiss >= npairs) break;   // a copy timed out, or the segment is done
+                // the segment's next blocks into the page cache (up to its last
+                // block: later table entries are not the sequence's), then the
+                // next part's first copies
+                PageCache& pcw = pc_all[warp];
+                const int f = pcw.first + kPageCache;
+                fill_pages(pcw, pcw.trow, f, min(pcw.last - f + 1, kPageCache), a.max_blocks, a.n_pages,
+                           (long long)a.Hkv * 2 * a.part_bytes, pcw.hoff, lane, 32);
+                __syncwarp();
+                if (lane == 0) pcw.first = f;
+                pidx = 0;
+                kiss = min(npairs, (f + kPageCache) * (C::TPB / 2) - wb);
+                if (lane == 0) {
+                    fence_proxy_async();
+                    for (int u = k; u < k + C::STAGES && u < kiss; ++u) issue_next(item + u);
+                }
+                __syncwarp();
+            }
+        } else {
+            pair_run(BoolTag<false>{}, kq);
+            if constexpr (FIFO) {
+                if (k == kq) pair_run(BoolTag<true>{}, npairs);
+            }
         }
         if (k < npairs) {
             // a copy timed out: flag it, wait (bounded) for this warp's copies in
             // flight, and issue no more copies in this kernel
             status = 1;
-            for (int u = k; u < npairs && u < k + C::STAGES; ++u)
+            for (int u = k; u < kiss && u < k + C::STAGES; ++u)
                 mbar_wait(&bars[(item + u) % C::STAGES], ((item + u) / C::STAGES) & 1u);
         }
         item += (uint32_t)npairs;
@@ -1235,7 +1274,7 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                     return rr == nrow ? a.new_v + islot * D : vr + (long long)(((int)(32 * P) + rr) % a.R) * D;
                 return FUSED && rr == nrow ? a.new_v + islot * D : vr + (long long)rr * D;
             };
-            build_q_frags<C, D, NQ>(nullptr, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
+            build_q_frags<C, D, NQ, QB_REGS>(nullptr, qf, qhc_s, qlc_s, qoff, qfrag, lane, qb, beta);   // step 1, zero 0
             for (int rp = rb; rp < re; ++rp) {
                 float sc[4];
 #pragma unroll
@@ -1253,7 +1292,8 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
                         af[1] = okg8 ? *reinterpret_cast<const uint32_t*>(kg8 + ch) : 0u;
                         af[2] = okg ? *reinterpret_cast<const uint32_t*>(kg + ch + 8) : 0u;
                         af[3] = okg8 ? *reinterpret_cast<const uint32_t*>(kg8 + ch + 8) : 0u;
-                        mma16816(c, af, qb[2 * kk], qb[2 * kk + 1]);
+                        const uint2 bq = qbk(kk);
+                        mma16816(c, af, bq.x, bq.y);
                     }
                     sc[2 * t] = okg ? c[0] + c[1] : -INFINITY;
                     sc[2 * t + 1] = okg8 ? c[2] + c[3] : -INFINITY;
