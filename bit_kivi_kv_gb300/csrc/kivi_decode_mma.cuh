@@ -1109,10 +1109,10 @@ __global__ void __launch_bounds__(kThreads, MinCtas<D, NQ>::value)
             if (live) {
                 // small tiles (at most four words a lane): both value tiles' words
                 // are loaded before the softmax, whose shuffles then hide their
-                // latency; the entries too in the fused, paged and queue
-                // instances (plain decode calls measured 0.5-1.2% faster loading
-                // them after it, the others faster as here)
-                constexpr bool HOIST = BITS != 8 && W <= 4, HOIST_E = HOIST && FUSED;
+                // latency; the entries too in the fused and queue instances
+                // (plain decode calls measured 0.5-1.2% faster loading them after
+                // it, paged calls 1%; the other two were faster as here)
+                constexpr bool HOIST = BITS != 8 && W <= 4, HOIST_E = HOIST && FUSED && !PAGED;
                 uint32_t wvh[2][W];
                 uint2 svh[2][NBF], zvh[2][NBF];
                 if constexpr (HOIST) {
