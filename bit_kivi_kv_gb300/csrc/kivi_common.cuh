@@ -145,12 +145,12 @@ __host__ __device__ inline long long map_owner(const WorkMap& m, long long x) {
     return ((x + 1) * m.n + m.Wt - 1) / m.Wt - 1;
 }
 // partials of slot s: workers [owner of its first unit's start, owner of its last unit's start]
-__host__ __device__ inline long long slot_first_cta(const WorkMap& m, long long s) {
+__host__ __device__ inline long long slot_first_worker(const WorkMap& m, long long s) {
     return map_owner(m, s * m.Ws + m.S0);
 }
 __host__ __device__ inline int slot_parts(const WorkMap& m, long long s) {
     if (m.P + m.PR == 0) return 0;
-    return (int)(map_owner(m, s * m.Ws + unit_start(m, m.P + m.PR - 1)) - slot_first_cta(m, s) + 1);
+    return (int)(map_owner(m, s * m.Ws + unit_start(m, m.P + m.PR - 1)) - slot_first_worker(m, s) + 1);
 }
 
 // ---- launchers (defined in the .cu files; return the launch status) -------

@@ -7,8 +7,8 @@
 //
 //   keys   : S[t][n]   = sum_c code[t][c] * Qt[c][n] + beta[n]
 //            Qt[c][2h] + Qt[c][2h+1] = q_h[c] * step_c (fp16 hi + lo parts,
-//            about 22 significant bits); beta = sum_c q_h[c] * zero_c enters
-//            as the accumulator's initial value.
+//            about 22 significant bits); beta = sum_c q_h[c] * zero_c is
+//            added to the MMA's sums (the block's zero-point term).
 //   values : O^T[c][n] = sum_t code[c][t] * Pt[t][n]  (+ sum_t p_t zero_t per
 //            channel group, accumulated on the side in fp32)
 //            Pt[t][n] = p_h(t) * step(t, group) as fp16 hi + lo parts.  Column
@@ -25,10 +25,11 @@
 // query side once per slot and the 2^-24 into the softmax; for values it is
 // the output row, so the accumulators are rescaled once after the quantized
 // tiles.  The integer pipe, the busiest one, does one mask per code pair.
-// Online softmax per warp in the log2 domain; each CTA of a persistent grid
+// Online softmax per warp in the log2 domain.  Each warp of a persistent grid
 // owns a balanced, weight-proportional share of the call's work (tile pairs of
-// 32 tokens, then fp16 residual pairs); warps split it and merge by
-// log-sum-exp, one partial result per slot; a merge kernel combines them.
+// 32 tokens, then fp16 residual pairs, per (batch row, kv head) slot) and
+// writes one partial result per slot it works on; a merge kernel combines a
+// slot's partials by log-sum-exp.
 #pragma once
 
 #include <math.h>
@@ -471,13 +472,13 @@ __device__ __forceinline__ void build_q_frags(const uint8_t* entries, const floa
     }
 }
 
-// Register budget: four CTAs per SM (128 registers a thread); at head_dim 128
-// with four query heads per kv head three, which leaves enough registers.
 template <bool B>
 struct BoolTag {
     static constexpr bool value = B;
 };
 
+// Register budget: four CTAs per SM (128 registers a thread); at head_dim 128
+// with four query heads per kv head three, which leaves enough registers.
 template <int D, int NQ>
 struct MinCtas {
     static constexpr int value = (D == 128 && NQ == 4) ? 3 : 4;

@@ -131,9 +131,9 @@ int main() {
         if (!ragged) {
             // the dense helpers agree with the walk
             for (long long s = 0; s < nslots; ++s) {
-                if (slot_first_cta(wm, s) != map_owner(wm, slots[(size_t)s].w0 + wm.S0)) { std::printf("first cta\n"); return 1; }
+                if (slot_first_worker(wm, s) != map_owner(wm, slots[(size_t)s].w0 + wm.S0)) { std::printf("first worker\n"); return 1; }
                 const long long last = slots[(size_t)s].w0 + unit_start(wm, wm.P + wm.PR - 1);
-                if (slot_parts(wm, s) != (int)(map_owner(wm, last) - slot_first_cta(wm, s) + 1)) { std::printf("parts\n"); return 1; }
+                if (slot_parts(wm, s) != (int)(map_owner(wm, last) - slot_first_worker(wm, s) + 1)) { std::printf("parts\n"); return 1; }
             }
         }
     }
