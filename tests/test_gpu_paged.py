@@ -69,14 +69,17 @@ def test_every_paged_instantiation(combo):
     serve(run, [3 * G + R + 5, R // 2, G + R], 24, rng, churn_at={12}, new_lengths=[2 * G + R])
 
 
-@pytest.mark.parametrize("shape", [(128, 2, 32, 6000), (64, 4, 64, 9500)], ids=["D128b2G32", "D64b4G64"])
+@pytest.mark.parametrize("shape", [(128, 2, 32, 6000, 4), (64, 4, 64, 9500, 4), (128, 4, 128, 20000, 2)],
+                         ids=["D128b2G32", "D64b4G64", "D128b4G128nq1"])
 def test_paged_one_cta_grid_long_segments(shape):
     """A one-CTA grid: each warp's share of a sequence runs past the 128 block
-    offsets a warp caches per segment, so the cache is refilled mid-segment."""
+    offsets a warp caches per segment, so the segment runs in parts with the
+    cache refilled between them (G 128: four tile pairs a block; one query head
+    per kv head: key fragments read from the warp's table)."""
     from bit_kivi_kv_gb300.kivi import kivi_paged_set_max_ctas
-    D, bits, G, L = shape
+    D, bits, G, L, Hq = shape
     nb = (L + 40) // G + 2
-    run = PagedRun(Hq=4, Hkv=2, D=D, bits=bits, G=G, R=2 * G, max_seqs=2, max_blocks=nb, n_pages=2 * nb, seed=11)
+    run = PagedRun(Hq=Hq, Hkv=2, D=D, bits=bits, G=G, R=2 * G, max_seqs=2, max_blocks=nb, n_pages=2 * nb, seed=11)
     kivi_paged_set_max_ctas(run.cache.handle, 1)
     a, b = run.add(L), run.add(L - 700)
     for t in range(12):
