@@ -440,16 +440,16 @@ kivi_status kivi_paged_append_decode(kivi_paged_t cache, const int* seqs, int n,
 /*
  * Failure detection.  Every wait of the tensor-core decode kernel on its bulk
  * copies is bounded (about 2 s); a copy that does not complete in time marks
- * the CTA's partial results, and the merge writes NaN for every query head of
- * the slots that CTA covered (the kernel then issues no more copies, finishes
- * and returns; the context stays usable).  The paged kernel also marks a
- * block-table entry outside the pool the same way.
+ * the waiting warp's partial results, and the merge writes NaN for every query
+ * head of the slots that warp covered (the warp then issues no more copies,
+ * finishes and returns; the context stays usable).  The paged kernel also
+ * marks a block-table entry outside the pool the same way.
  *
  * Test hook: KIVI_FAULT_COPY_STALL makes the next tensor-core decode call on
  * this cache (kivi_decode_attn or kivi_append_decode) expect 16 bytes more on
  * the first copy stage of CTA 0, warp 0 than its copies bring, so that wait
  * runs out: that call takes about 4 s more and returns NaN for the heads of the
- * slots CTA 0 covers, correct outputs elsewhere.  One call only; host-only.
+ * slots that warp covers, correct outputs elsewhere.  One call only; host-only.
  */
 typedef enum {
     KIVI_FAULT_NONE = 0,
